@@ -1,0 +1,174 @@
+/*
+ * fp64 CPU oracle for multi-LoRA shrink/expand over an unsorted mixed-adapter
+ * batch.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the CPU
+ * baseline leg of the benchmark call it; the product path never does.  It
+ * shares no code, header, table or constant with the CUDA library.
+ *
+ * What it computes (one LoRA-wrapped linear layer):
+ *
+ *   "[V1] LoRA - Add triton kernels for V1" (vLLM PR 13096), section "Why do
+ *   we need a new set of kernels": V1 does not sort requests by LoRA id; the
+ *   kernels are told which input token maps to which LoRA id and load the
+ *   right tokens themselves; the rest is the SGMV low-rank matmul.
+ *   "[Tracking] Multi-LoRA Serving" (MLC-LLM), Overview: SGMV gathers each
+ *   segment's adapter weights and applies the low-rank product per request.
+ *   "[Kernel] LoRA - Enable CUDAGraphs for V1" (vLLM PR 14626): buffers are
+ *   static, sized by max_num_tokens, and the CUDA-graph pad region past the
+ *   valid tokens is not zeroed, so it must never reach an output.
+ *
+ * With m = token_lora_mapping (-1 = no adapter), L adapters, rank R,
+ * S output slices of widths N_s at offsets off_s:
+ *
+ *   metadata:  stable grouping of t in [0, n) by m[t] (bin L = no adapter)
+ *   shrink:    u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]
+ *   expand:    y[t][off_s + j] += sum_r u[s][t][r] * B_s[m[t]][r][j]
+ *
+ * for t < n with 0 <= m[t] < L only.  Everything is plain loops in the
+ * order the definition states, accumulated in double.  Tokens are
+ * independent, so the token loop may run on several host threads (OpenMP)
+ * without changing any result.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* status bits reported by the metadata oracle */
+#define ORACLE_STATUS_BAD_LORA_ID 1u   /* an id outside [-1, L) among t < n */
+#define ORACLE_STATUS_BAD_NUM_TOKENS 2u /* n outside [0, max_num_tokens] */
+#define ORACLE_STATUS_NO_MEMORY 0x80000000u /* host allocation failed */
+
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t w = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &w, sizeof f);
+    return (double)f;
+}
+
+/* Bin of one token: its LoRA id, or L when it has no (valid) adapter. */
+static int64_t bin_of(int32_t id, int64_t num_loras, uint32_t *status)
+{
+    if (id >= 0 && (int64_t)id < num_loras) return id;
+    if (id != -1) *status |= ORACLE_STATUS_BAD_LORA_ID;
+    return num_loras;
+}
+
+/*
+ * Stable counting sort of the token indices 0..n-1 by their bin.
+ *   num_tokens_per_lora   [L+1]  count of each bin (bin L = no adapter)
+ *   lora_token_start_loc  [L+2]  exclusive prefix sum, last entry = n
+ *   sorted_token_ids      [T_max] bin 0's tokens ascending, then bin 1's, ...
+ *                                 entries n..T_max-1 are -1
+ * Mapping entries at t >= n are never read.  Returns the status bits.
+ */
+uint32_t oracle_prepare_metadata(const int32_t *token_lora_mapping, int64_t num_tokens,
+                                 int64_t max_num_tokens, int64_t num_loras,
+                                 int32_t *sorted_token_ids, int32_t *num_tokens_per_lora,
+                                 int32_t *lora_token_start_loc)
+{
+    uint32_t status = 0;
+    int64_t n = num_tokens;
+    if (n < 0) { n = 0; status |= ORACLE_STATUS_BAD_NUM_TOKENS; }
+    if (n > max_num_tokens) { n = max_num_tokens; status |= ORACLE_STATUS_BAD_NUM_TOKENS; }
+
+    /* histogram */
+    for (int64_t b = 0; b <= num_loras; ++b) num_tokens_per_lora[b] = 0;
+    for (int64_t t = 0; t < n; ++t)
+        num_tokens_per_lora[bin_of(token_lora_mapping[t], num_loras, &status)] += 1;
+
+    /* exclusive prefix sum */
+    lora_token_start_loc[0] = 0;
+    for (int64_t b = 0; b <= num_loras; ++b)
+        lora_token_start_loc[b + 1] = lora_token_start_loc[b] + num_tokens_per_lora[b];
+
+    /* stable scatter: walk the tokens in order; each goes to its bin's next free slot */
+    int64_t *cursor = (int64_t *)malloc((size_t)(num_loras + 1) * sizeof *cursor);
+    if (!cursor) return status | ORACLE_STATUS_NO_MEMORY;
+    for (int64_t b = 0; b <= num_loras; ++b) cursor[b] = lora_token_start_loc[b];
+    for (int64_t t = 0; t < n; ++t) {
+        uint32_t seen = 0;
+        int64_t b = bin_of(token_lora_mapping[t], num_loras, &seen);
+        sorted_token_ids[cursor[b]++] = (int32_t)t;
+    }
+    free(cursor);
+    for (int64_t t = n; t < max_num_tokens; ++t) sorted_token_ids[t] = -1;
+    return status;
+}
+
+/*
+ * Shrink: u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]   (fp64)
+ *   x             bf16 bits, row t at x + t * x_row_stride, hidden entries
+ *   lora_a[s]     bf16 bits, [L][R][hidden] row-major
+ *   u             double, [S][max_num_tokens][R]; only rows of tokens
+ *                 t < n with 0 <= m[t] < L are written, all else untouched
+ */
+void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                   const uint16_t *const *lora_a, int64_t num_slices, int64_t rank,
+                   double scale, const int32_t *token_lora_mapping, int64_t num_tokens,
+                   int64_t num_loras, double *u, int64_t max_num_tokens, int num_threads)
+{
+    int64_t t;
+#pragma omp parallel for schedule(dynamic, 4) num_threads(num_threads)
+    for (t = 0; t < num_tokens; ++t) {
+        int32_t id = token_lora_mapping[t];
+        if (id < 0 || (int64_t)id >= num_loras) continue;
+        const uint16_t *xrow = x + t * x_row_stride;
+        for (int64_t s = 0; s < num_slices; ++s) {
+            const uint16_t *a = lora_a[s] + (int64_t)id * rank * hidden;
+            for (int64_t r = 0; r < rank; ++r) {
+                double acc = 0.0;
+                for (int64_t h = 0; h < hidden; ++h)
+                    acc += bf16_bits_to_double(xrow[h]) * bf16_bits_to_double(a[r * hidden + h]);
+                u[(s * max_num_tokens + t) * rank + r] = scale * acc;
+            }
+        }
+    }
+}
+
+/*
+ * Expand: y_out[t][off_s + j] = y_in[t][off_s + j] + sum_r u[s][t][r] * B_s[m[t]][r][j]
+ *   u             double, [S][max_num_tokens][R]
+ *   lora_b[s]     bf16 bits, [L][R][slice_width[s]] row-major
+ *   y_in          bf16 bits, row t at y_in + t * y_row_stride
+ *   y_out         double, same indexing as y_in; every element of rows
+ *                 0..max_num_tokens-1 (columns < y_row_stride) is written:
+ *                 a copy of y_in, plus the LoRA term on adapter tokens t < n
+ */
+void oracle_expand(const double *u, const uint16_t *const *lora_b, const int64_t *slice_width,
+                   int64_t num_slices, int64_t rank, const uint16_t *y_in, int64_t y_row_stride,
+                   const int32_t *token_lora_mapping, int64_t num_tokens, int64_t num_loras,
+                   double *y_out, int64_t max_num_tokens, int num_threads)
+{
+    int64_t t;
+#pragma omp parallel for schedule(dynamic, 4) num_threads(num_threads)
+    for (t = 0; t < max_num_tokens; ++t) {
+        for (int64_t c = 0; c < y_row_stride; ++c)
+            y_out[t * y_row_stride + c] = bf16_bits_to_double(y_in[t * y_row_stride + c]);
+        if (t >= num_tokens) continue;
+        int32_t id = token_lora_mapping[t];
+        if (id < 0 || (int64_t)id >= num_loras) continue;
+        int64_t offset = 0;
+        for (int64_t s = 0; s < num_slices; ++s) {
+            const uint16_t *b = lora_b[s] + (int64_t)id * rank * slice_width[s];
+            for (int64_t j = 0; j < slice_width[s]; ++j) {
+                double acc = 0.0;
+                for (int64_t r = 0; r < rank; ++r)
+                    acc += u[(s * max_num_tokens + t) * rank + r] *
+                           bf16_bits_to_double(b[r * slice_width[s] + j]);
+                y_out[t * y_row_stride + offset + j] += acc;
+            }
+            offset += slice_width[s];
+        }
+    }
+}
+
+/* Threads the OpenMP runtime would use (1 when built without OpenMP). */
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    extern int omp_get_max_threads(void);
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
