@@ -1,0 +1,179 @@
+"""Thin ctypes binding of the C ABI in ``include/gathered_rank_gemm.h``.
+
+Argument marshalling only: every step of the path runs in the CUDA kernels
+of ``libgathered_rank_gemm.so``.  There is no CPU fallback: when the library
+is missing or a tensor is not on a CUDA device, the call raises.
+
+PyTorch provides device memory and streams.  Tensors are passed as raw
+pointers; bf16 tensors must be ``torch.bfloat16``, the work is enqueued on
+``stream`` (default: the current torch stream of the tensors' device).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgathered_rank_gemm.so")
+
+LORA_OK = 0
+LORA_STATUS_BAD_LORA_ID = 0x1
+LORA_STATUS_BAD_NUM_TOKENS = 0x2
+LORA_MAX_SLICES = 3
+LORA_MAX_LORAS = 1024
+LORA_MAX_NUM_TOKENS = 1 << 22
+
+EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora_expand",
+            "lora_read_status", "lora_error_string")
+
+_lib = None
+
+
+class LoraError(RuntimeError):
+    """A C-ABI call returned a negative LORA_ERR_* code."""
+
+    def __init__(self, name: str, code: int, text: str):
+        super().__init__(f"{name} failed with {code}: {text}")
+        self.code = code
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load the CUDA library (built by ``gathered_rank_gemm_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library {path} is missing; build it with "
+                           "gathered_rank_gemm_gb300.build.build() (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    i64, i32, p, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    lib.lora_workspace_size.restype = sz
+    lib.lora_workspace_size.argtypes = [i64, i64]
+    lib.lora_prepare_metadata.restype = i32
+    lib.lora_prepare_metadata.argtypes = [p, p, i64, i64, p, p, p, p, sz, p]
+    lib.lora_shrink.restype = i32
+    lib.lora_shrink.argtypes = [p, i64, i64, p, i32, i32, ctypes.c_float, p, p, p, i64, i64, p,
+                                sz, p]
+    lib.lora_expand.restype = i32
+    lib.lora_expand.argtypes = [p, p, p, i32, i32, p, i64, p, p, i64, i64, p, sz, p]
+    lib.lora_read_status.restype = i32
+    lib.lora_read_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), p]
+    lib.lora_error_string.restype = ctypes.c_char_p
+    lib.lora_error_string.argtypes = [i32]
+    _lib = lib
+    return lib
+
+
+def _check(name: str, rc: int) -> None:
+    if rc != LORA_OK:
+        raise LoraError(name, rc, load().lora_error_string(rc).decode())
+
+
+def _stream_ptr(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t, name: str):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    return t.data_ptr()
+
+
+def _ptr_array(tensors, name):
+    arr = (ctypes.c_void_p * len(tensors))(*[_dev(t, f"{name}[{i}]") for i, t in enumerate(tensors)])
+    return arr
+
+
+# ------------------------------------------------------------------ C-ABI calls
+
+def lora_workspace_size(max_num_tokens: int, max_loras: int) -> int:
+    return int(load().lora_workspace_size(int(max_num_tokens), int(max_loras)))
+
+
+def lora_prepare_metadata(token_lora_mapping, num_tokens, max_loras: int, sorted_token_ids,
+                          num_tokens_per_lora, lora_token_start_loc, workspace, stream=None):
+    """Stable grouping of the tokens by LoRA id (see the C header)."""
+    t_max = token_lora_mapping.shape[0]
+    rc = load().lora_prepare_metadata(
+        _dev(token_lora_mapping, "token_lora_mapping"), _dev(num_tokens, "num_tokens"), t_max,
+        int(max_loras), _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(num_tokens_per_lora, "num_tokens_per_lora"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream, workspace.device))
+    _check("lora_prepare_metadata", rc)
+
+
+def lora_shrink(x, lora_a, scale: float, u, sorted_token_ids, lora_token_start_loc, workspace,
+                stream=None):
+    """u[s][t][r] = scale * x[t] . A_s[m[t]][r] for the adapter tokens."""
+    lora_a = list(lora_a)
+    arr = _ptr_array(lora_a, "lora_a")
+    num_loras, rank, hidden = lora_a[0].shape
+    rc = load().lora_shrink(
+        _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(lora_a), rank,
+        float(scale), _dev(u, "u"), _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, x.device))
+    _check("lora_shrink", rc)
+
+
+def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace, stream=None):
+    """y[t][off_s + j] += u[s][t] . B_s[m[t]][:, j] for the adapter tokens (in place)."""
+    lora_b = list(lora_b)
+    arr = _ptr_array(lora_b, "lora_b")
+    widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
+    num_loras, rank = lora_b[0].shape[:2]
+    rc = load().lora_expand(
+        _dev(u, "u"), ctypes.addressof(arr), ctypes.addressof(widths), len(lora_b), rank,
+        _dev(y, "y"), y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), y.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, y.device))
+    _check("lora_expand", rc)
+
+
+def lora_read_status(workspace, stream=None) -> int:
+    """Status bits OR-ed since the last read (synchronises the stream, clears them)."""
+    out = ctypes.c_uint32(0)
+    rc = load().lora_read_status(_dev(workspace, "workspace"), ctypes.byref(out),
+                                 _stream_ptr(stream, workspace.device))
+    _check("lora_read_status", rc)
+    return int(out.value)
+
+
+# ------------------------------------------------------------------ buffers
+
+class LoraMetadata:
+    """Device buffers of one batch's grouping (sized by max_num_tokens / max_loras)."""
+
+    def __init__(self, max_num_tokens: int, max_loras: int, device="cuda"):
+        import torch
+        self.max_num_tokens = int(max_num_tokens)
+        self.max_loras = int(max_loras)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.sorted_token_ids = torch.empty(self.max_num_tokens, **i32)
+        self.num_tokens_per_lora = torch.empty(self.max_loras + 1, **i32)
+        self.lora_token_start_loc = torch.empty(self.max_loras + 2, **i32)
+        nbytes = lora_workspace_size(self.max_num_tokens, self.max_loras)
+        if nbytes == 0:
+            raise ValueError("max_num_tokens / max_loras outside the supported range")
+        self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+    def prepare(self, token_lora_mapping, num_tokens, stream=None):
+        lora_prepare_metadata(token_lora_mapping, num_tokens, self.max_loras,
+                              self.sorted_token_ids, self.num_tokens_per_lora,
+                              self.lora_token_start_loc, self.workspace, stream)
+
+    def shrink(self, x, lora_a, scale, u, stream=None):
+        lora_shrink(x, lora_a, scale, u, self.sorted_token_ids, self.lora_token_start_loc,
+                    self.workspace, stream)
+
+    def expand(self, u, lora_b, y, stream=None):
+        lora_expand(u, lora_b, y, self.sorted_token_ids, self.lora_token_start_loc,
+                    self.workspace, stream)
+
+    def read_status(self, stream=None) -> int:
+        return lora_read_status(self.workspace, stream)

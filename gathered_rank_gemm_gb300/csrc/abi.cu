@@ -1,0 +1,161 @@
+// The C ABI: argument validation and dispatch to the kernel launchers.
+// Declarations and the full contract live in include/gathered_rank_gemm.h.
+#include <cstdint>
+
+#include "../../include/gathered_rank_gemm.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool sizes_ok(int64_t max_num_tokens, int64_t max_loras) {
+  return max_num_tokens >= 1 && max_num_tokens <= LORA_MAX_NUM_TOKENS && max_loras >= 1 &&
+         max_loras <= LORA_MAX_LORAS;
+}
+
+bool rank_ok(int rank) {
+  return rank == 8 || rank == 16 || rank == 32 || rank == 64 || rank == 128;
+}
+
+constexpr int64_t kMaxHidden = 1 << 20;
+constexpr int64_t kMaxWidth = 1 << 20;
+
+}  // namespace
+
+#pragma GCC visibility push(default)
+extern "C" {
+
+size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras) {
+  if (!sizes_ok(max_num_tokens, max_loras)) return 0;
+  return grg::workspace_bytes_needed(max_num_tokens, max_loras);
+}
+
+int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
+                          int64_t max_num_tokens, int64_t max_loras, int32_t* sorted_token_ids,
+                          int32_t* num_tokens_per_lora, int32_t* lora_token_start_loc,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (!token_lora_mapping || !num_tokens || !sorted_token_ids || !num_tokens_per_lora ||
+      !lora_token_start_loc || !workspace)
+    return LORA_ERR_NULL;
+  if (!sizes_ok(max_num_tokens, max_loras)) return LORA_ERR_SHAPE;
+  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(token_lora_mapping) & 3u) ||
+      (reinterpret_cast<uintptr_t>(num_tokens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(sorted_token_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(num_tokens_per_lora) & 3u) ||
+      (reinterpret_cast<uintptr_t>(lora_token_start_loc) & 3u))
+    return LORA_ERR_ALIGN;
+  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_WORKSPACE;
+  return grg::launch_metadata(token_lora_mapping, num_tokens, static_cast<int>(max_num_tokens),
+                              static_cast<int>(max_loras), sorted_token_ids, num_tokens_per_lora,
+                              lora_token_start_loc, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                const uint16_t* const* lora_a, int num_slices, int rank, float scale, float* u,
+                const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (!x || !lora_a || !u || !sorted_token_ids || !lora_token_start_loc || !workspace)
+    return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+  for (int s = 0; s < num_slices; ++s)
+    if (!lora_a[s]) return LORA_ERR_NULL;
+  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || hidden < 8 ||
+      hidden > kMaxHidden || (hidden % 8) != 0 || x_row_stride < hidden)
+    return LORA_ERR_SHAPE;
+  if (!aligned16(x) || (x_row_stride % 8) != 0 || !aligned16(u) || !aligned16(workspace))
+    return LORA_ERR_ALIGN;
+  for (int s = 0; s < num_slices; ++s)
+    if (!aligned16(lora_a[s])) return LORA_ERR_ALIGN;
+  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_WORKSPACE;
+  grg::ShrinkArgs a;
+  a.x = x;
+  a.x_row_stride = x_row_stride;
+  a.hidden = static_cast<int>(hidden);
+  for (int s = 0; s < 3; ++s) a.lora_a[s] = s < num_slices ? lora_a[s] : lora_a[0];
+  a.num_slices = num_slices;
+  a.rank = rank;
+  a.scale = scale;
+  a.u = u;
+  a.sorted_ids = sorted_token_ids;
+  a.starts = lora_token_start_loc;
+  a.max_num_tokens = static_cast<int>(max_num_tokens);
+  a.num_loras = static_cast<int>(max_loras);
+  a.workspace = workspace;
+  return grg::launch_shrink(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_expand(const float* u, const uint16_t* const* lora_b, const int64_t* slice_width,
+                int num_slices, int rank, uint16_t* y, int64_t y_row_stride,
+                const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (!u || !lora_b || !slice_width || !y || !sorted_token_ids || !lora_token_start_loc ||
+      !workspace)
+    return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+  int64_t total = 0;
+  for (int s = 0; s < num_slices; ++s) {
+    if (!lora_b[s]) return LORA_ERR_NULL;
+    if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0)
+      return LORA_ERR_SHAPE;
+    total += slice_width[s];
+  }
+  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || y_row_stride < total)
+    return LORA_ERR_SHAPE;
+  if (!aligned16(u) || !aligned16(y) || (y_row_stride % 8) != 0 || !aligned16(workspace))
+    return LORA_ERR_ALIGN;
+  for (int s = 0; s < num_slices; ++s)
+    if (!aligned16(lora_b[s])) return LORA_ERR_ALIGN;
+  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_WORKSPACE;
+  grg::ExpandArgs a;
+  a.u = u;
+  for (int s = 0; s < 3; ++s) {
+    a.lora_b[s] = s < num_slices ? lora_b[s] : lora_b[0];
+    a.slice_width[s] = s < num_slices ? static_cast<int>(slice_width[s]) : 0;
+  }
+  a.num_slices = num_slices;
+  a.rank = rank;
+  a.y = y;
+  a.y_row_stride = y_row_stride;
+  a.sorted_ids = sorted_token_ids;
+  a.starts = lora_token_start_loc;
+  a.max_num_tokens = static_cast<int>(max_num_tokens);
+  a.num_loras = static_cast<int>(max_loras);
+  a.workspace = workspace;
+  return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_read_status(void* workspace, uint32_t* status, void* stream) {
+  if (!workspace || !status) return LORA_ERR_NULL;
+  if (!aligned16(workspace)) return LORA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return LORA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return LORA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return LORA_ERR_CUDA;
+  *status = host;
+  return LORA_OK;
+}
+
+const char* lora_error_string(int code) {
+  switch (code) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_NULL: return "a required pointer is NULL";
+    case LORA_ERR_ALIGN: return "a pointer or row stride is not 16-byte aligned";
+    case LORA_ERR_SHAPE: return "a size is outside the supported set";
+    case LORA_ERR_WORKSPACE: return "workspace too small (see lora_workspace_size)";
+    case LORA_ERR_LAUNCH: return "CUDA kernel launch failed";
+    case LORA_ERR_CUDA: return "a CUDA runtime call failed";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

@@ -1,0 +1,110 @@
+// Host-side launch helpers: per-device caches and the cudaLaunchKernelEx call.
+#include "launch.h"
+
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+
+namespace grg {
+
+namespace {
+std::mutex g_mu;
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+struct Key {
+  int dev;
+  const void* fn;
+  long long a;
+  long long b;
+  bool operator==(const Key& o) const { return dev == o.dev && fn == o.fn && a == o.a && b == o.b; }
+};
+struct KeyHash {
+  size_t operator()(const Key& k) const {
+    size_t h = std::hash<const void*>()(k.fn);
+    h ^= std::hash<long long>()(k.a * 1000003LL + k.b) + 0x9e3779b97f4a7c15ULL + (h << 6) + (h >> 2);
+    return h ^ static_cast<size_t>(k.dev);
+  }
+};
+std::unordered_map<Key, int, KeyHash> g_smem_set;   // largest smem limit set
+std::unordered_map<Key, int, KeyHash> g_occupancy;  // blocks per SM
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+}  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return -1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+int ensure_smem_attr(const void* func, size_t smem_bytes) {
+  const int dev = current_device();
+  if (dev < 0) return -1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Key k{dev, func, 0, 0};
+  auto it = g_smem_set.find(k);
+  if (it != g_smem_set.end() && it->second >= static_cast<long long>(smem_bytes)) return 0;
+  if (smem_bytes > 48 * 1024) {
+    if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes)) != cudaSuccess)
+      return -1;
+  }
+  g_smem_set[k] = static_cast<int>(smem_bytes);
+  return 0;
+}
+
+int occupancy_blocks(const void* func, int threads, size_t smem_bytes) {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_occupancy.find(Key{dev, func, threads, static_cast<long long>(smem_bytes)});
+    if (it != g_occupancy.end()) return it->second;
+  }
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem_bytes) != cudaSuccess)
+    n = 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_occupancy[Key{dev, func, threads, static_cast<long long>(smem_bytes)}] = n;
+  return n;
+}
+
+int launch_raw(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               int cluster, void* params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  int na = 0;
+  attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (cluster > 0) {
+    attrs[na].id = cudaLaunchAttributeClusterDimension;
+    attrs[na].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attrs[na].val.clusterDim.y = 1;
+    attrs[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = na;
+  void* args[1] = {params};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
+  if (e != cudaSuccess) return -5;
+  return 0;
+}
+
+}  // namespace grg

@@ -1,0 +1,69 @@
+// Host-side launch helpers shared by the kernel launchers (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace grg {
+
+// Raises a kernel's dynamic shared-memory limit once per (device, kernel).
+int ensure_smem_attr(const void* func, size_t smem_bytes);
+
+// Streaming multiprocessors of the current device (cached).
+int device_sm_count();
+
+// Resident CTAs per SM for a kernel (cached per device, kernel, block, smem).
+int occupancy_blocks(const void* func, int threads, size_t smem_bytes);
+
+// Launches func(params) with programmatic dependent launch allowed and, when
+// cluster > 0, a 1-D thread-block cluster of that size.  Returns 0 or a
+// LORA_ERR_* code.
+int launch_raw(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               int cluster, void* params);
+
+template <typename P>
+int launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               int cluster, P* params) {
+  return launch_raw(func, grid, block, smem, stream, cluster, static_cast<void*>(params));
+}
+
+int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
+                    int num_loras, int32_t* sorted_ids, int32_t* counts, int32_t* starts,
+                    void* workspace, cudaStream_t stream);
+
+struct ShrinkArgs {
+  const void* x;
+  long long x_row_stride;
+  int hidden;
+  const void* lora_a[3];
+  int num_slices;
+  int rank;
+  float scale;
+  float* u;
+  const int32_t* sorted_ids;
+  const int32_t* starts;
+  int max_num_tokens;
+  int num_loras;
+  const void* workspace;
+};
+int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
+
+struct ExpandArgs {
+  const float* u;
+  const void* lora_b[3];
+  int slice_width[3];
+  int num_slices;
+  int rank;
+  void* y;
+  long long y_row_stride;
+  const int32_t* sorted_ids;
+  const int32_t* starts;
+  int max_num_tokens;
+  int num_loras;
+  const void* workspace;
+};
+int launch_expand(const ExpandArgs& a, cudaStream_t stream);
+
+}  // namespace grg

@@ -1,0 +1,223 @@
+// Device metadata: stable grouping of the batch's tokens by LoRA id.
+//
+// "[V1] LoRA - Add triton kernels for V1" (vLLM PR 13096), "Why do we need a
+// new set of kernels": V1 batches are not sorted by LoRA id, so the kernels
+// need, on the device, which tokens belong to which adapter.  "[Kernel] LoRA -
+// Enable CUDAGraphs for V1" (vLLM PR 14626): the map is a static buffer of
+// max_num_tokens entries and the pad rows past n hold garbage.
+//
+// One CTA of 16 warps runs a stable counting sort over bins 0..L (bin L = no
+// adapter):
+//   1. warp w takes the contiguous token range [w*seg, (w+1)*seg) and counts
+//      its tokens per bin (lanes with the same bin are grouped with
+//      __match_any_sync, the group leader adds the group size);
+//   2. per bin, an exclusive scan over the 16 warp counts gives each warp's
+//      offset inside the bin; a block scan over the bin totals gives
+//      lora_token_start_loc;
+//   3. each warp walks its range again in order; a token's slot is
+//      start[bin] + warp offset + (earlier lanes of its group in this step).
+// Warp ranges are in token order and lanes are in token order, so equal ids
+// keep ascending token order (stable).  The grid is one CTA whatever the data,
+// so the launch is graph-safe.  The kernel also writes, for each tile height
+// in {16, 32, 64, 128}, the list of (position, lora) tiles that the shrink and
+// expand kernels walk with a fixed grid.
+#include "common.cuh"
+#include "launch.h"
+
+namespace grg {
+
+constexpr int kMetaThreads = 512;
+constexpr int kMetaWarps = kMetaThreads / 32;
+
+// Exclusive scan of in[0..count) into out[0..count], out[count] = total.
+// Called by every thread of the block; in and out must not overlap.
+__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int count,
+                                     int32_t* warp_sums) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthreads = blockDim.x, nwarps = nthreads >> 5;
+  const int per = (count + nthreads - 1) / nthreads;
+  const int begin = min(tid * per, count), end = min(begin + per, count);
+  int local = 0;
+  for (int i = begin; i < end; ++i) local += in[i];
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? warp_sums[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nwarps) warp_sums[lane] = wi - w;
+  }
+  __syncthreads();
+  int run = warp_sums[warp] + incl - local;
+  for (int i = begin; i < end; ++i) {
+    out[i] = run;
+    run += in[i];
+  }
+  if (tid == nthreads - 1) out[count] = run;
+  __syncthreads();
+}
+
+struct MetaParams {
+  const int32_t* mapping;
+  const int32_t* num_tokens;
+  int max_num_tokens;
+  int num_loras;
+  int32_t* sorted_ids;
+  int32_t* counts;
+  int32_t* starts;
+  WsView ws;
+};
+
+__global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaParams p) {
+  extern __shared__ int32_t sm[];
+  __shared__ int32_t warp_sums[32];
+  __shared__ int s_n;
+  __shared__ uint32_t s_status;
+
+  const int L = p.num_loras;
+  const int nbins = L + 1;
+  int32_t* hist = sm;                        // [kMetaWarps][nbins], then warp offsets
+  int32_t* total = hist + kMetaWarps * nbins;  // [nbins]
+  int32_t* start = total + nbins;            // [nbins + 1]
+  int32_t* ntile = start + nbins + 1;        // [L]
+  int32_t* toff = ntile + L;                 // [L + 1]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (tid == 0) {
+    int n = *p.num_tokens;
+    uint32_t st = 0;
+    if (n < 0) { n = 0; st |= 2u; }
+    if (n > p.max_num_tokens) { n = p.max_num_tokens; st |= 2u; }
+    s_n = n;
+    s_status = st;
+  }
+  for (int i = tid; i < kMetaWarps * nbins; i += kMetaThreads) hist[i] = 0;
+  __syncthreads();
+  const int n = s_n;
+
+  const int seg = ((n + kMetaWarps - 1) / kMetaWarps + 31) & ~31;
+  const int lo = min(warp * seg, n), hi = min(lo + seg, n);
+  int32_t* my_hist = hist + warp * nbins;
+
+  // pass 1: per-warp histogram
+  bool bad = false;
+  for (int base = lo; base < hi; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < hi;
+    int bin = nbins;  // never a real bin: groups the idle lanes
+    if (valid) {
+      const int id = p.mapping[t];
+      if (id >= 0 && id < L) {
+        bin = id;
+      } else {
+        bin = L;
+        bad |= (id != -1);
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (valid && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
+    __syncwarp();
+  }
+  if (bad) atomicOr(&s_status, 1u);
+  __syncthreads();
+
+  // pass 2: warp offsets inside each bin, bin totals, bin starts
+  for (int b = tid; b < nbins; b += kMetaThreads) {
+    int run = 0;
+    for (int w = 0; w < kMetaWarps; ++w) {
+      const int c = hist[w * nbins + b];
+      hist[w * nbins + b] = run;
+      run += c;
+    }
+    total[b] = run;
+  }
+  __syncthreads();
+  block_exclusive_scan(total, start, nbins, warp_sums);
+
+  // pass 3: stable scatter
+  for (int base = lo; base < hi; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < hi;
+    int bin = nbins;
+    if (valid) {
+      const int id = p.mapping[t];
+      bin = (id >= 0 && id < L) ? id : L;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, bin);
+    if (valid) {
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      p.sorted_ids[start[bin] + my_hist[bin] + rank] = t;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
+    __syncwarp();
+  }
+  for (int t = n + tid; t < p.max_num_tokens; t += kMetaThreads) p.sorted_ids[t] = -1;
+  for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
+  for (int b = tid; b <= nbins; b += kMetaThreads) p.starts[b] = start[b];
+
+  // work lists for the fixed-grid kernels
+#pragma unroll
+  for (int k = 0; k < kNumTileSizes; ++k) {
+    const int rows = tile_rows_of(k);
+    for (int l = tid; l < L; l += kMetaThreads) ntile[l] = (total[l] + rows - 1) / rows;
+    __syncthreads();
+    block_exclusive_scan(ntile, toff, L, warp_sums);
+    const int count = toff[L];
+    int2* list = p.ws.lists[k];
+    for (int i = tid; i < count; i += kMetaThreads) {
+      // largest l with toff[l] <= i (l in [0, L))
+      int a = 0, b = L - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (toff[mid] <= i) a = mid; else b = mid - 1;
+      }
+      list[i] = make_int2(start[a] + (i - toff[a]) * rows, a);
+    }
+    if (tid == 0) p.ws.num_tiles[k] = count;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *p.ws.n = n;
+    if (s_status) atomicOr(p.ws.status, s_status);
+  }
+}
+
+static size_t meta_smem_bytes(int num_loras) {
+  const size_t nb = static_cast<size_t>(num_loras) + 1;
+  return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + (nb - 1) + nb);
+}
+
+int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
+                    int num_loras, int32_t* sorted_ids, int32_t* counts, int32_t* starts,
+                    void* workspace, cudaStream_t stream) {
+  MetaParams p;
+  p.mapping = mapping;
+  p.num_tokens = num_tokens;
+  p.max_num_tokens = max_num_tokens;
+  p.num_loras = num_loras;
+  p.sorted_ids = sorted_ids;
+  p.counts = counts;
+  p.starts = starts;
+  p.ws = ws_view(workspace, max_num_tokens, num_loras);
+  const size_t smem = meta_smem_bytes(num_loras);
+  if (ensure_smem_attr(reinterpret_cast<const void*>(lora_metadata_kernel), smem) != 0)
+    return -6;
+  return launch_pdl(reinterpret_cast<const void*>(lora_metadata_kernel), dim3(1),
+                    dim3(kMetaThreads), smem, stream, 1, &p);
+}
+
+}  // namespace grg

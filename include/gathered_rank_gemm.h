@@ -1,0 +1,171 @@
+/*
+ * gathered_rank_gemm — multi-LoRA shrink / expand over an unsorted,
+ * mixed-adapter token batch, for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (one LoRA-wrapped linear layer):
+ *
+ *   "[V1] LoRA - Add triton kernels for V1" (vLLM PR 13096), section "Why do
+ *   we need a new set of kernels": the batch is NOT sorted by LoRA id; the
+ *   kernels are given the token -> LoRA map and use it to load each token's
+ *   rows, then run the low-rank (SGMV-style) matmuls.  Point 1 of "Kernel Code
+ *   Change": the launch grid must not depend on the batch, so the calls can be
+ *   captured once in a CUDA graph.
+ *   "[Kernel] LoRA - Enable CUDAGraphs for V1" (vLLM PR 14626): buffers are
+ *   static, sized by max_num_tokens, and the pad rows past the valid tokens are
+ *   not zeroed, so they must never be read into an output.
+ *
+ * With m = token_lora_mapping (-1 = no adapter), n valid tokens, L adapter
+ * slots, rank R and S in {1,2,3} output slices of widths N_s at column
+ * offsets off_s = N_0 + ... + N_{s-1}:
+ *
+ *   lora_prepare_metadata: stable grouping of t in [0, n) by m[t]
+ *   lora_shrink:  u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]   (fp32 out)
+ *   lora_expand:  y[t][off_s + j] = bf16( y[t][off_s + j]
+ *                                       + sum_r u[s][t][r] * B_s[m[t]][r][j] )
+ *
+ * for t < n with 0 <= m[t] < L.  Rows of tokens with m[t] = -1 and rows t >= n
+ * are never read from x and never read from or written to u and y.
+ *
+ * Conventions for every call:
+ *  - Every array argument is a DEVICE pointer owned by the caller, except the
+ *    small per-slice arrays (lora_a, lora_b, slice_width), which are HOST
+ *    arrays of num_slices entries read during the call (their device pointers
+ *    are copied into the kernel parameters).  The library never allocates,
+ *    frees or synchronises (lora_read_status excepted).
+ *  - bf16 data is passed as uint16_t bit patterns (IEEE bfloat16).
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) on the current device, so every call can be captured into a CUDA
+ *    graph.  The number of valid tokens n lives in device memory, so one
+ *    captured graph serves every n <= max_num_tokens.
+ *  - Kernels are launched with programmatic dependent launch enabled; each
+ *    one waits for the preceding work on the stream before touching memory.
+ *  - Return value: LORA_OK when the work was enqueued, a negative LORA_ERR_*
+ *    code when an argument was rejected (nothing is launched) or the launch
+ *    failed.  Problems that only the data reveals (a LoRA id outside [-1, L),
+ *    n outside [0, max_num_tokens]) cannot be reported synchronously: they set
+ *    bits in the status word inside the workspace (lora_read_status), and the
+ *    offending tokens are treated as having no adapter / n is clamped.
+ */
+#ifndef GATHERED_RANK_GEMM_H
+#define GATHERED_RANK_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_OK 0
+#define LORA_ERR_NULL (-1)       /* a required pointer is NULL */
+#define LORA_ERR_ALIGN (-2)      /* a pointer or row stride breaks the 16-byte rule */
+#define LORA_ERR_SHAPE (-3)      /* a size is outside the supported set */
+#define LORA_ERR_WORKSPACE (-4)  /* workspace too small */
+#define LORA_ERR_LAUNCH (-5)     /* the CUDA launch failed (cudaGetLastError) */
+#define LORA_ERR_CUDA (-6)       /* another CUDA runtime call failed */
+
+#define LORA_STATUS_BAD_LORA_ID 0x1u     /* some m[t], t < n, was outside [-1, L) */
+#define LORA_STATUS_BAD_NUM_TOKENS 0x2u  /* n was outside [0, max_num_tokens]; clamped */
+
+#define LORA_MAX_SLICES 3
+#define LORA_MAX_LORAS 1024
+#define LORA_MAX_NUM_TOKENS (1 << 22)
+
+/*
+ * Bytes of device workspace that lora_prepare_metadata fills and lora_shrink /
+ * lora_expand read: a status word, the clamped n and per-tile work lists for
+ * the fixed-grid kernels.  Grows as max_num_tokens / 16 + 4 * max_loras
+ * entries of 8 bytes (about 22 KB at 8192 tokens and 128 LoRAs).  Returns 0
+ * for sizes outside the supported range.
+ */
+size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras);
+
+/*
+ * Stable grouping of the batch's tokens by LoRA id ("[V1] LoRA - Add triton
+ * kernels for V1", "Why do we need a new set of kernels": V1 keeps the batch
+ * unsorted, so the grouping is computed on the device from the token -> LoRA
+ * map; "[Kernel] LoRA - Enable CUDAGraphs for V1": the map is a static
+ * max_num_tokens buffer).  One single-CTA histogram / prefix-sum / stable
+ * scatter; the grid does not depend on the data.
+ *
+ *   token_lora_mapping   int32[max_num_tokens]; entries t >= n are never read
+ *   num_tokens           device int32: n
+ *   sorted_token_ids     int32[max_num_tokens] out: tokens of LoRA 0 in
+ *                        ascending order, then LoRA 1, ..., then the tokens
+ *                        without an adapter; entries n.. are -1
+ *   num_tokens_per_lora  int32[max_loras + 1] out: entry L counts tokens
+ *                        without an adapter
+ *   lora_token_start_loc int32[max_loras + 2] out: exclusive prefix sum of the
+ *                        counts; entry L+1 equals n
+ *   workspace            lora_workspace_size(max_num_tokens, max_loras) bytes,
+ *                        16-byte aligned; its status word is OR-ed (never
+ *                        cleared here) and the rest is overwritten
+ * Sizes: 1 <= max_num_tokens <= LORA_MAX_NUM_TOKENS, 1 <= max_loras <= LORA_MAX_LORAS.
+ */
+int lora_prepare_metadata(const int32_t *token_lora_mapping, const int32_t *num_tokens,
+                          int64_t max_num_tokens, int64_t max_loras,
+                          int32_t *sorted_token_ids, int32_t *num_tokens_per_lora,
+                          int32_t *lora_token_start_loc, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/*
+ * Shrink ("[V1] LoRA - Add triton kernels for V1": gather each token's input
+ * row through the token -> LoRA information and multiply by its adapter's A):
+ *   u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]     (bf16 in, fp32 out)
+ *
+ *   x                bf16[max_num_tokens][x_row_stride], hidden columns used
+ *   lora_a           HOST array of num_slices device pointers, each
+ *                    bf16[max_loras][rank][hidden] row-major
+ *   u                fp32[num_slices][max_num_tokens][rank] out; only rows of
+ *                    adapter tokens t < n are written
+ *   sorted_token_ids, lora_token_start_loc, workspace: from lora_prepare_metadata
+ *                    with the same max_num_tokens / max_loras
+ * Sizes: hidden a multiple of 8, rank in {8, 16, 32, 64, 128}, 1 <= num_slices
+ * <= 3; x, every A_s and u 16-byte aligned, x_row_stride a multiple of 8 and
+ * >= hidden.  Accumulation is fp32 (tensor cores, bf16 operands).
+ */
+int lora_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                const uint16_t *const *lora_a, int num_slices, int rank, float scale,
+                float *u, const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * Expand ("[V1] LoRA - Add triton kernels for V1": same token loading, rank ->
+ * width matmul added into the layer's output):
+ *   y[t][off_s + j] = bf16( float(y[t][off_s + j]) + sum_r u[s][t][r] * B_s[m[t]][r][j] )
+ * one round-to-nearest-even per element; y is updated in place.
+ *
+ *   u                fp32[num_slices][max_num_tokens][rank] (from lora_shrink)
+ *   lora_b           HOST array of num_slices device pointers, each
+ *                    bf16[max_loras][rank][slice_width[s]] row-major
+ *   slice_width      HOST array of num_slices widths, each a multiple of 8
+ *   y                bf16[max_num_tokens][y_row_stride] in/out; slice s covers
+ *                    columns off_s .. off_s + slice_width[s] - 1
+ *   sorted_token_ids, lora_token_start_loc, workspace: from lora_prepare_metadata
+ * Sizes: y_row_stride a multiple of 8 and >= the sum of the widths; rank in
+ * {8, 16, 32, 64, 128}; u, y and every B_s 16-byte aligned.  The rank
+ * contraction runs on tensor cores with u split into two bf16 terms
+ * (high + low part), so u keeps about 16 significant bits.
+ */
+int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *slice_width,
+                int num_slices, int rank, uint16_t *y, int64_t y_row_stride,
+                const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                size_t workspace_bytes, void *stream);
+
+/*
+ * Copies the workspace's status word (LORA_STATUS_* bits OR-ed by every
+ * lora_prepare_metadata since the last read) to *status, then clears it.
+ * Synchronises `stream`.  Not capturable in a CUDA graph.
+ */
+int lora_read_status(void *workspace, uint32_t *status, void *stream);
+
+/* Static text for a LORA_OK / LORA_ERR_* code. */
+const char *lora_error_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GATHERED_RANK_GEMM_H */

@@ -1,0 +1,185 @@
+"""Shared helpers for the GPU parity tests: moving seeded inputs to the device,
+guarded buffers, running the library path and the oracle, tolerance checks."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from gathered_rank_gemm_gb300 import binding
+from gathered_rank_gemm_gb300 import workloads as W
+
+U_SENTINEL_BITS = 0x7FC0DEAD   # fp32 NaN pattern pre-filled in u
+GUARD_BYTES = 256
+RTOL = 1e-2
+ATOL = 1e-2
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def bf16_dev(a: np.ndarray, dev):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+
+def bits_of(t) -> np.ndarray:
+    torch = torch_mod()
+    return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class Guarded:
+    """A device buffer with sentinel-filled guard bands before and after."""
+
+    def __init__(self, shape, dtype, dev, fill_bits: int | None = None, init=None):
+        torch = torch_mod()
+        self.dtype = dtype
+        esz = torch.empty((), dtype=dtype).element_size()
+        self.g = GUARD_BYTES // esz
+        numel = int(np.prod(shape))
+        self.full = torch.empty(numel + 2 * self.g, dtype=dtype, device=dev)
+        int_dt = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[esz]
+        self.full.view(int_dt).fill_(0x5A5A if esz == 2 else 0x5A)
+        if esz == 4:
+            self.full.view(torch.int32).fill_(0x5A5A5A5A)
+        self.view = self.full[self.g:self.g + numel].view(*shape)
+        if fill_bits is not None:
+            self.view.view(int_dt).fill_(fill_bits - (1 << (8 * esz)) if fill_bits >= 1 << (8 * esz - 1) else fill_bits)
+        if init is not None:
+            self.view.copy_(init)
+        self._int_dt = int_dt
+        self.guard_before = self.full[:self.g].view(int_dt).clone()
+        self.guard_after = self.full[self.g + numel:].view(int_dt).clone()
+
+    def guards_intact(self) -> bool:
+        torch = torch_mod()
+        numel = self.view.numel()
+        a = torch.equal(self.full[:self.g].view(self._int_dt), self.guard_before)
+        b = torch.equal(self.full[self.g + numel:].view(self._int_dt), self.guard_after)
+        return bool(a and b)
+
+
+class DeviceCase:
+    """One layer's inputs on the device plus the metadata buffers (guarded)."""
+
+    def __init__(self, shape: W.LayerShape, mapping: np.ndarray, layer: W.Layer, dev,
+                 x_pad: int = 0, y_pad: int = 0):
+        torch = torch_mod()
+        self.shape, self.mapping_np, self.layer, self.dev = shape, mapping, layer, dev
+        T, L = shape.max_num_tokens, shape.max_loras
+        self.mapping = torch.from_numpy(mapping).to(dev)
+        self.n = torch.tensor([shape.num_tokens], dtype=torch.int32, device=dev)
+        xs = np.zeros((T, shape.hidden + x_pad), np.uint16)
+        xs[:, :shape.hidden] = layer.x
+        if x_pad:
+            xs[:, shape.hidden:] = W.BF16_QNAN_PAYLOAD   # never read
+        self.x_full = bf16_dev(xs, dev)
+        self.x = self.x_full[:, :shape.hidden]
+        ys = np.zeros((T, shape.out_width + y_pad), np.uint16)
+        ys[:, :shape.out_width] = layer.y
+        if y_pad:
+            ys[:, shape.out_width:] = W.BF16_Y_SENTINEL
+        self.y_in_bits = ys
+        self.y = Guarded((T, shape.out_width + y_pad), torch.bfloat16, dev, init=bf16_dev(ys, dev))
+        self.y_view = self.y.view[:, :shape.out_width]
+        self.a = [bf16_dev(v, dev) for v in layer.lora_a]
+        self.b = [bf16_dev(v, dev) for v in layer.lora_b]
+        self.u = Guarded((shape.num_slices, T, shape.rank), torch.float32, dev,
+                         fill_bits=U_SENTINEL_BITS)
+        self.sorted = Guarded((T,), torch.int32, dev, fill_bits=0x11111111)
+        self.counts = Guarded((L + 1,), torch.int32, dev, fill_bits=0x22222222)
+        self.starts = Guarded((L + 2,), torch.int32, dev, fill_bits=0x33333333)
+        ws_bytes = binding.lora_workspace_size(T, L)
+        self.ws = Guarded((ws_bytes,), torch.uint8, dev, fill_bits=0)
+
+    def prepare(self, stream=None):
+        binding.lora_prepare_metadata(self.mapping, self.n, self.shape.max_loras,
+                                      self.sorted.view, self.counts.view, self.starts.view,
+                                      self.ws.view, stream)
+
+    def shrink(self, stream=None):
+        binding.lora_shrink(self.x, self.a, self.shape.scale, self.u.view, self.sorted.view,
+                            self.starts.view, self.ws.view, stream)
+
+    def expand(self, stream=None, u=None):
+        binding.lora_expand(self.u.view if u is None else u, self.b, self.y_view,
+                            self.sorted.view, self.starts.view, self.ws.view, stream)
+
+    def run(self):
+        self.prepare()
+        self.shrink()
+        self.expand()
+        torch_mod().cuda.synchronize()
+
+    def guards_intact(self):
+        return all(g.guards_intact() for g in (self.y, self.u, self.sorted, self.counts,
+                                                self.starts, self.ws))
+
+
+def within_tol(gpu: np.ndarray, ref: np.ndarray):
+    """Per-element |gpu - ref| <= 1e-2 + 1e-2 |ref|; returns (ok, worst ratio)."""
+    err = np.abs(gpu - ref)
+    bound = ATOL + RTOL * np.abs(ref)
+    ratio = float(np.max(err / bound)) if err.size else 0.0
+    return bool(np.all(err <= bound)), ratio
+
+
+def lora_rows(mapping: np.ndarray, n: int, L: int) -> np.ndarray:
+    m = mapping[:n]
+    return np.nonzero((m >= 0) & (m < L))[0]
+
+
+def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None):
+    """Runs the path and checks metadata (bit-exact), u and y (tolerance),
+    untouched rows (bit-exact) and guard bands.  Returns diagnostics."""
+    sh, lay = case.shape, case.layer
+    T, L, n = sh.max_num_tokens, sh.max_loras, sh.num_tokens
+    case.run()
+    s_ref, c_ref, st_ref, status_ref = oracle.prepare_metadata(case.mapping_np, n, L)
+    assert np.array_equal(case.sorted.view.cpu().numpy(), s_ref), "sorted_token_ids differ"
+    assert np.array_equal(case.counts.view.cpu().numpy(), c_ref), "num_tokens_per_lora differ"
+    assert np.array_equal(case.starts.view.cpu().numpy(), st_ref), "lora_token_start_loc differ"
+    assert case.guards_intact(), "a guard band was overwritten"
+
+    rows = lora_rows(case.mapping_np, n, L)
+    if sample_rows is not None and len(rows) > sample_rows:
+        rows = np.sort(np.random.default_rng(5).choice(rows, sample_rows, replace=False))
+    keep = np.zeros(T, bool)
+    keep[lora_rows(case.mapping_np, n, L)] = True
+
+    u_gpu = case.u.view.cpu().numpy()
+    u_bits = u_gpu.view(np.uint32)
+    assert np.all(u_bits[:, ~keep, :] == U_SENTINEL_BITS), "u rows without adapter were written"
+
+    # oracle on the selected rows only (others: mapping -1 so the oracle skips them)
+    m_sel = np.full(T, -1, np.int32)
+    m_sel[rows] = case.mapping_np[rows]
+    u_ref = oracle.shrink(lay.x, lay.lora_a, sh.scale, m_sel, n, L,
+                          u_init=np.zeros((sh.num_slices, T, sh.rank)))
+    ok_u, r_u = within_tol(u_gpu[:, rows].astype(np.float64), u_ref[:, rows])
+    assert ok_u, f"u differs from the oracle (worst err/bound {r_u:.3f})"
+
+    y_gpu_bits = bits_of(case.y.view)
+    y_gpu = oracle.bf16_bits_to_f64(y_gpu_bits)
+    y_in = case.y_in_bits
+    untouched = ~keep
+    assert np.array_equal(y_gpu_bits[untouched], y_in[untouched]), "y rows without adapter changed"
+    if y_in.shape[1] > sh.out_width:
+        assert np.array_equal(y_gpu_bits[:, sh.out_width:], y_in[:, sh.out_width:]), \
+            "y columns past the slices changed"
+    y_in_used = np.ascontiguousarray(y_in[:, :sh.out_width])
+    # (i) end to end: oracle u in fp64
+    y_ref = oracle.expand(u_ref, lay.lora_b, y_in_used, m_sel, n, L)
+    ok_y, r_y = within_tol(y_gpu[rows, :sh.out_width], y_ref[rows])
+    assert ok_y, f"y differs from the oracle end to end (worst err/bound {r_y:.3f})"
+    # (ii) expand alone: the GPU's own u fed to the oracle, zero base output
+    zero_y = np.zeros_like(y_in_used)
+    d_ref = oracle.expand(np.nan_to_num(u_gpu.astype(np.float64)), lay.lora_b, zero_y, m_sel, n, L)
+    d_gpu = y_gpu[rows, :sh.out_width] - oracle.bf16_bits_to_f64(y_in_used[rows])
+    # the GPU delta carries the final bf16 rounding of y: bound it by half an ulp of y
+    ulp = np.abs(y_gpu[rows, :sh.out_width]) * 2.0 ** -8
+    err = np.abs(d_gpu - d_ref[rows])
+    assert np.all(err <= ATOL + RTOL * np.abs(d_ref[rows]) + ulp), \
+        "expand delta differs from the oracle's expand of the GPU u"
+    return dict(rows=len(rows), worst_u=r_u, worst_y=r_y)

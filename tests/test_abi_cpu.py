@@ -1,0 +1,150 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every
+function the header declares; host-side validation rejects bad arguments
+before any CUDA call (so these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gathered_rank_gemm_gb300 import binding
+from gathered_rank_gemm_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gathered_rank_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("lora_prepare_metadata", "lora_shrink", "lora_expand", "lora_workspace_size",
+              "lora_read_status", "lora_error_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert set(binding.EXPORTED) <= set(declared_functions())
+
+
+def test_only_the_abi_is_exported():
+    out = os.popen(f"nm -D --defined-only {binding.LIB_PATH}").read()
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    ours = {s for s in syms if "grg" in s or s.startswith("lora_")}
+    assert ours == set(declared_functions())
+
+
+def test_workspace_size(lib):
+    assert binding.lora_workspace_size(8192, 128) > 0
+    assert binding.lora_workspace_size(8192, 128) % 256 == 0
+    assert binding.lora_workspace_size(0, 4) == 0
+    assert binding.lora_workspace_size(64, 0) == 0
+    assert binding.lora_workspace_size(64, binding.LORA_MAX_LORAS + 1) == 0
+    assert binding.lora_workspace_size(binding.LORA_MAX_NUM_TOKENS + 1, 4) == 0
+    # grows with both sizes, and covers the four tile lists
+    small = binding.lora_workspace_size(64, 4)
+    assert binding.lora_workspace_size(128, 4) > small
+    assert binding.lora_workspace_size(64, 8) > small
+    entries = sum((64 + r - 1) // r + 4 for r in (16, 32, 64, 128))
+    assert small >= 64 + 8 * entries
+
+
+def test_error_strings(lib):
+    for code in range(0, -7, -1):
+        assert lib.lora_error_string(code)
+    assert b"unknown" in lib.lora_error_string(-99)
+
+
+# Fake, never-dereferenced pointer values: validation must reject the call
+# before anything reaches the GPU.
+P16 = 0x10000      # 16-byte aligned
+PODD = 0x10002     # misaligned
+
+
+def _arr(*vals):
+    return (ctypes.c_void_p * len(vals))(*vals)
+
+
+def test_prepare_metadata_validation(lib):
+    f = lib.lora_prepare_metadata
+    assert f(None, P16, 64, 4, P16, P16, P16, P16, 1 << 20, None) == -1
+    assert f(P16, P16, 0, 4, P16, P16, P16, P16, 1 << 20, None) == -3
+    assert f(P16, P16, 64, 0, P16, P16, P16, P16, 1 << 20, None) == -3
+    assert f(P16, P16, 64, 4, P16, P16, P16, PODD, 1 << 20, None) == -2
+    assert f(P16, P16, 64, 4, P16, P16, P16, P16, 16, None) == -4
+
+
+def test_shrink_validation(lib):
+    f = lib.lora_shrink
+    a = _arr(P16)
+    ws = 1 << 20
+    args = dict(x=P16, stride=512, hidden=512, a=ctypes.addressof(a), s=1, r=8, scale=1.0,
+                u=P16, sorted=P16, starts=P16, T=64, L=4, ws=P16, wsb=ws)
+
+    def call(**kw):
+        d = dict(args, **kw)
+        return f(d["x"], d["stride"], d["hidden"], d["a"], d["s"], d["r"], d["scale"], d["u"],
+                 d["sorted"], d["starts"], d["T"], d["L"], d["ws"], d["wsb"], None)
+
+    assert call(x=None) == -1
+    assert call(a=None) == -1
+    assert call(a=ctypes.addressof(_arr(None))) == -1
+    assert call(s=0) == -3 and call(s=4) == -3
+    assert call(r=12) == -3 and call(r=256) == -3
+    assert call(hidden=500, stride=504) == -3
+    assert call(stride=256) == -3
+    assert call(x=PODD) == -2
+    assert call(stride=514) == -2
+    assert call(u=PODD) == -2
+    assert call(a=ctypes.addressof(_arr(PODD))) == -2
+    assert call(wsb=8) == -4
+
+
+def test_expand_validation(lib):
+    f = lib.lora_expand
+    b = _arr(P16, P16)
+    w = (ctypes.c_int64 * 2)(512, 512)
+
+    def call(u=P16, bp=None, wp=None, s=2, r=16, y=P16, ystride=1024, T=64, L=4, ws=P16,
+             wsb=1 << 20):
+        return f(u, ctypes.addressof(b) if bp is None else bp,
+                 ctypes.addressof(w) if wp is None else wp, s, r, y, ystride, P16, P16, T, L, ws,
+                 wsb, None)
+
+    assert call(u=None) == -1
+    assert call(y=None) == -1
+    assert call(wp=0) == -1
+    assert call(s=0) == -3
+    assert call(r=7) == -3
+    assert call(ystride=1000) == -3
+    assert call(ystride=1028) == -2
+    assert call(y=PODD) == -2
+    bad_w = (ctypes.c_int64 * 2)(512, 500)
+    assert call(wp=ctypes.addressof(bad_w)) == -3
+    assert call(wsb=8) == -4
+
+
+def test_read_status_validation(lib):
+    st = ctypes.c_uint32(0)
+    assert lib.lora_read_status(None, ctypes.byref(st), None) == -1
+    assert lib.lora_read_status(P16, None, None) == -1
+    assert lib.lora_read_status(PODD, ctypes.byref(st), None) == -2
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(4, 8, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding.lora_prepare_metadata(x[0], x[0, :1], 4, x[0], x[0], x[0], x[0])

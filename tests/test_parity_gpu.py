@@ -1,0 +1,314 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Metadata is compared bit-exactly over whole buffers; u and y per element
+within |gpu - oracle| <= 1e-2 + 1e-2 |oracle|; rows without an adapter, pad
+rows, columns past the slices and guard bands bit-exactly against their
+pre-call contents.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gathered_rank_gemm_gb300 import binding
+from gathered_rank_gemm_gb300 import workloads as W
+
+from helpers import (DeviceCase, U_SENTINEL_BITS, bf16_dev, bits_of, check_case, lora_rows,
+                     within_tol)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gathered_rank_gemm_gb300 import build
+    build.build()
+    binding.load()
+    return torch.device("cuda:0")
+
+
+def make_case(shape, dev, seed=0, **kw):
+    rng = np.random.default_rng(seed)
+    mapping = W.make_mapping(shape, rng)
+    layer = W.make_layer(shape, rng)
+    return DeviceCase(shape, mapping, layer, dev, **kw)
+
+
+# ------------------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("name", ["tiny", "decode_qkv", "chunked_prefill", "mlp_gate_up",
+                                  "down_proj_graph"])
+def test_named_workload_full_size(name, dev):
+    wl = W.make_workload(name)
+    case = DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev)
+    info = check_case(case, sample_rows=None if name in ("tiny", "decode_qkv") else 600)
+    assert case.ws.view[:4].view(torch.int32).item() == 0   # status clean
+    print(name, info)
+
+
+# ------------------------------------------------------------ shapes and ragged edges
+
+SHAPES = [
+    # (T, n, H, widths, L, R, mapping)
+    (48, 48, 520, (264,), 3, 8, "uniform"),            # H not a multiple of 64, width not of 256
+    (100, 77, 136, (40, 24, 16), 5, 16, "uniform"),    # three unequal slices, pad rows
+    (300, 300, 1000, (72, 200), 7, 32, "zipf"),        # rank 32, two slices
+    (130, 129, 256, (128,), 2, 64, "uniform"),         # rank 64
+    (70, 70, 384, (96, 96, 96), 3, 128, "uniform"),    # rank 128, three slices (S*R = 384)
+    (64, 64, 64, (8,), 1, 8, "uniform"),               # one LoRA, narrowest slice
+    (1, 1, 8, (8,), 1, 8, "all_zero"),                 # a single token, smallest sizes
+    (2048, 1500, 512, (512,), 16, 16, "runs"),         # long runs, pad rows
+]
+
+
+@pytest.mark.parametrize("T,n,H,widths,L,R,kind", SHAPES)
+def test_ragged_and_edge_shapes(T, n, H, widths, L, R, kind, dev):
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, mapping=kind, neg_prob=0.15)
+    case = make_case(shape, dev, seed=T + H + R)
+    check_case(case)
+
+
+@pytest.mark.parametrize("R", [8, 16, 32, 64, 128])
+@pytest.mark.parametrize("S", [1, 2, 3])
+def test_every_rank_and_slice_count(R, S, dev):
+    shape = W.custom_shape(max_num_tokens=96, num_tokens=90, hidden=192, slice_widths=(64,) * S,
+                           max_loras=4, rank=R, mapping="uniform", neg_prob=0.1)
+    check_case(make_case(shape, dev, seed=R * 10 + S))
+
+
+def test_strided_rows_are_respected(dev):
+    shape = W.custom_shape(max_num_tokens=80, num_tokens=80, hidden=256, slice_widths=(128, 64),
+                           max_loras=3, rank=16)
+    case = make_case(shape, dev, seed=3, x_pad=40, y_pad=24)
+    check_case(case)
+
+
+def test_no_tokens_changes_nothing(dev):
+    shape = W.custom_shape(max_num_tokens=64, num_tokens=0, hidden=128, slice_widths=(64,),
+                           max_loras=2, rank=8)
+    case = make_case(shape, dev)
+    check_case(case)
+    assert np.all(case.sorted.view.cpu().numpy() == -1)
+
+
+def test_all_tokens_without_adapter(dev):
+    shape = W.custom_shape(max_num_tokens=64, num_tokens=64, hidden=128, slice_widths=(64,),
+                           max_loras=2, rank=8, neg_prob=1.0)
+    check_case(make_case(shape, dev))
+
+
+def test_many_loras_uses_every_bin(dev):
+    shape = W.custom_shape(max_num_tokens=4096, num_tokens=4096, hidden=64, slice_widths=(64,),
+                           max_loras=1024, rank=8, neg_prob=0.05)
+    check_case(make_case(shape, dev, seed=9), sample_rows=500)
+
+
+# ------------------------------------------------------------ exact integer cases
+
+def _int_case(dev, T, H, sparse_k=None, seed=0):
+    rng = np.random.default_rng(seed)
+    L, R, widths = 3, 8, (16, 8)
+    if sparse_k is None:
+        xi = rng.choice([-2, 0, 2], size=(T, H))
+    else:
+        xi = np.zeros((T, H), np.int64)
+        for t in range(T):
+            xi[t, rng.choice(H, sparse_k, replace=False)] = rng.choice([-2, 2], size=sparse_k)
+    ai = [rng.choice([-1, 0, 1], size=(L, R, H)) for _ in widths]
+    bi = [rng.choice([-1, 0, 1], size=(L, R, w)) for w in widths]
+    yi = rng.integers(-8, 9, size=(T, sum(widths)))
+    m = rng.integers(-1, L, size=T).astype(np.int32)
+    f = lambda a: W.f32_to_bf16_bits(np.asarray(a, np.float32))
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=T, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, scale=0.5)
+    layer = W.Layer(x=f(xi), lora_a=[f(v) for v in ai], lora_b=[f(v) for v in bi], y=f(yi))
+    return DeviceCase(shape, m, layer, dev), (xi, ai, bi, yi, m)
+
+
+@pytest.mark.parametrize("T,H,sparse", [(24, 16, None), (64, 4096, 16)])
+def test_small_integer_inputs_are_bit_exact(T, H, sparse, dev):
+    case, (xi, ai, bi, yi, m) = _int_case(dev, T, H, sparse, seed=H)
+    case.run()
+    u = case.u.view.cpu().numpy()
+    y = oracle.bf16_bits_to_f64(bits_of(case.y.view))
+    u_ref = oracle.shrink(case.layer.x, case.layer.lora_a, 0.5, m, T, 3,
+                          u_init=np.zeros((2, T, 8)))
+    y_ref = oracle.expand(u_ref, case.layer.lora_b, case.layer.y, m, T, 3)
+    rows = lora_rows(m, T, 3)
+    assert np.array_equal(u[:, rows].astype(np.float64), u_ref[:, rows])
+    assert np.array_equal(y, y_ref)
+
+
+# ------------------------------------------------------------ invariants
+
+def test_one_adapter_batch_equals_dense_fp32_torch(dev):
+    T, H, N, R = 200, 1024, 768, 16
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=T, hidden=H, slice_widths=(N,),
+                           max_loras=2, rank=R, mapping="all_zero", scale=0.75)
+    case = make_case(shape, dev, seed=4)
+    x32 = case.x.float()
+    a32 = case.a[0][0].float()
+    b32 = case.b[0][0].float()
+    y0 = case.y_view.float().clone()
+    case.run()
+    u_dense = 0.75 * (x32 @ a32.T)
+    y_dense = y0 + u_dense @ b32
+    u = case.u.view[0]
+    assert torch.all((u - u_dense).abs() <= 1e-2 + 1e-2 * u_dense.abs())
+    y = case.y_view.float()
+    assert torch.all((y - y_dense).abs() <= 1e-2 + 1e-2 * y_dense.abs())
+
+
+def test_zero_base_output_isolates_the_delta(dev):
+    shape = W.CONFIGS["decode_qkv"]
+    wl = W.make_workload(shape)
+    layer = wl.layers[0]
+    layer = W.Layer(x=layer.x, lora_a=layer.lora_a, lora_b=layer.lora_b,
+                    y=np.zeros_like(layer.y))
+    case = DeviceCase(shape, wl.mapping, layer, dev)
+    case.run()
+    rows = lora_rows(wl.mapping, shape.num_tokens, shape.max_loras)
+    u_ref = oracle.shrink(layer.x, layer.lora_a, 1.0, wl.mapping, shape.num_tokens, 4,
+                          u_init=np.zeros((3, shape.max_num_tokens, 8)))
+    d_ref = oracle.expand(u_ref, layer.lora_b, layer.y, wl.mapping, shape.num_tokens, 4)
+    d = oracle.bf16_bits_to_f64(bits_of(case.y.view))
+    ok, worst = within_tol(d[rows], d_ref[rows])
+    assert ok
+    # the delta is small (std ~0.07): also hold it to bf16 precision, relative
+    rel = np.abs(d[rows] - d_ref[rows]) / (np.abs(d_ref[rows]) + 1e-3)
+    assert np.median(rel) < 4e-3
+
+
+def test_token_permutation_permutes_the_outputs(dev):
+    shape = W.custom_shape(max_num_tokens=256, num_tokens=256, hidden=512, slice_widths=(256,),
+                           max_loras=4, rank=16)
+    rng = np.random.default_rng(17)
+    m = W.make_mapping(shape, rng)
+    layer = W.make_layer(shape, rng)
+    perm = rng.permutation(256)
+    c1 = DeviceCase(shape, m, layer, dev)
+    c1.run()
+    lp = W.Layer(x=layer.x[perm], lora_a=layer.lora_a, lora_b=layer.lora_b, y=layer.y[perm])
+    c2 = DeviceCase(shape, np.ascontiguousarray(m[perm]), lp, dev)
+    c2.run()
+    y1 = c1.y_view.float().cpu().numpy()[perm]
+    y2 = c2.y_view.float().cpu().numpy()
+    assert np.all(np.abs(y1 - y2) <= 1e-2 + 1e-2 * np.abs(y1))
+
+
+def test_bad_ids_and_bad_n_set_status_bits(dev):
+    shape = W.custom_shape(max_num_tokens=64, num_tokens=64, hidden=64, slice_widths=(64,),
+                           max_loras=4, rank=8)
+    rng = np.random.default_rng(2)
+    m = W.make_mapping(shape, rng)
+    m[[3, 17, 40]] = [4, 1000, -5]          # out of range: treated as no adapter
+    case = DeviceCase(shape, m, W.make_layer(shape, rng), dev)
+    check_case(case)
+    assert case.ws.view[:4].view(torch.int32).item() == binding.LORA_STATUS_BAD_LORA_ID
+    st = binding.lora_read_status(case.ws.view)
+    assert st == binding.LORA_STATUS_BAD_LORA_ID
+    assert binding.lora_read_status(case.ws.view) == 0      # cleared by the read
+    case.n.fill_(65)                                          # n > max_num_tokens: clamped
+    case.prepare()
+    assert binding.lora_read_status(case.ws.view) & binding.LORA_STATUS_BAD_NUM_TOKENS
+    assert case.starts.view[-1].item() == 64
+
+
+def test_argument_errors_launch_nothing(dev):
+    shape = W.custom_shape(max_num_tokens=64, num_tokens=64, hidden=64, slice_widths=(64,),
+                           max_loras=2, rank=8)
+    case = make_case(shape, dev)
+    case.run()
+    y_before = bits_of(case.y.view).copy()
+    with pytest.raises(binding.LoraError):
+        binding.lora_expand(case.u.view, case.b, case.y_view, case.sorted.view,
+                            case.starts.view, case.ws.view[:8])
+    with pytest.raises(binding.LoraError):
+        binding.lora_shrink(case.x[:, 1:], case.a, 1.0, case.u.view, case.sorted.view,
+                            case.starts.view, case.ws.view)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits_of(case.y.view), y_before)
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+def test_graph_captured_once_replays_new_mappings_and_n(dev):
+    sh = W.custom_shape(max_num_tokens=1024, num_tokens=700, hidden=1024, slice_widths=(512,),
+                        max_loras=32, rank=32, neg_prob=0.25)
+    if True:
+        rng = np.random.default_rng(8)
+        m1 = W.make_mapping(sh, rng)
+        layer = W.make_layer(sh, rng)
+        g_case = DeviceCase(sh, m1, layer, dev)
+        stream = torch.cuda.Stream()
+        y_clean = g_case.y.view.clone()
+        g_case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+        torch.cuda.synchronize()
+        # warm up on the side stream (sets kernel attributes), then capture
+        with torch.cuda.stream(stream):
+            g_case.prepare(stream); g_case.shrink(stream); g_case.expand(stream)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            g_case.prepare(stream)
+            g_case.shrink(stream)
+            g_case.expand(stream)
+        for trial, n_new in enumerate((700, 333, 1024, 0)):
+            m_new = W.make_mapping(W.custom_shape(max_num_tokens=1024, num_tokens=n_new,
+                                                  hidden=8, slice_widths=(8,), max_loras=32,
+                                                  rank=8, neg_prob=0.3),
+                                   np.random.default_rng(100 + trial))
+            g_case.mapping.copy_(torch.from_numpy(m_new))
+            g_case.n.fill_(n_new)
+            g_case.y.view.copy_(y_clean)
+            g_case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+            torch.cuda.synchronize()
+            graph.replay()
+            torch.cuda.synchronize()
+            # a fresh eager run on separate buffers must agree bit for bit
+            sh2 = W.custom_shape(max_num_tokens=1024, num_tokens=n_new, hidden=1024,
+                                 slice_widths=(512,), max_loras=32, rank=32)
+            eager = DeviceCase(sh2, m_new, layer, dev)
+            eager.run()
+            assert torch.equal(g_case.sorted.view, eager.sorted.view)
+            assert torch.equal(g_case.starts.view, eager.starts.view)
+            assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
+            assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
+
+
+def test_down_proj_workload_inside_a_graph(dev):
+    wl = W.make_workload("down_proj_graph")
+    sh = wl.shape
+    case = DeviceCase(sh, wl.mapping, wl.layers[0], dev)
+    stream = torch.cuda.Stream()
+    y0 = case.y.view.clone()
+    with torch.cuda.stream(stream):
+        case.prepare(stream); case.shrink(stream); case.expand(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        case.prepare(stream); case.shrink(stream); case.expand(stream)
+    for _ in range(2):
+        case.y.view.copy_(y0)
+        case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        rows = lora_rows(wl.mapping, sh.num_tokens, sh.max_loras)
+        sample = np.sort(np.random.default_rng(1).choice(rows, 300, replace=False))
+        m_sel = np.full(sh.max_num_tokens, -1, np.int32)
+        m_sel[sample] = wl.mapping[sample]
+        lay = wl.layers[0]
+        u_ref = oracle.shrink(lay.x, lay.lora_a, 1.0, m_sel, sh.num_tokens, sh.max_loras,
+                              u_init=np.zeros((1, sh.max_num_tokens, sh.rank)))
+        y_ref = oracle.expand(u_ref, lay.lora_b, lay.y, m_sel, sh.num_tokens, sh.max_loras)
+        y = oracle.bf16_bits_to_f64(bits_of(case.y.view))
+        ok, worst = within_tol(y[sample], y_ref[sample])
+        assert ok, worst
+        tail = bits_of(case.y.view)[sh.num_tokens:]
+        assert np.all(tail == W.BF16_Y_SENTINEL)
+        u_bits = case.u.view.cpu().numpy().view(np.uint32)
+        assert np.all(u_bits[:, sh.num_tokens:] == U_SENTINEL_BITS)
