@@ -316,6 +316,15 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         step()  # first call per device sets kernel attributes outside capture
     stream.synchronize()
+    if args.mode == "profile":
+        for _ in range(args.steps):
+            with torch.cuda.stream(stream):
+                step()
+        stream.synchronize()
+        if rank == 0:
+            print(json.dumps({"mode": "profile", "workload": shape.name, "layers": layers,
+                              "steps": args.steps, "launches": (1 + 2 * layers) * (args.steps + 1)}))
+        return 0
     for which in ("all", "metadata", "shrink", "expand"):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -452,6 +461,8 @@ def main(argv=None):
     ap.add_argument("--config", choices=list(W.CONFIGS), default="decode_qkv")
     ap.add_argument("--layers", type=int, default=0, help="layers per step (0: >= 2x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+                    help="profile: only run --steps eager steps (for ncu launch lists)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 0)
     world, rank, local = dist_setup(args)

@@ -2,7 +2,7 @@
 // Declarations and the full contract live in include/gathered_rank_gemm.h.
 #include <cstdint>
 
-#include "../../include/gathered_rank_gemm.h"
+#include "gathered_rank_gemm.h"
 #include "common.cuh"
 #include "launch.h"
 

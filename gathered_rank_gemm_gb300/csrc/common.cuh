@@ -11,17 +11,20 @@ namespace grg {
 // ---------------------------------------------------------------- workspace
 // [0]   uint32 status word (LORA_STATUS_* bits, OR-ed by the metadata kernel)
 // [4]   int32  n after clamping
-// [16]  int32  num_tiles[kNumTileSizes]: entries of each work list
-// [64]  work lists, one per tile height in kTileRows: int2 {pos, lora} where
-//       pos indexes sorted_token_ids; the tile covers
-//       min(rows, lora_token_start_loc[lora + 1] - pos) tokens of that LoRA.
+// [16]  int32  num_tiles[kNumTileSizes]: records in each work list
+// [64]  work lists, one per tile height rows = 16 << i.  Record j of list i is
+//       rows + 4 int32: {lora, count, pos, 0, token[0 .. rows-1]}: `count`
+//       (1..rows) tokens of adapter `lora`, taken from sorted_token_ids[pos..]
+//       and copied inline so that a CTA gets its whole tile with one load.
 constexpr int kNumTileSizes = 4;
 constexpr int kWsHeaderBytes = 64;
+constexpr int kRecordHeaderInts = 4;
 
 __host__ __device__ constexpr int tile_rows_of(int i) { return 16 << i; }
 __host__ __device__ inline int tile_index_of(int rows) {
   return rows == 16 ? 0 : rows == 32 ? 1 : rows == 64 ? 2 : 3;
 }
+__host__ __device__ constexpr int record_ints(int rows) { return rows + kRecordHeaderInts; }
 __host__ __device__ inline int64_t tile_list_capacity(int64_t max_num_tokens, int64_t max_loras,
                                                       int i) {
   const int64_t rows = tile_rows_of(i);
@@ -30,7 +33,8 @@ __host__ __device__ inline int64_t tile_list_capacity(int64_t max_num_tokens, in
 __host__ __device__ inline int64_t tile_list_offset(int64_t max_num_tokens, int64_t max_loras,
                                                     int i) {
   int64_t off = kWsHeaderBytes;
-  for (int j = 0; j < i; ++j) off += 8 * tile_list_capacity(max_num_tokens, max_loras, j);
+  for (int j = 0; j < i; ++j)
+    off += 4LL * record_ints(tile_rows_of(j)) * tile_list_capacity(max_num_tokens, max_loras, j);
   return off;
 }
 inline size_t workspace_bytes_needed(int64_t max_num_tokens, int64_t max_loras) {
@@ -42,7 +46,7 @@ struct WsView {
   uint32_t* status;
   int32_t* n;
   int32_t* num_tiles;
-  int2* lists[kNumTileSizes];
+  int32_t* lists[kNumTileSizes];
 };
 inline WsView ws_view(void* ws, int64_t max_num_tokens, int64_t max_loras) {
   char* b = static_cast<char*>(ws);
@@ -51,8 +55,38 @@ inline WsView ws_view(void* ws, int64_t max_num_tokens, int64_t max_loras) {
   v.n = reinterpret_cast<int32_t*>(b + 4);
   v.num_tiles = reinterpret_cast<int32_t*>(b + 16);
   for (int i = 0; i < kNumTileSizes; ++i)
-    v.lists[i] = reinterpret_cast<int2*>(b + tile_list_offset(max_num_tokens, max_loras, i));
+    v.lists[i] = reinterpret_cast<int32_t*>(b + tile_list_offset(max_num_tokens, max_loras, i));
   return v;
+}
+
+// Copies tile record `item` of a list (rows + 4 ints, 16-byte aligned) into
+// shared memory with 16-byte loads; the caller synchronises afterwards.
+template <int ROWS>
+__device__ __forceinline__ void load_record(const int32_t* list, int item, int32_t* srec) {
+  const int4* src = reinterpret_cast<const int4*>(list + static_cast<long long>(item) * record_ints(ROWS));
+  for (int i = threadIdx.x; i < record_ints(ROWS) / 4; i += blockDim.x)
+    reinterpret_cast<int4*>(srec)[i] = src[i];
+}
+
+// Decoded tile: adapter, token count and the token of row r (-1 past count).
+// Fields are range-checked, so a workspace that was never prepared cannot
+// send an access out of bounds.
+struct TileView {
+  int lora;
+  int count;
+  __device__ __forceinline__ static TileView of(const int32_t* srec, int rows, int num_loras) {
+    TileView t;
+    const int l = srec[0], c = srec[1];
+    const bool ok = l >= 0 && l < num_loras && c > 0 && c <= rows;
+    t.lora = ok ? l : 0;
+    t.count = ok ? c : 0;
+    return t;
+  }
+};
+__device__ __forceinline__ int record_token(const int32_t* srec, int r, int count,
+                                            int max_num_tokens) {
+  const int t = r < count ? srec[kRecordHeaderInts + r] : -1;
+  return (t >= 0 && t < max_num_tokens) ? t : -1;
 }
 
 // ---------------------------------------------------------------- PTX helpers

@@ -33,9 +33,7 @@ struct ExpandParams {
   int cb_total;         // column blocks over all slices
   __nv_bfloat16* y;
   long long y_stride;
-  const int32_t* sorted_ids;
-  const int32_t* starts;
-  const int2* tiles;
+  const int32_t* records;  // tile records of height BM
   const int32_t* num_tiles;
   int tile_capacity;
   int num_loras;
@@ -46,19 +44,50 @@ __device__ __forceinline__ uint32_t swz512(int k, int ch) {
   return static_cast<uint32_t>(k * 512 + (((ch & ~7) | ((ch ^ k) & 7)) << 4));
 }
 
+template <int RANK>
+struct UFrag {
+  // k-steps of 16 ranks (rank 8 packs high and low parts into one k-step)
+  static constexpr int KK = RANK == 8 ? 1 : RANK / 16;
+  float2 v[KK][4];  // rows g / g+8 x columns 2q / 2q+8 of each k-step
+};
+
+template <int RANK>
+__device__ __forceinline__ void load_u(UFrag<RANK>& f, const float* u0, const float* u1, bool ok0,
+                                       bool ok1, int q) {
+  const float2 z = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int kk = 0; kk < UFrag<RANK>::KK; ++kk) {
+    const int kc = kk * 16 + 2 * q;
+    f.v[kk][0] = ok0 ? *reinterpret_cast<const float2*>(u0 + kc) : z;
+    f.v[kk][1] = ok1 ? *reinterpret_cast<const float2*>(u1 + kc) : z;
+    if (RANK != 8) {
+      f.v[kk][2] = ok0 ? *reinterpret_cast<const float2*>(u0 + kc + 8) : z;
+      f.v[kk][3] = ok1 ? *reinterpret_cast<const float2*>(u1 + kc + 8) : z;
+    }
+  }
+}
+
 template <int BM, int RANK>
-__global__ void __launch_bounds__(kExpandThreads) lora_expand_kernel(const ExpandParams p) {
+__global__ void __launch_bounds__(kExpandThreads, RANK >= 128 ? 2 : 4) lora_expand_kernel(const ExpandParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  int32_t* tok = reinterpret_cast<int32_t*>(smem + RANK * 512);
+  int32_t* rec = reinterpret_cast<int32_t*>(smem + RANK * 512);
   const uint32_t sb = smem_u32(smem);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
+  // u fragments are prefetched with y when they are small enough to sit in registers
+  constexpr bool kPrefetchU = RANK <= 32;
+  constexpr int MT = BM / 16;
 
   pdl_wait();
   pdl_launch_dependents();
+  {
+    const int first = blockIdx.x / max(p.cb_total, 1);
+    if (first < p.tile_capacity) load_record<BM>(p.records, first, rec);
+  }
   // clamped so that a workspace that was never prepared stays in bounds
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
   const int nitems = ntiles * p.cb_total;
+  int loaded = blockIdx.x / max(p.cb_total, 1);
 
   for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
     const int tile = item / p.cb_total;
@@ -75,70 +104,77 @@ __global__ void __launch_bounds__(kExpandThreads) lora_expand_kernel(const Expan
     const int width = s == 0 ? p.w0 : (s == 1 ? p.w1 : p.w2);
     const int off = s == 0 ? p.off0 : (s == 1 ? p.off1 : p.off2);
     const __nv_bfloat16* bsl = s == 0 ? p.b0 : (s == 1 ? p.b1 : p.b2);
-    const int2 td = p.tiles[tile];
-    const bool tile_ok = td.y >= 0 && td.y < p.num_loras && td.x >= 0 && td.x < p.max_num_tokens;
-    const int pos = tile_ok ? td.x : 0, lora = tile_ok ? td.y : 0;
-    const int cnt = tile_ok ? min(min(BM, p.starts[lora + 1] - pos), p.max_num_tokens - pos) : 0;
-    const int c0 = cb * kEN;
-
-    if (tid < BM) {
-      const int t = tid < cnt ? p.sorted_ids[pos + tid] : -1;
-      tok[tid] = (t >= 0 && t < p.max_num_tokens) ? t : -1;
+    if (tile != loaded) {
+      load_record<BM>(p.records, tile, rec);
+      loaded = tile;
     }
+    __syncthreads();  // record visible
+    const TileView tv = TileView::of(rec, BM, p.num_loras);
+    const int lora = tv.lora, cnt = tv.count;
+    const int c0 = cb * kEN;
 
     // B_s[lora][0:RANK][c0:c0+256] -> shared memory
     const __nv_bfloat16* bl = bsl + static_cast<long long>(lora) * RANK * width;
     for (int c = tid; c < RANK * 32; c += kExpandThreads) {
       const int k = c >> 5, ch = c & 31;
       const int col = c0 + ch * 8;
-      const bool ok = col < width;
+      const bool ok = col < width && cnt > 0;
       cp_async_16(sb + swz512(k, ch), ok ? bl + static_cast<long long>(k) * width + col : bsl, ok);
     }
     cp_async_commit();
-    __syncthreads();  // tok[] visible
 
-    // this warp's 64 columns of the gathered y rows -> registers
+    // this warp's 64 columns of the gathered y rows (and u) -> registers
     const int colw = c0 + warp * 64;
-    uint32_t yv[BM / 16][8][2];
+    int tk[MT][2];
+    uint32_t yv[MT][8][2];
+    UFrag<RANK> uf[kPrefetchU ? MT : 1];
 #pragma unroll
-    for (int mi = 0; mi < BM / 16; ++mi) {
-      const int t0 = tok[mi * 16 + g], t1 = tok[mi * 16 + g + 8];
+    for (int mi = 0; mi < MT; ++mi) {
+      tk[mi][0] = record_token(rec, mi * 16 + g, cnt, p.max_num_tokens);
+      tk[mi][1] = record_token(rec, mi * 16 + g + 8, cnt, p.max_num_tokens);
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
         const int col = colw + nt * 8 + 2 * q;
         const bool cok = col < width;
-        yv[mi][nt][0] = (cok && t0 >= 0)
-                            ? *reinterpret_cast<const uint32_t*>(
-                                  p.y + static_cast<long long>(t0) * p.y_stride + off + col)
-                            : 0u;
-        yv[mi][nt][1] = (cok && t1 >= 0)
-                            ? *reinterpret_cast<const uint32_t*>(
-                                  p.y + static_cast<long long>(t1) * p.y_stride + off + col)
-                            : 0u;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          yv[mi][nt][h] = (cok && tk[mi][h] >= 0)
+                              ? *reinterpret_cast<const uint32_t*>(
+                                    p.y + static_cast<long long>(tk[mi][h]) * p.y_stride + off + col)
+                              : 0u;
+      }
+      if constexpr (kPrefetchU) {
+        const float* u0 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(tk[mi][0], 0)) * RANK;
+        const float* u1 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(tk[mi][1], 0)) * RANK;
+        load_u<RANK>(uf[mi], u0, u1, tk[mi][0] >= 0, tk[mi][1] >= 0, q);
       }
     }
     cp_async_wait<0>();
     __syncthreads();  // B tile visible
 
 #pragma unroll
-    for (int mi = 0; mi < BM / 16; ++mi) {
-      const int t0 = tok[mi * 16 + g], t1 = tok[mi * 16 + g + 8];
+    for (int mi = 0; mi < MT; ++mi) {
+      const int t0 = tk[mi][0], t1 = tk[mi][1];
       if (__all_sync(0xffffffffu, t0 < 0 && t1 < 0)) continue;
       float acc[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-      const float* u0 = p.u + (static_cast<long long>(s) * p.max_num_tokens + (t0 < 0 ? 0 : t0)) * RANK;
-      const float* u1 = p.u + (static_cast<long long>(s) * p.max_num_tokens + (t1 < 0 ? 0 : t1)) * RANK;
+      UFrag<RANK> ul;
+      if constexpr (kPrefetchU) {
+        ul = uf[mi];
+      } else {
+        const float* u0 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(t0, 0)) * RANK;
+        const float* u1 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(t1, 0)) * RANK;
+        load_u<RANK>(ul, u0, u1, t0 >= 0, t1 >= 0, q);
+      }
 
       if constexpr (RANK == 8) {
         // k = 0..7 carry the high parts, k = 8..15 the residuals; B rows repeat.
-        const float2 v0 = t0 >= 0 ? *reinterpret_cast<const float2*>(u0 + 2 * q) : make_float2(0.f, 0.f);
-        const float2 v1 = t1 >= 0 ? *reinterpret_cast<const float2*>(u1 + 2 * q) : make_float2(0.f, 0.f);
         uint32_t a[4];
-        split_bf16x2(v0.x, v0.y, a[0], a[2]);
-        split_bf16x2(v1.x, v1.y, a[1], a[3]);
+        split_bf16x2(ul.v[0][0].x, ul.v[0][0].y, a[0], a[2]);
+        split_bf16x2(ul.v[0][1].x, ul.v[0][1].y, a[1], a[3]);
 #pragma unroll
         for (int nt = 0; nt < 8; nt += 4) {
           uint32_t bfr[4];
@@ -149,16 +185,9 @@ __global__ void __launch_bounds__(kExpandThreads) lora_expand_kernel(const Expan
       } else {
 #pragma unroll
         for (int kk = 0; kk < RANK / 16; ++kk) {
-          const int kc = kk * 16 + 2 * q;
-          const float2 v00 = t0 >= 0 ? *reinterpret_cast<const float2*>(u0 + kc) : make_float2(0.f, 0.f);
-          const float2 v10 = t1 >= 0 ? *reinterpret_cast<const float2*>(u1 + kc) : make_float2(0.f, 0.f);
-          const float2 v01 = t0 >= 0 ? *reinterpret_cast<const float2*>(u0 + kc + 8) : make_float2(0.f, 0.f);
-          const float2 v11 = t1 >= 0 ? *reinterpret_cast<const float2*>(u1 + kc + 8) : make_float2(0.f, 0.f);
           uint32_t ah[4], al[4];
-          split_bf16x2(v00.x, v00.y, ah[0], al[0]);
-          split_bf16x2(v10.x, v10.y, ah[1], al[1]);
-          split_bf16x2(v01.x, v01.y, ah[2], al[2]);
-          split_bf16x2(v11.x, v11.y, ah[3], al[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_bf16x2(ul.v[kk][e].x, ul.v[kk][e].y, ah[e], al[e]);
 #pragma unroll
           for (int nt = 0; nt < 8; nt += 2) {
             uint32_t bfr[4];
@@ -190,14 +219,14 @@ __global__ void __launch_bounds__(kExpandThreads) lora_expand_kernel(const Expan
         }
       }
     }
-    __syncthreads();  // before the next item overwrites tok[] and the B tile
+    __syncthreads();  // before the next item overwrites the record and the B tile
   }
 }
 
 template <int BM, int RANK>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
   const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK>);
-  const size_t smem = static_cast<size_t>(RANK) * 512 + BM * sizeof(int32_t);
+  const size_t smem = static_cast<size_t>(RANK) * 512 + record_ints(BM) * sizeof(int32_t);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -237,10 +266,8 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
   p.cb_total = cb_total;
   p.y = static_cast<__nv_bfloat16*>(a.y);
   p.y_stride = a.y_row_stride;
-  p.sorted_ids = a.sorted_ids;
-  p.starts = a.starts;
   WsView ws = ws_view(const_cast<void*>(a.workspace), a.max_num_tokens, a.num_loras);
-  p.tiles = ws.lists[tile_index_of(BM)];
+  p.records = ws.lists[tile_index_of(BM)];
   p.num_tiles = ws.num_tiles + tile_index_of(BM);
   p.tile_capacity =
       static_cast<int>(tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM)));

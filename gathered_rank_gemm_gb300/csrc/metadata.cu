@@ -19,8 +19,9 @@
 // Warp ranges are in token order and lanes are in token order, so equal ids
 // keep ascending token order (stable).  The grid is one CTA whatever the data,
 // so the launch is graph-safe.  The kernel also writes, for each tile height
-// in {16, 32, 64, 128}, the list of (position, lora) tiles that the shrink and
-// expand kernels walk with a fixed grid.
+// in {16, 32, 64, 128}, the list of tile records (adapter, count and the
+// tile's token ids inline) that the shrink and expand kernels walk with a
+// fixed grid.
 #include "common.cuh"
 #include "launch.h"
 
@@ -86,11 +87,11 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
 
   const int L = p.num_loras;
   const int nbins = L + 1;
-  int32_t* hist = sm;                        // [kMetaWarps][nbins], then warp offsets
+  int32_t* hist = sm;                          // [kMetaWarps][nbins], then warp offsets
   int32_t* total = hist + kMetaWarps * nbins;  // [nbins]
-  int32_t* start = total + nbins;            // [nbins + 1]
-  int32_t* ntile = start + nbins + 1;        // [L]
-  int32_t* toff = ntile + L;                 // [L + 1]
+  int32_t* start = total + nbins;              // [nbins + 1]
+  int32_t* ntile = start + nbins + 1;          // [L]
+  int32_t* toff = ntile + L;                   // [kNumTileSizes][L + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
@@ -147,7 +148,16 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   __syncthreads();
   block_exclusive_scan(total, start, nbins, warp_sums);
 
-  // pass 3: stable scatter
+  // tiles per adapter and their offsets in each work list
+#pragma unroll
+  for (int k = 0; k < kNumTileSizes; ++k) {
+    const int rows = tile_rows_of(k);
+    for (int l = tid; l < L; l += kMetaThreads) ntile[l] = (total[l] + rows - 1) / rows;
+    __syncthreads();
+    block_exclusive_scan(ntile, toff + k * (L + 1), L, warp_sums);
+  }
+
+  // pass 3: stable scatter into sorted_token_ids and into the tile records
   for (int base = lo; base < hi; base += 32) {
     const int t = base + lane;
     const bool valid = t < hi;
@@ -158,8 +168,16 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
     }
     const unsigned peers = __match_any_sync(0xffffffffu, bin);
     if (valid) {
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      p.sorted_ids[start[bin] + my_hist[bin] + rank] = t;
+      const int rel = my_hist[bin] + __popc(peers & ((1u << lane) - 1u));
+      p.sorted_ids[start[bin] + rel] = t;
+      if (bin < L) {
+#pragma unroll
+        for (int k = 0; k < kNumTileSizes; ++k) {
+          const int tile = toff[k * (L + 1) + bin] + (rel >> (4 + k));
+          p.ws.lists[k][static_cast<long long>(tile) * record_ints(tile_rows_of(k)) +
+                        kRecordHeaderInts + (rel & (tile_rows_of(k) - 1))] = t;
+        }
+      }
     }
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
@@ -169,26 +187,25 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
   for (int b = tid; b <= nbins; b += kMetaThreads) p.starts[b] = start[b];
 
-  // work lists for the fixed-grid kernels
+  // record headers
 #pragma unroll
   for (int k = 0; k < kNumTileSizes; ++k) {
     const int rows = tile_rows_of(k);
-    for (int l = tid; l < L; l += kMetaThreads) ntile[l] = (total[l] + rows - 1) / rows;
-    __syncthreads();
-    block_exclusive_scan(ntile, toff, L, warp_sums);
-    const int count = toff[L];
-    int2* list = p.ws.lists[k];
+    const int32_t* off = toff + k * (L + 1);
+    const int count = off[L];
+    int32_t* list = p.ws.lists[k];
     for (int i = tid; i < count; i += kMetaThreads) {
-      // largest l with toff[l] <= i (l in [0, L))
+      // largest l with off[l] <= i (adapters with no tile share the next offset)
       int a = 0, b = L - 1;
       while (a < b) {
         const int mid = (a + b + 1) >> 1;
-        if (toff[mid] <= i) a = mid; else b = mid - 1;
+        if (off[mid] <= i) a = mid; else b = mid - 1;
       }
-      list[i] = make_int2(start[a] + (i - toff[a]) * rows, a);
+      const int j = i - off[a];
+      int4 h = make_int4(a, min(rows, total[a] - j * rows), start[a] + j * rows, 0);
+      *reinterpret_cast<int4*>(list + static_cast<long long>(i) * record_ints(rows)) = h;
     }
     if (tid == 0) p.ws.num_tiles[k] = count;
-    __syncthreads();
   }
   if (tid == 0) {
     *p.ws.n = n;
@@ -198,7 +215,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
 
 static size_t meta_smem_bytes(int num_loras) {
   const size_t nb = static_cast<size_t>(num_loras) + 1;
-  return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + (nb - 1) + nb);
+  return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + (nb - 1) + kNumTileSizes * nb);
 }
 
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,

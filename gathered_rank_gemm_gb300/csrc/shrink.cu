@@ -21,7 +21,6 @@
 namespace grg {
 
 constexpr int kShrinkThreads = 128;
-constexpr int kShrinkStages = 4;
 constexpr int kBK = 64;  // bf16 columns per k-block: one 128-byte row chunk
 
 struct ShrinkParams {
@@ -39,15 +38,13 @@ struct ShrinkParams {
   float scale;
   float* u;
   int max_num_tokens;
-  const int32_t* sorted_ids;
-  const int32_t* starts;
-  const int2* tiles;
+  const int32_t* records;    // tile records of height BM
   const int32_t* num_tiles;
-  int tile_capacity;  // entries the work list can hold
+  int tile_capacity;         // records the list can hold
   int num_loras;
   int warps_n;     // warps splitting the S*R columns (1, 2 or 4)
   int ntw;         // n8 column tiles per warp
-  int tok_offset;  // byte offset of tok[] in shared memory
+  int rec_offset;  // byte offset of the tile record in shared memory
 };
 
 // Byte offset of 16-byte chunk ch (0..7) of a 128-byte row, XOR-swizzled so
@@ -56,10 +53,10 @@ __device__ __forceinline__ uint32_t swz128(int row, int ch) {
   return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
 }
 
-template <int BM, int NTW>
-__global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const ShrinkParams p) {
+template <int BM, int NTW, int NST>
+__global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const ShrinkParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  int32_t* tok = reinterpret_cast<int32_t*>(smem + p.tok_offset);
+  int32_t* rec = reinterpret_cast<int32_t*>(smem + p.rec_offset);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int SR = p.sr;
@@ -83,20 +80,15 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
 
   pdl_wait();
   pdl_launch_dependents();
-  // the list comes from the metadata kernel; clamp it so that a workspace
-  // that was never prepared cannot send an access out of bounds
+  // the first record is fetched together with the count (it may be unused)
+  if (cluster_id < p.tile_capacity) load_record<BM>(p.records, cluster_id, rec);
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
 
   for (int item = cluster_id; item < ntiles; item += nclusters) {
-    const int2 td = p.tiles[item];
-    const bool tile_ok = td.y >= 0 && td.y < p.num_loras && td.x >= 0 && td.x < p.max_num_tokens;
-    const int pos = tile_ok ? td.x : 0, lora = tile_ok ? td.y : 0;
-    const int cnt = tile_ok ? min(min(BM, p.starts[lora + 1] - pos), p.max_num_tokens - pos) : 0;
-    if (tid < BM) {
-      int t = tid < cnt ? p.sorted_ids[pos + tid] : -1;
-      tok[tid] = (t >= 0 && t < p.max_num_tokens) ? t : -1;
-    }
+    if (item != cluster_id) load_record<BM>(p.records, item, rec);
     __syncthreads();
+    const TileView tv = TileView::of(rec, BM, p.num_loras);
+    const int lora = tv.lora, cnt = tv.count;
 
     auto load_stage = [&](int st, int kb) {
       const uint32_t sx = smem_base + st * stage_bytes;
@@ -104,7 +96,7 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
       const int col = kb * kBK;
       for (int c = tid; c < BM * 8; c += kShrinkThreads) {
         const int row = c >> 3, ch = c & 7;
-        const int t = tok[row];
+        const int t = record_token(rec, row, cnt, p.max_num_tokens);
         const int kcol = col + ch * 8;
         const bool ok = (t >= 0) && (kcol < p.hidden);
         const __nv_bfloat16* src = ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x;
@@ -115,7 +107,7 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
         const int s = row >> p.rank_shift;
         const int r = row - (s << p.rank_shift);
         const int kcol = col + ch * 8;
-        const bool ok = kcol < p.hidden;
+        const bool ok = kcol < p.hidden && cnt > 0;
         const __nv_bfloat16* a = s == 0 ? p.a0 : (s == 1 ? p.a1 : p.a2);
         const __nv_bfloat16* src =
             ok ? a + (static_cast<long long>(lora) * p.rank + r) * p.hidden + kcol : p.a0;
@@ -131,20 +123,21 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
 
+    // keep NST - 1 k-blocks in flight (all of them when the range is short)
 #pragma unroll
-    for (int s = 0; s < kShrinkStages - 1; ++s) {
+    for (int s = 0; s < NST - 1; ++s) {
       if (s < nkb) load_stage(s, kb0 + s);
       cp_async_commit();
     }
 
     for (int i = 0; i < nkb; ++i) {
-      cp_async_wait<kShrinkStages - 2>();
+      cp_async_wait<NST - 2>();
       __syncthreads();
-      const int nxt = i + kShrinkStages - 1;
-      if (nxt < nkb) load_stage(nxt % kShrinkStages, kb0 + nxt);
+      const int nxt = i + NST - 1;
+      if (nxt < nkb) load_stage(nxt % NST, kb0 + nxt);
       cp_async_commit();
 
-      const uint32_t sx = smem_base + (i % kShrinkStages) * stage_bytes;
+      const uint32_t sx = smem_base + (i % NST) * stage_bytes;
       const uint32_t sw = sx + BM * 128;
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks) {
@@ -207,7 +200,8 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
       const int e = idx << 2;
       const int row = e / SR;
       const int col = e - row * SR;
-      if (row >= cnt || tok[row] < 0) continue;
+      const int t = record_token(rec, row, cnt, p.max_num_tokens);
+      if (t < 0) continue;
       float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 0; c < C; ++c) {
         for (int w = 0; w < WK; ++w) {
@@ -222,7 +216,7 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
       }
       const int s = col >> p.rank_shift;
       const int r = col - (s << p.rank_shift);
-      float* dst = p.u + (static_cast<long long>(s) * p.max_num_tokens + tok[row]) * p.rank + r;
+      float* dst = p.u + (static_cast<long long>(s) * p.max_num_tokens + t) * p.rank + r;
       *reinterpret_cast<float4*>(dst) =
           make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
     }
@@ -230,10 +224,10 @@ __global__ void __launch_bounds__(kShrinkThreads) lora_shrink_kernel(const Shrin
   }
 }
 
-template <int BM, int NTW>
+template <int BM, int NTW, int NST>
 static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStream_t stream,
                       long long max_tiles) {
-  const void* fn = reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW>);
+  const void* fn = reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST>);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -261,13 +255,17 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   int cluster = 1;
   while (cluster < 8 && static_cast<long long>(cluster) * 2 * max_tiles <= 2LL * sms) cluster *= 2;
   while (cluster > 1 && cluster > kblocks) cluster /= 2;
+  const int kb_per = (kblocks + cluster - 1) / cluster;
+  // deep ring when a CTA's whole k-range fits: every load is in flight at once
+  const size_t stage = static_cast<size_t>(BM + SR) * 128;
+  const int nst = (kb_per <= 8 && 8 * stage <= 96 * 1024 && ntw <= 8) ? 8 : 4;
 
   ShrinkParams p;
   p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.x_stride = a.x_row_stride;
   p.hidden = a.hidden;
   p.kblocks = kblocks;
-  p.kb_per_rank = (kblocks + cluster - 1) / cluster;
+  p.kb_per_rank = kb_per;
   p.a0 = static_cast<const __nv_bfloat16*>(a.lora_a[0]);
   p.a1 = static_cast<const __nv_bfloat16*>(a.num_slices > 1 ? a.lora_a[1] : a.lora_a[0]);
   p.a2 = static_cast<const __nv_bfloat16*>(a.num_slices > 2 ? a.lora_a[2] : a.lora_a[0]);
@@ -277,26 +275,26 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.scale = a.scale;
   p.u = a.u;
   p.max_num_tokens = a.max_num_tokens;
-  p.sorted_ids = a.sorted_ids;
-  p.starts = a.starts;
   WsView ws = ws_view(const_cast<void*>(a.workspace), a.max_num_tokens, a.num_loras);
-  p.tiles = ws.lists[tile_index_of(BM)];
+  p.records = ws.lists[tile_index_of(BM)];
   p.num_tiles = ws.num_tiles + tile_index_of(BM);
   p.tile_capacity = static_cast<int>(max_tiles);
   p.num_loras = a.num_loras;
   p.warps_n = warps_n;
   p.ntw = ntw;
-  const size_t ring = static_cast<size_t>(kShrinkStages) * (BM + SR) * 128;
+  const size_t ring = static_cast<size_t>(nst) * stage;
   const size_t red = static_cast<size_t>(WK) * BM * SR * 4;
   const size_t body = ring > red ? ring : red;
-  p.tok_offset = static_cast<int>(body);
-  const size_t smem = body + BM * sizeof(int32_t);
+  p.rec_offset = static_cast<int>(body);
+  const size_t smem = body + record_ints(BM) * sizeof(int32_t);
 
   if (BM == 16) {
-    if (ntw <= 8) return run_shrink<16, 8>(p, cluster, smem, stream, max_tiles);
-    return run_shrink<16, 12>(p, cluster, smem, stream, max_tiles);
+    if (ntw > 8) return run_shrink<16, 12, 4>(p, cluster, smem, stream, max_tiles);
+    if (nst == 8) return run_shrink<16, 8, 8>(p, cluster, smem, stream, max_tiles);
+    return run_shrink<16, 8, 4>(p, cluster, smem, stream, max_tiles);
   }
-  return run_shrink<32, 8>(p, cluster, smem, stream, max_tiles);
+  if (nst == 8) return run_shrink<32, 8, 8>(p, cluster, smem, stream, max_tiles);
+  return run_shrink<32, 8, 4>(p, cluster, smem, stream, max_tiles);
 }
 
 }  // namespace grg
