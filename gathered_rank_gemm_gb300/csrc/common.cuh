@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -68,6 +69,16 @@ __device__ __forceinline__ void load_record(const int32_t* list, int item, int32
     reinterpret_cast<int4*>(srec)[i] = src[i];
 }
 
+// Same, asynchronously (cp.async, part of the caller's next commit group).
+template <int ROWS>
+__device__ __forceinline__ void load_record_async(const int32_t* list, int item, int32_t* srec) {
+  const int32_t* src = list + static_cast<long long>(item) * record_ints(ROWS);
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(srec));
+  for (int i = threadIdx.x; i < record_ints(ROWS) / 4; i += blockDim.x)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16 * i), "l"(src + 4 * i)
+                 : "memory");
+}
+
 // Decoded tile: adapter, token count and the token of row r (-1 past count).
 // Fields are range-checked, so a workspace that was never prepared cannot
 // send an access out of bounds.
@@ -106,6 +117,20 @@ __device__ __forceinline__ void cp_async_commit() {
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+// Waits until at most n of this thread's most recent cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    case 7: cp_async_wait<7>(); break;
+    default: cp_async_wait<8>(); break;
+  }
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -158,6 +183,107 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+// ---------------------------------------------------------------- TMA bulk copies + mbarriers
+// Spin limit for every mbarrier wait: a wait that has not completed after this
+// many nanoseconds of %globaltimer gives up and reports LORA_STATUS_TIMEOUT.
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
+constexpr uint32_t kStatusTimeout = 0x4u;
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+// Makes barrier initialisation visible to the async proxy (and the cluster).
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase with the given parity; false if the time limit passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+// global -> shared bulk copy (16-byte aligned, size a multiple of 16) that
+// completes `bytes` transactions on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// 2-D tiled TMA load of box (x, y) of a tensor map into shared memory,
+// completing the box's bytes on the mbarrier.  x must be a multiple of 8
+// bf16 elements (16 bytes); out-of-range elements are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+// Offset inside a 1024-byte-aligned [rows][128 B] box written by TMA with the
+// 128-byte swizzle: 16-byte chunk ch of row r lands at chunk ch ^ (r % 8).
+__device__ __forceinline__ uint32_t swz128(int row, int ch) {
+  return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
+}
+
+// shared -> global bulk copy, tracked by the thread's bulk async-groups.
+__device__ __forceinline__ void bulk_s2g(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// The thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// The thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+// Orders this thread's generic-proxy shared-memory accesses before later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
+// L2 is the coherence point of the GPU, so prefetching data that an earlier
+// kernel may still be writing is harmless: later reads through L2 see the
+// final values.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding grid's memory, and let

@@ -4,196 +4,255 @@
 // grouping as the shrink and adds the rank -> width product into the output).
 //
 // Work decomposition (fixed grid, graph-safe): an item is one tile of up to BM
-// tokens of one LoRA (from the metadata kernel's list) times one block of 256
-// output columns of one slice.  A CTA of four warps copies the adapter's
-// B_s[lora][0:R][block] into XOR-swizzled shared memory with cp.async, while
-// every warp issues the loads of its 64 columns of the gathered y rows into
-// registers; then each warp runs tensor-core MMAs (m16n8k16, fp32 accumulate)
-// of the 16-token x R slice of u against B, and adds the product into y with
-// one bf16 rounding per element.  u is fed to the tensor cores as two bf16
-// terms (high part + residual), so about 16 significant bits of the fp32 u
-// reach the product.  CTAs loop over the items with a stride of the grid.
+// tokens of one LoRA (a record of the metadata kernel's list) times one block
+// of 256 output columns of one slice.  CTAs walk the items with a stride of
+// the grid.
+//
+// Data movement, per item, into a shared-memory stage:
+//  - the adapter block B_s[lora][0:R][block] as four R x 64 TMA tile loads
+//    (tensor map, 128-byte swizzle), completing on the stage's mbarrier;
+//  - the gathered 256-column segments of y and the gathered rows of u with
+//    16-byte cp.async (rows padded so the epilogue hits distinct banks).
+// Ranks up to 32 use two stages, so the next item's copies fly while the
+// current one is computed.  Before griddepcontrol.wait only metadata and
+// weights are fetched (the first record and B block) and the first y rows
+// are prefetched into L2; u and y are copied after it.
+//
+// Compute: four warps, 64 columns each; per 16-token m-tile a warp runs
+// mma.sync m16n8k16 (bf16 operands, fp32 accumulate) of the u rows against B.
+// u enters the tensor cores as two bf16 terms (high part + residual), so about
+// 16 significant bits of the fp32 u reach the product.  The sum is added to
+// the staged y in fp32, rounded once to bf16, written back into the stage and
+// stored with coalesced 16-byte stores.
 #include "common.cuh"
 #include "launch.h"
 
 namespace grg {
 
 constexpr int kExpandThreads = 128;
-constexpr int kEN = 256;  // output columns per item (64 per warp)
+constexpr int kEN = 256;     // output columns per item (64 per warp)
+constexpr int kYPitch = 528; // staged y row bytes (512 + 16)
 
 struct ExpandParams {
+  CUtensorMap tmap[3];  // B_s viewed as [L * R][N_s], boxes of R x 64
   const float* u;
   int max_num_tokens;
-  const __nv_bfloat16* b0;
-  const __nv_bfloat16* b1;
-  const __nv_bfloat16* b2;
-  int w0, w1, w2;       // slice widths
-  int off0, off1, off2; // slice column offsets in y
-  int cb0, cb1;         // column blocks of slices 0 and 1
-  int cb_total;         // column blocks over all slices
+  int w0, w1, w2;        // slice widths
+  int off0, off1, off2;  // slice column offsets in y
+  int cb0, cb1;          // column blocks of slices 0 and 1
+  int cb_total;          // column blocks over all slices
   __nv_bfloat16* y;
   long long y_stride;
   const int32_t* records;  // tile records of height BM
   const int32_t* num_tiles;
+  uint32_t* status;
   int tile_capacity;
   int num_loras;
 };
 
-// Byte offset of 16-byte chunk ch (0..31) of row k of a [R][256] bf16 tile.
-__device__ __forceinline__ uint32_t swz512(int k, int ch) {
-  return static_cast<uint32_t>(k * 512 + (((ch & ~7) | ((ch ^ k) & 7)) << 4));
-}
-
-template <int RANK>
-struct UFrag {
-  // k-steps of 16 ranks (rank 8 packs high and low parts into one k-step)
-  static constexpr int KK = RANK == 8 ? 1 : RANK / 16;
-  float2 v[KK][4];  // rows g / g+8 x columns 2q / 2q+8 of each k-step
+template <int BM, int RANK>
+struct ExpandLayout {
+  static constexpr int kUPitch = RANK * 4 + 16;  // staged u row bytes
+  static constexpr int kB = 0;                   // 4 boxes of [RANK][128 B], 1024-aligned
+  static constexpr int kY = 4 * RANK * 128;
+  static constexpr int kU = kY + BM * kYPitch;
+  static constexpr int kStage = (kU + BM * kUPitch + 1023) / 1024 * 1024;
+  static constexpr int kNStage = RANK <= 32 ? 2 : 1;
+  static constexpr int kRecBytes = record_ints(BM) * 4;
+  static constexpr int kRec = kNStage * kStage;      // three record slots
+  static constexpr int kBar = kRec + 3 * kRecBytes;  // one mbarrier per stage
+  static constexpr int kSmem = 1024 + kBar + 8 * kNStage;
 };
 
-template <int RANK>
-__device__ __forceinline__ void load_u(UFrag<RANK>& f, const float* u0, const float* u1, bool ok0,
-                                       bool ok1, int q) {
-  const float2 z = make_float2(0.f, 0.f);
-#pragma unroll
-  for (int kk = 0; kk < UFrag<RANK>::KK; ++kk) {
-    const int kc = kk * 16 + 2 * q;
-    f.v[kk][0] = ok0 ? *reinterpret_cast<const float2*>(u0 + kc) : z;
-    f.v[kk][1] = ok1 ? *reinterpret_cast<const float2*>(u1 + kc) : z;
-    if (RANK != 8) {
-      f.v[kk][2] = ok0 ? *reinterpret_cast<const float2*>(u0 + kc + 8) : z;
-      f.v[kk][3] = ok1 ? *reinterpret_cast<const float2*>(u1 + kc + 8) : z;
-    }
-  }
-}
-
 template <int BM, int RANK>
-__global__ void __launch_bounds__(kExpandThreads, RANK >= 128 ? 2 : 4) lora_expand_kernel(const ExpandParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  int32_t* rec = reinterpret_cast<int32_t*>(smem + RANK * 512);
-  const uint32_t sb = smem_u32(smem);
+__global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
+    lora_expand_kernel(const __grid_constant__ ExpandParams p) {
+  using Lay = ExpandLayout<BM, RANK>;
+  constexpr int NS = Lay::kNStage;
+  constexpr int MT = BM / 16;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA's 128-byte swizzle is laid out on 1024-byte boundaries
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sbase - raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
-  // u fragments are prefetched with y when they are small enough to sit in registers
-  constexpr bool kPrefetchU = RANK <= 32;
-  constexpr int MT = BM / 16;
 
-  pdl_wait();
-  pdl_launch_dependents();
-  {
-    const int first = blockIdx.x / max(p.cb_total, 1);
-    if (first < p.tile_capacity) load_record<BM>(p.records, first, rec);
-  }
-  // clamped so that a workspace that was never prepared stays in bounds
+  // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
   const int nitems = ntiles * p.cb_total;
-  int loaded = blockIdx.x / max(p.cb_total, 1);
+  const int G = gridDim.x;
+  const int nloc = static_cast<int>(blockIdx.x) < nitems
+                       ? (nitems - 1 - static_cast<int>(blockIdx.x)) / G + 1
+                       : 0;
+  if (nloc == 0) return;  // this CTA writes nothing
 
-  for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(sbase + Lay::kBar + 8 * s, 1);
+    fence_mbar_init();
+  }
+
+  auto rec_of = [&](int k) {
+    return reinterpret_cast<int32_t*>(smem + Lay::kRec + (k % 3) * Lay::kRecBytes);
+  };
+  struct Item {
+    int s, width, off, c0;
+  };
+  auto item_of = [&](int k) {
+    const int item = static_cast<int>(blockIdx.x) + k * G;
     const int tile = item / p.cb_total;
     int cb = item - tile * p.cb_total;
-    int s = 0;
+    Item it;
+    it.s = 0;
     if (cb >= p.cb0) {
       cb -= p.cb0;
-      s = 1;
+      it.s = 1;
       if (cb >= p.cb1) {
         cb -= p.cb1;
-        s = 2;
+        it.s = 2;
       }
     }
-    const int width = s == 0 ? p.w0 : (s == 1 ? p.w1 : p.w2);
-    const int off = s == 0 ? p.off0 : (s == 1 ? p.off1 : p.off2);
-    const __nv_bfloat16* bsl = s == 0 ? p.b0 : (s == 1 ? p.b1 : p.b2);
-    if (tile != loaded) {
-      load_record<BM>(p.records, tile, rec);
-      loaded = tile;
-    }
-    __syncthreads();  // record visible
+    it.width = it.s == 0 ? p.w0 : (it.s == 1 ? p.w1 : p.w2);
+    it.off = it.s == 0 ? p.off0 : (it.s == 1 ? p.off1 : p.off2);
+    it.c0 = cb * kEN;
+    return it;
+  };
+  auto tile_of = [&](int k) { return (static_cast<int>(blockIdx.x) + k * G) / p.cb_total; };
+
+  // B block of item k -> stage (thread 0): boxes starting past the slice are skipped
+  auto fill_b = [&](int k) {
+    const Item it = item_of(k);
+    const TileView tv = TileView::of(rec_of(k), BM, p.num_loras);
+    const uint32_t st = sbase + (k % NS) * Lay::kStage;
+    const uint32_t bar = sbase + Lay::kBar + 8 * (k % NS);
+    const int boxes = min(4, (it.width - it.c0 + 63) / 64);
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * RANK * 128));
+    for (int b = 0; b < boxes; ++b)
+      tma_load_2d(st + Lay::kB + b * RANK * 128, &p.tmap[it.s], it.c0 + 64 * b, tv.lora * RANK,
+                  bar);
+  };
+  // gathered y segments and u rows of item k -> stage (every thread)
+  auto fill_uy = [&](int k) {
+    const Item it = item_of(k);
+    const int32_t* rec = rec_of(k);
     const TileView tv = TileView::of(rec, BM, p.num_loras);
-    const int lora = tv.lora, cnt = tv.count;
-    const int c0 = cb * kEN;
-
-    // B_s[lora][0:RANK][c0:c0+256] -> shared memory
-    const __nv_bfloat16* bl = bsl + static_cast<long long>(lora) * RANK * width;
-    for (int c = tid; c < RANK * 32; c += kExpandThreads) {
-      const int k = c >> 5, ch = c & 31;
-      const int col = c0 + ch * 8;
-      const bool ok = col < width && cnt > 0;
-      cp_async_16(sb + swz512(k, ch), ok ? bl + static_cast<long long>(k) * width + col : bsl, ok);
+    const uint32_t st = sbase + (k % NS) * Lay::kStage;
+    const int ych = tid & 31;
+    const int col = it.c0 + ych * 8;
+#pragma unroll
+    for (int i = 0; i < BM / 4; ++i) {
+      const int row = (tid >> 5) + 4 * i;
+      const int t = record_token(rec, row, tv.count, p.max_num_tokens);
+      const bool ok = t >= 0 && col < it.width;
+      cp_async_16(st + Lay::kY + row * kYPitch + ych * 16,
+                  ok ? p.y + static_cast<long long>(t) * p.y_stride + it.off + col : p.y, ok);
     }
-    cp_async_commit();
-
-    // this warp's 64 columns of the gathered y rows (and u) -> registers
-    const int colw = c0 + warp * 64;
-    int tk[MT][2];
-    uint32_t yv[MT][8][2];
-    UFrag<RANK> uf[kPrefetchU ? MT : 1];
-#pragma unroll
-    for (int mi = 0; mi < MT; ++mi) {
-      tk[mi][0] = record_token(rec, mi * 16 + g, cnt, p.max_num_tokens);
-      tk[mi][1] = record_token(rec, mi * 16 + g + 8, cnt, p.max_num_tokens);
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int col = colw + nt * 8 + 2 * q;
-        const bool cok = col < width;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          yv[mi][nt][h] = (cok && tk[mi][h] >= 0)
-                              ? *reinterpret_cast<const uint32_t*>(
-                                    p.y + static_cast<long long>(tk[mi][h]) * p.y_stride + off + col)
-                              : 0u;
-      }
-      if constexpr (kPrefetchU) {
-        const float* u0 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(tk[mi][0], 0)) * RANK;
-        const float* u1 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(tk[mi][1], 0)) * RANK;
-        load_u<RANK>(uf[mi], u0, u1, tk[mi][0] >= 0, tk[mi][1] >= 0, q);
-      }
+    constexpr int UCH = RANK / 4;  // 16-byte chunks per u row
+    for (int c = tid; c < BM * UCH; c += kExpandThreads) {
+      const int row = c / UCH, ch = c - row * UCH;
+      const int t = record_token(rec, row, tv.count, p.max_num_tokens);
+      const bool ok = t >= 0;
+      cp_async_16(st + Lay::kU + row * Lay::kUPitch + ch * 16,
+                  ok ? p.u + (static_cast<long long>(it.s) * p.max_num_tokens + t) * RANK + ch * 4
+                     : p.u,
+                  ok);
     }
+  };
+
+  // prologue: record 0 and the B block of item 0 before the wait, the rest after it
+  load_record_async<BM>(p.records, tile_of(0), rec_of(0));
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();  // record 0 and the barrier initialisation are visible
+  if (tid == 0) {
+    for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
+    fill_b(0);
+  }
+  {
+    // warm L2 (and the TLB) with item 0's y rows while the previous kernel finishes
+    const Item it = item_of(0);
+    const int32_t* rec = rec_of(0);
+    const TileView tv = TileView::of(rec, BM, p.num_loras);
+    const int bytes = min(kEN, it.width - it.c0) * 2;
+    for (int r = tid; r < tv.count; r += kExpandThreads) {
+      const int t = record_token(rec, r, tv.count, p.max_num_tokens);
+      if (t >= 0) prefetch_l2(p.y + static_cast<long long>(t) * p.y_stride + it.off + it.c0, bytes);
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  fill_uy(0);
+  if (1 < nloc) load_record_async<BM>(p.records, tile_of(1), rec_of(1));
+  cp_async_commit();
+
+  bool timed_out = false;
+  for (int k = 0; k < nloc; ++k) {
     cp_async_wait<0>();
-    __syncthreads();  // B tile visible
+    __syncthreads();  // item k's y/u and record k+1 have landed; item k-1 is finished
+    if (NS == 2) {
+      if (k + 1 < nloc) {
+        if (tid == 0) fill_b(k + 1);
+        fill_uy(k + 1);
+      }
+      if (k + 2 < nloc) load_record_async<BM>(p.records, tile_of(k + 2), rec_of(k + 2));
+      cp_async_commit();
+    }
+
+    const Item it = item_of(k);
+    const int32_t* rec = rec_of(k);
+    const TileView tv = TileView::of(rec, BM, p.num_loras);
+    unsigned char* stp = smem + (k % NS) * Lay::kStage;
+    const uint32_t st = sbase + (k % NS) * Lay::kStage;
+    if (!mbar_wait(sbase + Lay::kBar + 8 * (k % NS), (k / NS) & 1)) timed_out = true;
 
 #pragma unroll
     for (int mi = 0; mi < MT; ++mi) {
-      const int t0 = tk[mi][0], t1 = tk[mi][1];
-      if (__all_sync(0xffffffffu, t0 < 0 && t1 < 0)) continue;
+      if (mi * 16 >= tv.count) break;
       float acc[8][4];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-      UFrag<RANK> ul;
-      if constexpr (kPrefetchU) {
-        ul = uf[mi];
-      } else {
-        const float* u0 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(t0, 0)) * RANK;
-        const float* u1 = p.u + (static_cast<long long>(s) * p.max_num_tokens + max(t1, 0)) * RANK;
-        load_u<RANK>(ul, u0, u1, t0 >= 0, t1 >= 0, q);
-      }
+      const float* u0 =
+          reinterpret_cast<const float*>(stp + Lay::kU + (mi * 16 + g) * Lay::kUPitch);
+      const float* u1 =
+          reinterpret_cast<const float*>(stp + Lay::kU + (mi * 16 + g + 8) * Lay::kUPitch);
+      // B box of this warp's 64 columns
+      const uint32_t bw = st + Lay::kB + warp * RANK * 128;
 
       if constexpr (RANK == 8) {
         // k = 0..7 carry the high parts, k = 8..15 the residuals; B rows repeat.
+        const float2 v0 = *reinterpret_cast<const float2*>(u0 + 2 * q);
+        const float2 v1 = *reinterpret_cast<const float2*>(u1 + 2 * q);
         uint32_t a[4];
-        split_bf16x2(ul.v[0][0].x, ul.v[0][0].y, a[0], a[2]);
-        split_bf16x2(ul.v[0][1].x, ul.v[0][1].y, a[1], a[3]);
+        split_bf16x2(v0.x, v0.y, a[0], a[2]);
+        split_bf16x2(v1.x, v1.y, a[1], a[3]);
 #pragma unroll
         for (int nt = 0; nt < 8; nt += 4) {
           uint32_t bfr[4];
-          ldsm_x4_trans(bfr, sb + swz512(lane & 7, warp * 8 + nt + (lane >> 3)));
+          ldsm_x4_trans(bfr, bw + swz128(lane & 7, nt + (lane >> 3)));
 #pragma unroll
           for (int j = 0; j < 4; ++j) mma_bf16(acc[nt + j], a, bfr[j], bfr[j]);
         }
       } else {
 #pragma unroll
         for (int kk = 0; kk < RANK / 16; ++kk) {
+          const int kc = kk * 16 + 2 * q;
+          const float2 v00 = *reinterpret_cast<const float2*>(u0 + kc);
+          const float2 v10 = *reinterpret_cast<const float2*>(u1 + kc);
+          const float2 v01 = *reinterpret_cast<const float2*>(u0 + kc + 8);
+          const float2 v11 = *reinterpret_cast<const float2*>(u1 + kc + 8);
           uint32_t ah[4], al[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(ul.v[kk][e].x, ul.v[kk][e].y, ah[e], al[e]);
+          split_bf16x2(v00.x, v00.y, ah[0], al[0]);
+          split_bf16x2(v10.x, v10.y, ah[1], al[1]);
+          split_bf16x2(v01.x, v01.y, ah[2], al[2]);
+          split_bf16x2(v11.x, v11.y, ah[3], al[3]);
 #pragma unroll
           for (int nt = 0; nt < 8; nt += 2) {
             uint32_t bfr[4];
             const int mat = lane >> 3;
-            ldsm_x4_trans(bfr, sb + swz512(kk * 16 + ((mat & 1) << 3) + (lane & 7),
-                                           warp * 8 + nt + (mat >> 1)));
+            ldsm_x4_trans(bfr, bw + swz128(kk * 16 + ((mat & 1) << 3) + (lane & 7),
+                                           nt + (mat >> 1)));
             mma_bf16(acc[nt], ah, bfr[0], bfr[1]);
             mma_bf16(acc[nt], al, bfr[0], bfr[1]);
             mma_bf16(acc[nt + 1], ah, bfr[2], bfr[3]);
@@ -202,31 +261,51 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 128 ? 2 : 4) lora_expa
         }
       }
 
+      // staged y + acc -> bf16, written back into the stage
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const int col = colw + nt * 8 + 2 * q;
-        if (col < width) {
-          if (t0 >= 0) {
-            const float2 yf = unpack_bf16x2(yv[mi][nt][0]);
-            *reinterpret_cast<uint32_t*>(p.y + static_cast<long long>(t0) * p.y_stride + off + col) =
-                pack_bf16x2(yf.x + acc[nt][0], yf.y + acc[nt][1]);
-          }
-          if (t1 >= 0) {
-            const float2 yf = unpack_bf16x2(yv[mi][nt][1]);
-            *reinterpret_cast<uint32_t*>(p.y + static_cast<long long>(t1) * p.y_stride + off + col) =
-                pack_bf16x2(yf.x + acc[nt][2], yf.y + acc[nt][3]);
-          }
-        }
+        const int cbyte = (warp * 64 + nt * 8 + 2 * q) * 2;
+        uint32_t* y0 =
+            reinterpret_cast<uint32_t*>(stp + Lay::kY + (mi * 16 + g) * kYPitch + cbyte);
+        uint32_t* y1 =
+            reinterpret_cast<uint32_t*>(stp + Lay::kY + (mi * 16 + g + 8) * kYPitch + cbyte);
+        const float2 f0 = unpack_bf16x2(*y0);
+        const float2 f1 = unpack_bf16x2(*y1);
+        *y0 = pack_bf16x2(f0.x + acc[nt][0], f0.y + acc[nt][1]);
+        *y1 = pack_bf16x2(f1.x + acc[nt][2], f1.y + acc[nt][3]);
       }
     }
-    __syncthreads();  // before the next item overwrites the record and the B tile
+    __syncthreads();  // the updated stage is complete
+
+    // coalesced 16-byte stores of the valid rows and columns
+    {
+      const int ych = tid & 31;
+      const int col = it.c0 + ych * 8;
+#pragma unroll
+      for (int i = 0; i < BM / 4; ++i) {
+        const int row = (tid >> 5) + 4 * i;
+        const int t = record_token(rec, row, tv.count, p.max_num_tokens);
+        if (t >= 0 && col < it.width)
+          *reinterpret_cast<int4*>(p.y + static_cast<long long>(t) * p.y_stride + it.off + col) =
+              *reinterpret_cast<const int4*>(stp + Lay::kY + row * kYPitch + ych * 16);
+      }
+    }
+
+    if (NS == 1 && k + 1 < nloc) {
+      __syncthreads();  // the single stage is free again
+      if (tid == 0) fill_b(k + 1);
+      fill_uy(k + 1);
+      if (k + 2 < nloc) load_record_async<BM>(p.records, tile_of(k + 2), rec_of(k + 2));
+      cp_async_commit();
+    }
   }
+  if (timed_out) atomicOr(p.status, kStatusTimeout);
 }
 
 template <int BM, int RANK>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
   const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK>);
-  const size_t smem = static_cast<size_t>(RANK) * 512 + record_ints(BM) * sizeof(int32_t);
+  const size_t smem = ExpandLayout<BM, RANK>::kSmem;
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -245,35 +324,41 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
   ExpandParams p;
   p.u = a.u;
   p.max_num_tokens = a.max_num_tokens;
-  const __nv_bfloat16* b[3];
   int w[3] = {0, 0, 0}, off[3] = {0, 0, 0}, cbs[3] = {0, 0, 0};
   int acc_off = 0, cb_total = 0;
   for (int s = 0; s < 3; ++s) {
-    const int ss = s < a.num_slices ? s : 0;
-    b[s] = static_cast<const __nv_bfloat16*>(a.lora_b[ss]);
     if (s < a.num_slices) {
       w[s] = a.slice_width[s];
       off[s] = acc_off;
       acc_off += w[s];
       cbs[s] = (w[s] + kEN - 1) / kEN;
       cb_total += cbs[s];
+      if (make_weight_tmap(&p.tmap[s], a.lora_b[s], w[s],
+                           static_cast<long long>(a.num_loras) * a.rank, a.rank) != 0)
+        return -6;
+    } else {
+      p.tmap[s] = p.tmap[0];
     }
   }
-  p.b0 = b[0]; p.b1 = b[1]; p.b2 = b[2];
-  p.w0 = w[0]; p.w1 = w[1]; p.w2 = w[2];
-  p.off0 = off[0]; p.off1 = off[1]; p.off2 = off[2];
-  p.cb0 = cbs[0]; p.cb1 = cbs[1];
+  p.w0 = w[0];
+  p.w1 = w[1];
+  p.w2 = w[2];
+  p.off0 = off[0];
+  p.off1 = off[1];
+  p.off2 = off[2];
+  p.cb0 = cbs[0];
+  p.cb1 = cbs[1];
   p.cb_total = cb_total;
   p.y = static_cast<__nv_bfloat16*>(a.y);
   p.y_stride = a.y_row_stride;
   WsView ws = ws_view(const_cast<void*>(a.workspace), a.max_num_tokens, a.num_loras);
   p.records = ws.lists[tile_index_of(BM)];
   p.num_tiles = ws.num_tiles + tile_index_of(BM);
+  p.status = ws.status;
   p.tile_capacity =
       static_cast<int>(tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM)));
   p.num_loras = a.num_loras;
-  const long long max_items =
-      tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM)) * cb_total;
+  const long long max_items = static_cast<long long>(p.tile_capacity) * cb_total;
   switch (a.rank) {
     case 8: return run_expand<BM, 8>(p, stream, max_items);
     case 16: return run_expand<BM, 16>(p, stream, max_items);

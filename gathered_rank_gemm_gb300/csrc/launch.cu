@@ -1,6 +1,8 @@
 // Host-side launch helpers: per-device caches and the cudaLaunchKernelEx call.
 #include "launch.h"
 
+#include <cudaTypedefs.h>
+
 #include <mutex>
 #include <unordered_map>
 #include <utility>
@@ -105,6 +107,30 @@ int launch_raw(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_
   const cudaError_t e = cudaLaunchKernelExC(&cfg, func, args);
   if (e != cudaSuccess) return -5;
   return 0;
+}
+
+int make_weight_tmap(CUtensorMap* map, const void* base, long long cols, long long rows,
+                     int box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode) return -6;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? 0 : -6;
 }
 
 }  // namespace grg

@@ -1,6 +1,7 @@
 // Host-side launch helpers shared by the kernel launchers (internal).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -28,6 +29,11 @@ int launch_pdl(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_
                int cluster, P* params) {
   return launch_raw(func, grid, block, smem, stream, cluster, static_cast<void*>(params));
 }
+
+// 2-D tensor map over a row-major bf16 matrix [rows][cols] for TMA tile loads
+// of box_rows x 64 columns with the 128-byte swizzle (out of range -> zeros).
+int make_weight_tmap(CUtensorMap* map, const void* base, long long cols, long long rows,
+                     int box_rows);
 
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
                     int num_loras, int32_t* sorted_ids, int32_t* counts, int32_t* starts,

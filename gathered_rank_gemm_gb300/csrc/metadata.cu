@@ -94,8 +94,9 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   int32_t* toff = ntile + L;                   // [kNumTileSizes][L + 1]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Dependents are released only at the very end, after a fence: kernels of
+  // this library read the work list before their own dependency wait.
   pdl_wait();
-  pdl_launch_dependents();
 
   if (tid == 0) {
     int n = *p.num_tokens;
@@ -211,6 +212,9 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
     *p.ws.n = n;
     if (s_status) atomicOr(p.ws.status, s_status);
   }
+  __threadfence();
+  __syncthreads();
+  pdl_launch_dependents();
 }
 
 static size_t meta_smem_bytes(int num_loras) {

@@ -7,56 +7,66 @@
 // Work decomposition (fixed grid, graph-safe): the metadata kernel wrote a
 // list of tiles, each up to BM tokens of one LoRA.  A thread-block cluster of
 // C CTAs owns one tile at a time and splits the hidden dimension H into C
-// contiguous ranges; every CTA streams its range of the gathered x rows and of
-// the adapter's A rows (all slices stacked, S*R rows) through a 4-stage
-// cp.async ring into XOR-swizzled shared memory and multiplies them on the
-// tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate).  The C partial
-// tiles are then summed in a fixed order through distributed shared memory
-// (no atomics, no global scratch), scaled once and stored to u.  Clusters loop
-// over the tile list with a stride of the cluster count, so the grid depends
-// only on the device, never on the batch.
+// contiguous ranges; clusters walk the list with a stride of the cluster
+// count, so the grid depends only on the device.
+//
+// Data movement, per 64-column k-block, into a ring of NST stages:
+//  - the adapter's R x 64 block of every slice with one TMA tile load each
+//    (tensor map, 128-byte swizzle), completing on the stage's mbarrier;
+//  - the BM gathered x rows with 16-byte cp.async (zero-filled past the
+//    tile's tokens and past H), one commit group per stage.
+// The adapter blocks of the first tile are requested before
+// griddepcontrol.wait (weights are never written by the preceding kernel) and
+// the first x rows are prefetched into L2 there.
+//
+// Compute: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate); warps
+// split the S*R columns and/or the k-steps.  The C partial tiles are summed in
+// rank order through distributed shared memory (no atomics, no global
+// scratch), scaled once and stored to u.
 #include "common.cuh"
 #include "launch.h"
 
 namespace grg {
 
 constexpr int kShrinkThreads = 128;
-constexpr int kBK = 64;  // bf16 columns per k-block: one 128-byte row chunk
+constexpr int kBK = 64;  // bf16 columns per k-block: one 128-byte (swizzled) row chunk
 
 struct ShrinkParams {
+  CUtensorMap tmap[3];  // A_s viewed as [L * R][hidden], boxes of R x 64
   const __nv_bfloat16* x;
   long long x_stride;
   int hidden;
   int kblocks;      // ceil(hidden / kBK)
   int kb_per_rank;  // k-blocks owned by each CTA of a cluster
-  const __nv_bfloat16* a0;
-  const __nv_bfloat16* a1;
-  const __nv_bfloat16* a2;
+  int num_slices;
   int rank;
   int rank_shift;  // log2(rank)
   int sr;          // num_slices * rank: stacked A rows
   float scale;
   float* u;
   int max_num_tokens;
-  const int32_t* records;    // tile records of height BM
+  const int32_t* records;  // tile records of height BM
   const int32_t* num_tiles;
-  int tile_capacity;         // records the list can hold
+  uint32_t* status;
+  int tile_capacity;  // records the list can hold
   int num_loras;
   int warps_n;     // warps splitting the S*R columns (1, 2 or 4)
   int ntw;         // n8 column tiles per warp
-  int rec_offset;  // byte offset of the tile record in shared memory
+  int stage_bytes;
+  int rec_offset;  // byte offsets from the 1024-aligned base
+  int bar_offset;
 };
 
-// Byte offset of 16-byte chunk ch (0..7) of a 128-byte row, XOR-swizzled so
-// that eight consecutive rows read at the same chunk hit distinct banks.
-__device__ __forceinline__ uint32_t swz128(int row, int ch) {
-  return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
-}
-
 template <int BM, int NTW, int NST>
-__global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const ShrinkParams p) {
-  extern __shared__ __align__(128) unsigned char smem[];
+__global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
+    lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // TMA's 128-byte swizzle is laid out on 1024-byte boundaries
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sbase - raw);
   int32_t* rec = reinterpret_cast<int32_t*>(smem + p.rec_offset);
+  const uint32_t bars = sbase + p.bar_offset;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int SR = p.sr;
@@ -65,8 +75,6 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
   const int wn = warp % p.warps_n, wk = warp / p.warps_n;
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
-  const int stage_bytes = (BM + SR) * 128;
-  const uint32_t smem_base = smem_u32(smem);
 
   uint32_t cl_size;
   asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cl_size));
@@ -78,42 +86,75 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
   const int kb1 = min(kb0 + p.kb_per_rank, p.kblocks);
   const int nkb = max(kb1 - kb0, 0);
 
-  pdl_wait();
-  pdl_launch_dependents();
-  // the first record is fetched together with the count (it may be unused)
-  if (cluster_id < p.tile_capacity) load_record<BM>(p.records, cluster_id, rec);
+  if (tid == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(bars + 8 * s, 1);
+    fence_mbar_init();
+    for (int s = 0; s < p.num_slices; ++s) prefetch_tmap(&p.tmap[s]);
+  }
+  __syncthreads();
+
+  // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
+  uint32_t phase = 0;  // bit s: parity of the next phase of stage s
+  bool waited = false, timed_out = false;
+
+  // this thread's x chunks: rows (tid >> 3) + 16 j, chunk tid & 7
+  constexpr int XJ = BM / 16;
+  const int xch = tid & 7;
 
   for (int item = cluster_id; item < ntiles; item += nclusters) {
-    if (item != cluster_id) load_record<BM>(p.records, item, rec);
+    load_record<BM>(p.records, item, rec);
     __syncthreads();
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     const int lora = tv.lora, cnt = tv.count;
+    const __nv_bfloat16* xrow[XJ];
+#pragma unroll
+    for (int j = 0; j < XJ; ++j) {
+      const int t = record_token(rec, (tid >> 3) + 16 * j, cnt, p.max_num_tokens);
+      xrow[j] = t >= 0 ? p.x + static_cast<long long>(t) * p.x_stride + xch * 8 : nullptr;
+    }
 
-    auto load_stage = [&](int st, int kb) {
-      const uint32_t sx = smem_base + st * stage_bytes;
-      const uint32_t sw = sx + BM * 128;
-      const int col = kb * kBK;
-      for (int c = tid; c < BM * 8; c += kShrinkThreads) {
-        const int row = c >> 3, ch = c & 7;
-        const int t = record_token(rec, row, cnt, p.max_num_tokens);
-        const int kcol = col + ch * 8;
-        const bool ok = (t >= 0) && (kcol < p.hidden);
-        const __nv_bfloat16* src = ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x;
-        cp_async_16(sx + swz128(row, ch), src, ok);
-      }
-      for (int c = tid; c < SR * 8; c += kShrinkThreads) {
-        const int row = c >> 3, ch = c & 7;
-        const int s = row >> p.rank_shift;
-        const int r = row - (s << p.rank_shift);
-        const int kcol = col + ch * 8;
-        const bool ok = kcol < p.hidden && cnt > 0;
-        const __nv_bfloat16* a = s == 0 ? p.a0 : (s == 1 ? p.a1 : p.a2);
-        const __nv_bfloat16* src =
-            ok ? a + (static_cast<long long>(lora) * p.rank + r) * p.hidden + kcol : p.a0;
-        cp_async_16(sw + swz128(row, ch), src, ok);
-      }
+    // A blocks of all slices for k-block kb -> stage st (thread 0)
+    auto fill_a = [&](int st, int kb) {
+      const uint32_t bar = bars + 8 * st;
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(SR * 128));
+      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
+      for (int s = 0; s < p.num_slices; ++s)
+        tma_load_2d(sa + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
     };
+    // gathered x rows for k-block kb -> stage st (every thread, one group)
+    auto fill_x = [&](int st, int kb) {
+      const uint32_t sx = sbase + st * p.stage_bytes;
+      const int kcol = kb * kBK + xch * 8;
+#pragma unroll
+      for (int j = 0; j < XJ; ++j) {
+        const int row = (tid >> 3) + 16 * j;
+        const bool ok = xrow[j] != nullptr && kcol < p.hidden;
+        cp_async_16(sx + swz128(row, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
+      }
+      cp_async_commit();
+    };
+
+    const int npro = min(nkb, NST);
+    if (tid == 0)
+      for (int s = 0; s < npro; ++s) fill_a(s, kb0 + s);
+    if (!waited) {
+      if (npro > 0) {
+        // warm L2 (and the TLB) with this CTA's first x rows while the
+        // previous kernel finishes; the copies below then hit L2
+        const int kcol = kb0 * kBK;
+        const int bytes = min(npro * kBK, p.hidden - kcol) * 2;
+        for (int r = tid; r < cnt; r += kShrinkThreads) {
+          const int t = record_token(rec, r, cnt, p.max_num_tokens);
+          if (t >= 0) prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + kcol, bytes);
+        }
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      waited = true;
+    }
+    for (int s = 0; s < npro; ++s) fill_x(s, kb0 + s);
+    int issued = npro;
 
     float acc[BM / 16][NTW][4];
 #pragma unroll
@@ -123,21 +164,13 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
 
-    // keep NST - 1 k-blocks in flight (all of them when the range is short)
-#pragma unroll
-    for (int s = 0; s < NST - 1; ++s) {
-      if (s < nkb) load_stage(s, kb0 + s);
-      cp_async_commit();
-    }
-
     for (int i = 0; i < nkb; ++i) {
-      cp_async_wait<NST - 2>();
-      __syncthreads();
-      const int nxt = i + NST - 1;
-      if (nxt < nkb) load_stage(nxt % NST, kb0 + nxt);
-      cp_async_commit();
-
-      const uint32_t sx = smem_base + (i % NST) * stage_bytes;
+      const int st = i % NST;
+      cp_async_wait_dyn(issued - 1 - i);
+      __syncthreads();  // everyone's x chunks of this stage are in
+      if (!mbar_wait(bars + 8 * st, (phase >> st) & 1u)) timed_out = true;
+      phase ^= 1u << st;
+      const uint32_t sx = sbase + st * p.stage_bytes;
       const uint32_t sw = sx + BM * 128;
 #pragma unroll
       for (int ks = 0; ks < kBK / 16; ++ks) {
@@ -170,11 +203,16 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
           }
         }
       }
+      if (i + NST < nkb) {
+        __syncthreads();  // every warp is done with this stage
+        if (tid == 0) fill_a(st, kb0 + i + NST);
+        fill_x(st, kb0 + i + NST);
+        ++issued;
+      }
     }
-    cp_async_wait<0>();
-    __syncthreads();
+    __syncthreads();  // the ring is free: it becomes the reduction buffer
 
-    // partial tile -> red[wk][row][col] (aliases the stage ring)
+    // partial tile -> red[wk][row][col], then the k-split warps are summed into red[0]
     float* red = reinterpret_cast<float*>(smem);
     {
       const int g = lane >> 2, q = lane & 3;
@@ -192,26 +230,43 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
           }
         }
     }
+    const int e4 = (BM * SR) >> 2;
+    if (WK > 1) {
+      __syncthreads();
+      for (int idx = tid; idx < e4; idx += kShrinkThreads) {
+        float4 v = reinterpret_cast<float4*>(red)[idx];
+        for (int w = 1; w < WK; ++w) {
+          const float4 o = reinterpret_cast<float4*>(red + w * BM * SR)[idx];
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        reinterpret_cast<float4*>(red)[idx] = v;
+      }
+    }
     cluster_sync_all();
 
-    // cluster reduction in a fixed order, scale, store the valid rows
-    const int e4 = (BM * SR) >> 2;
+    // cluster reduction in rank order, scale, store the valid rows
     for (int idx = crank * kShrinkThreads + tid; idx < e4; idx += C * kShrinkThreads) {
       const int e = idx << 2;
       const int row = e / SR;
       const int col = e - row * SR;
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
       if (t < 0) continue;
-      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < C; ++c) {
-        for (int w = 0; w < WK; ++w) {
-          const uint32_t local =
-              smem_base + static_cast<uint32_t>(((w * BM + row) * SR + col) * 4);
-          const float4 v = ld_dsmem_f4(mapa_shared(local, static_cast<uint32_t>(c)));
-          sum.x += v.x;
-          sum.y += v.y;
-          sum.z += v.z;
-          sum.w += v.w;
+      const uint32_t local = sbase + static_cast<uint32_t>(e * 4);
+      float4 part[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        if (c < C) part[c] = ld_dsmem_f4(mapa_shared(local, static_cast<uint32_t>(c)));
+      float4 sum = part[0];
+#pragma unroll
+      for (int c = 1; c < 8; ++c) {
+        if (c < C) {
+          sum.x += part[c].x;
+          sum.y += part[c].y;
+          sum.z += part[c].z;
+          sum.w += part[c].w;
         }
       }
       const int s = col >> p.rank_shift;
@@ -220,8 +275,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 4) lora_shrink_kernel(const Sh
       *reinterpret_cast<float4*>(dst) =
           make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
     }
+    fence_proxy_async();  // generic use of the ring before the next item's TMA writes
     cluster_sync_all();
   }
+  if (timed_out) atomicOr(p.status, kStatusTimeout);
 }
 
 template <int BM, int NTW, int NST>
@@ -252,23 +309,32 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int kblocks = (a.hidden + kBK - 1) / kBK;
   const long long max_tiles = tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM));
   const int sms = device_sm_count();
+  // split the hidden dimension over a cluster until ~3 CTAs per SM have work
   int cluster = 1;
-  while (cluster < 8 && static_cast<long long>(cluster) * 2 * max_tiles <= 2LL * sms) cluster *= 2;
-  while (cluster > 1 && cluster > kblocks) cluster /= 2;
+  while (cluster < 8 && static_cast<long long>(cluster) * max_tiles < 3LL * sms &&
+         kblocks >= 8 * cluster)
+    cluster *= 2;
   const int kb_per = (kblocks + cluster - 1) / cluster;
-  // deep ring when a CTA's whole k-range fits: every load is in flight at once
-  const size_t stage = static_cast<size_t>(BM + SR) * 128;
-  const int nst = (kb_per <= 8 && 8 * stage <= 96 * 1024 && ntw <= 8) ? 8 : 4;
+  // a deep ring keeps up to 8 k-blocks in flight per CTA (all of a short range)
+  const int stage = (BM + SR) * 128;  // a multiple of 1024: BM and S*R are multiples of 8
+  const int nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
 
   ShrinkParams p;
+  for (int s = 0; s < 3; ++s) {
+    if (s < a.num_slices) {
+      if (make_weight_tmap(&p.tmap[s], a.lora_a[s], a.hidden,
+                           static_cast<long long>(a.num_loras) * a.rank, a.rank) != 0)
+        return -6;
+    } else {
+      p.tmap[s] = p.tmap[0];
+    }
+  }
   p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.x_stride = a.x_row_stride;
   p.hidden = a.hidden;
   p.kblocks = kblocks;
   p.kb_per_rank = kb_per;
-  p.a0 = static_cast<const __nv_bfloat16*>(a.lora_a[0]);
-  p.a1 = static_cast<const __nv_bfloat16*>(a.num_slices > 1 ? a.lora_a[1] : a.lora_a[0]);
-  p.a2 = static_cast<const __nv_bfloat16*>(a.num_slices > 2 ? a.lora_a[2] : a.lora_a[0]);
+  p.num_slices = a.num_slices;
   p.rank = a.rank;
   p.rank_shift = __builtin_ctz(static_cast<unsigned>(a.rank));
   p.sr = SR;
@@ -278,23 +344,31 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   WsView ws = ws_view(const_cast<void*>(a.workspace), a.max_num_tokens, a.num_loras);
   p.records = ws.lists[tile_index_of(BM)];
   p.num_tiles = ws.num_tiles + tile_index_of(BM);
+  p.status = ws.status;
   p.tile_capacity = static_cast<int>(max_tiles);
   p.num_loras = a.num_loras;
   p.warps_n = warps_n;
   p.ntw = ntw;
-  const size_t ring = static_cast<size_t>(nst) * stage;
-  const size_t red = static_cast<size_t>(WK) * BM * SR * 4;
-  const size_t body = ring > red ? ring : red;
-  p.rec_offset = static_cast<int>(body);
-  const size_t smem = body + record_ints(BM) * sizeof(int32_t);
+  p.stage_bytes = stage;
+  const int ring = nst * stage;
+  const int red = WK * BM * SR * 4;
+  const int body = ((ring > red ? ring : red) + 127) / 128 * 128;
+  p.rec_offset = body;
+  p.bar_offset = body + record_ints(BM) * 4;
+  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 8 * 8;
 
   if (BM == 16) {
-    if (ntw > 8) return run_shrink<16, 12, 4>(p, cluster, smem, stream, max_tiles);
+    if (ntw > 8) {
+      if (nst == 4) return run_shrink<16, 12, 4>(p, cluster, smem, stream, max_tiles);
+      return run_shrink<16, 12, 2>(p, cluster, smem, stream, max_tiles);
+    }
     if (nst == 8) return run_shrink<16, 8, 8>(p, cluster, smem, stream, max_tiles);
-    return run_shrink<16, 8, 4>(p, cluster, smem, stream, max_tiles);
+    if (nst == 4) return run_shrink<16, 8, 4>(p, cluster, smem, stream, max_tiles);
+    return run_shrink<16, 8, 2>(p, cluster, smem, stream, max_tiles);
   }
   if (nst == 8) return run_shrink<32, 8, 8>(p, cluster, smem, stream, max_tiles);
-  return run_shrink<32, 8, 4>(p, cluster, smem, stream, max_tiles);
+  if (nst == 4) return run_shrink<32, 8, 4>(p, cluster, smem, stream, max_tiles);
+  return run_shrink<32, 8, 2>(p, cluster, smem, stream, max_tiles);
 }
 
 }  // namespace grg
