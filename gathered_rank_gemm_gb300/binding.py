@@ -22,8 +22,10 @@ LORA_MAX_SLICES = 3
 LORA_MAX_LORAS = 1024
 LORA_MAX_NUM_TOKENS = 1 << 22
 
+LORA_NOALLOC_SCRATCH_BYTES = 384 * 1024
+
 EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora_expand",
-            "lora_read_status", "lora_error_string")
+            "lora_read_status", "lora_error_string", "lora_apply_noalloc")
 
 _lib = None
 
@@ -59,6 +61,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_read_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), p]
     lib.lora_error_string.restype = ctypes.c_char_p
     lib.lora_error_string.argtypes = [i32]
+    lib.lora_apply_noalloc.restype = i32
+    lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
+                                       ctypes.c_float, p, p, i64, p, p, p, p, p]
     _lib = lib
     return lib
 
@@ -142,6 +147,34 @@ def lora_read_status(workspace, stream=None) -> int:
                                  _stream_ptr(stream, workspace.device))
     _check("lora_read_status", rc)
     return int(out.value)
+
+
+def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale: float, u, y,
+                       sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
+                       status=None, stream=None):
+    """Grouping + shrink + expand of one layer without any allocation.
+
+    For callers that cannot allocate device memory: the workspace is the
+    library's static device array (LORA_NOALLOC_SCRATCH_BYTES), shared by all
+    calls, so calls that overlap on the GPU race.  The first call on a device
+    looks the array up; make it before any stream capture.  ``status``: an
+    optional int32 CUDA tensor of one element receiving the status bits.
+    """
+    lora_a, lora_b = list(lora_a), list(lora_b)
+    arr_a = _ptr_array(lora_a, "lora_a")
+    arr_b = _ptr_array(lora_b, "lora_b")
+    widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
+    num_loras, rank, hidden = lora_a[0].shape
+    rc = load().lora_apply_noalloc(
+        _dev(token_lora_mapping, "token_lora_mapping"), _dev(num_tokens, "num_tokens"),
+        token_lora_mapping.shape[0], num_loras, _dev(x, "x"), x.stride(0), hidden,
+        ctypes.addressof(arr_a), ctypes.addressof(arr_b), ctypes.addressof(widths), len(lora_a),
+        rank, float(scale), _dev(u, "u"), _dev(y, "y"), y.stride(0),
+        _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(num_tokens_per_lora, "num_tokens_per_lora"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"),
+        None if status is None else _dev(status, "status"), _stream_ptr(stream, x.device))
+    _check("lora_apply_noalloc", rc)
 
 
 # ------------------------------------------------------------------ buffers

@@ -161,6 +161,41 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
  */
 int lora_read_status(void *workspace, uint32_t *status, void *stream);
 
+/*
+ * One layer - grouping, shrink and expand - without allocating anything.
+ * The paper has no counterpart to this call: it exists for callers that
+ * cannot call cudaMalloc (a memory manager that owns the whole device, a
+ * plugin host that hands out no device memory, code that must not allocate)
+ * and so cannot provide the workspace the three calls above take.
+ *
+ * Arguments are those of lora_prepare_metadata, lora_shrink and lora_expand
+ * (same meaning, layout and rules), minus the workspace; the caller still
+ * passes every input and output, u and the three metadata arrays included.
+ * `status` (optional, device pointer) receives this call's LORA_STATUS_* bits.
+ *
+ * The workspace is a file-scope device array of LORA_NOALLOC_SCRATCH_BYTES
+ * (384 KB) in the library, which every GPU that loads the library holds
+ * until the process exits.  It fits 8192 tokens with 128 adapters; sizes
+ * whose workspace (lora_workspace_size) exceeds it are rejected with
+ * LORA_ERR_WORKSPACE before anything is enqueued.  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current): make that first call before any stream capture.  Every
+ * call uses the same array and leaves its contents behind; the call clears
+ * the status word it needs zeroed itself.  Calls that overlap on the GPU
+ * (other streams, other threads) race on the array: serialise them.  An
+ * argument error in the shrink or expand step is reported after the earlier
+ * steps of the same call were enqueued.
+ */
+#define LORA_NOALLOC_SCRATCH_BYTES (384 * 1024)
+int lora_apply_noalloc(const int32_t *token_lora_mapping, const int32_t *num_tokens,
+                       int64_t max_num_tokens, int64_t max_loras, const uint16_t *x,
+                       int64_t x_row_stride, int64_t hidden, const uint16_t *const *lora_a,
+                       const uint16_t *const *lora_b, const int64_t *slice_width,
+                       int num_slices, int rank, float scale, float *u, uint16_t *y,
+                       int64_t y_row_stride, int32_t *sorted_token_ids,
+                       int32_t *num_tokens_per_lora, int32_t *lora_token_start_loc,
+                       uint32_t *status, void *stream);
+
 /* Static text for a LORA_OK / LORA_ERR_* code. */
 const char *lora_error_string(int code);
 
