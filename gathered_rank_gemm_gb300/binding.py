@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgathered
 LORA_OK = 0
 LORA_STATUS_BAD_LORA_ID = 0x1
 LORA_STATUS_BAD_NUM_TOKENS = 0x2
+LORA_STATUS_TIMEOUT = 0x4
 LORA_MAX_SLICES = 3
 LORA_MAX_LORAS = 1024
 LORA_MAX_NUM_TOKENS = 1 << 22

@@ -66,6 +66,7 @@ extern "C" {
 
 #define LORA_STATUS_BAD_LORA_ID 0x1u     /* some m[t], t < n, was outside [-1, L) */
 #define LORA_STATUS_BAD_NUM_TOKENS 0x2u  /* n was outside [0, max_num_tokens]; clamped */
+#define LORA_STATUS_TIMEOUT 0x4u         /* a kernel's bounded wait for its own copies gave up */
 
 #define LORA_MAX_SLICES 3
 #define LORA_MAX_LORAS 1024
@@ -73,10 +74,12 @@ extern "C" {
 
 /*
  * Bytes of device workspace that lora_prepare_metadata fills and lora_shrink /
- * lora_expand read: a status word, the clamped n and per-tile work lists for
- * the fixed-grid kernels.  Grows as max_num_tokens / 16 + 4 * max_loras
- * entries of 8 bytes (about 22 KB at 8192 tokens and 128 LoRAs).  Returns 0
- * for sizes outside the supported range.
+ * lora_expand read: a status word, the clamped n and, for tile heights of
+ * 16, 32, 64 and 128 tokens, the list of tile records (adapter, count and the
+ * tile's token ids) that the fixed-grid kernels walk.  About 4 * 4 bytes per
+ * token plus 1 KB per adapter (277 KB at 8192 tokens and 128 LoRAs).  Returns
+ * 0 for sizes outside the supported range.  Besides the grouping kernel, the
+ * shrink and expand kernels may OR LORA_STATUS_TIMEOUT into its status word.
  */
 size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras);
 
