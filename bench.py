@@ -42,6 +42,7 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {"expand": "gathered_rank_gemm_gb300/csrc/expand.cu",
                   "shrink": "gathered_rank_gemm_gb300/csrc/shrink.cu",
+                  "shrink_expand": "gathered_rank_gemm_gb300/csrc/fused.cu",
                   "metadata": "gathered_rank_gemm_gb300/csrc/metadata.cu"}
 
 
@@ -303,13 +304,20 @@ def run_ours(args, world, rank, local):
           for _ in wl.layers]
     torch.cuda.synchronize()
 
+    # per layer, one lora_shrink_expand call: one fused kernel when the batch
+    # fits on chip, else the shrink and expand kernels back to back
+    per_layer_kernels = binding.lora_shrink_expand_kernels(T, L, shape.hidden,
+                                                           shape.slice_widths, shape.rank)
+
     def step(which="all"):
-        if which in ("all", "metadata"):
+        if which in ("all", "metadata", "profile"):
             meta.prepare(mapping, n_dev, stream)
         for k in range(layers):
-            if which in ("all", "shrink"):
+            if which in ("all", "one_call", "profile"):
+                meta.shrink_expand(xs[k], As[k], Bs[k], shape.scale, us[k], ys[k], stream)
+            if which == "shrink":
                 meta.shrink(xs[k], As[k], shape.scale, us[k], stream)
-            if which in ("all", "expand"):
+            if which == "expand":
                 meta.expand(us[k], Bs[k], ys[k], stream)
 
     graphs = {}
@@ -325,7 +333,7 @@ def run_ours(args, world, rank, local):
             print(json.dumps({"mode": "profile", "workload": shape.name, "layers": layers,
                               "steps": args.steps, "launches": (1 + 2 * layers) * (args.steps + 1)}))
         return 0
-    for which in ("all", "metadata", "shrink", "expand"):
+    for which in ("all", "metadata", "one_call", "shrink", "expand"):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             step(which)
@@ -365,6 +373,7 @@ def run_ours(args, world, rank, local):
     ms_step = e0.elapsed_time(e1) / args.steps
     # per-kernel launch times (each graph launches that kernel `layers` times)
     ms_meta = time_graph(graphs["metadata"], args.steps, 3)
+    ms_one = time_graph(graphs["one_call"], args.steps, 3) / layers
     ms_shrink = time_graph(graphs["shrink"], args.steps, 3) / layers
     ms_expand = time_graph(graphs["expand"], args.steps, 3) / layers
     clk = clocks.stop()
@@ -406,12 +415,19 @@ def run_ours(args, world, rank, local):
 
     alg = algorithmic_bytes(shape, wl.mapping)
     peak, peak_kind = load_peaks()
-    dominant = "expand" if alg["expand"] >= alg["shrink"] else "shrink"
-    t_dom = ms_expand if dominant == "expand" else ms_shrink
-    achieved = alg[dominant] / (t_dom * 1e-3) / 1e9
+    if per_layer_kernels == 1:
+        # one fused kernel per layer: it moves the bytes of both steps
+        dominant, kernel_name = "shrink_expand", "lora_fused_kernel"
+        dom_bytes, t_dom = alg["shrink"] + alg["expand"], ms_one
+    else:
+        dominant = "expand" if alg["expand"] >= alg["shrink"] else "shrink"
+        kernel_name = f"lora_{dominant}_kernel"
+        dom_bytes = alg[dominant]
+        t_dom = ms_expand if dominant == "expand" else ms_shrink
+    achieved = dom_bytes / (t_dom * 1e-3) / 1e9
     value = n * layers * world / (ms_step_max * 1e-3)
     e2e_value = n * layers * world / (ms_e2e * 1e-3)
-    launches = (1 + 2 * layers) * args.steps
+    launches = (1 + per_layer_kernels * layers) * args.steps
 
     result = None
     if rank == 0:
@@ -426,18 +442,20 @@ def run_ours(args, world, rank, local):
                        "max_loras": L, "rank": shape.rank, "layers_per_step": layers,
                        "l2": f"inputs larger than L2: {layers} distinct layers, "
                              f"{layers * per_layer / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
-                       "graph": "one CUDA graph per step (grouping + shrink/expand per layer)",
+                       "graph": "one CUDA graph per step: grouping, then one lora_shrink_expand call per layer",
                        "parallelism": f"replicas x{world} (independent batches, no collective)"},
-            "roofline": {"bound": "hbm", "kernel": f"lora_{dominant}_kernel",
+            "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "algorithmic_bytes_per_launch": alg[dominant],
+                         "algorithmic_bytes_per_launch": dom_bytes,
                          "traffic": recorded_traffic(dominant, shape.name)},
-            "kernels_us": {"metadata": 1e3 * ms_meta, "shrink": 1e3 * ms_shrink,
-                           "expand": 1e3 * ms_expand,
+            "kernels_per_layer": per_layer_kernels,
+            "kernels_us": {"metadata": 1e3 * ms_meta, "shrink_expand_one_call": 1e3 * ms_one,
+                           "shrink": 1e3 * ms_shrink, "expand": 1e3 * ms_expand,
                            "layer_in_graph": 1e3 * ms_step / layers},
             "hbm_gbs": {"shrink": alg["shrink"] / (ms_shrink * 1e-3) / 1e9,
                         "expand": alg["expand"] / (ms_expand * 1e-3) / 1e9,
+                        "shrink_expand_one_call": (alg["shrink"] + alg["expand"]) / (ms_one * 1e-3) / 1e9,
                         "layer": (alg["shrink"] + alg["expand"]) / (ms_step / layers * 1e-3) / 1e9},
             "tflops": {"shrink": alg["flops"]["shrink"] / (ms_shrink * 1e-3) / 1e12,
                        "expand": alg["flops"]["expand"] / (ms_expand * 1e-3) / 1e12},

@@ -4,8 +4,10 @@ The compute lives in the CUDA library ``libgathered_rank_gemm.so`` (C ABI in
 ``include/gathered_rank_gemm.h``); ``binding`` is its thin ctypes wrapper and
 ``workloads`` draws seeded synthetic inputs.
 """
-from .binding import (LoraError, LoraMetadata, lora_expand, lora_prepare_metadata,  # noqa: F401
-                      lora_read_status, lora_shrink, lora_workspace_size)
+from .binding import (LoraError, LoraMetadata, lora_apply_noalloc, lora_expand,  # noqa: F401
+                      lora_prepare_metadata, lora_read_status, lora_shrink, lora_shrink_expand,
+                      lora_workspace_size)
 
-__all__ = ["LoraError", "LoraMetadata", "lora_expand", "lora_prepare_metadata",
-           "lora_read_status", "lora_shrink", "lora_workspace_size"]
+__all__ = ["LoraError", "LoraMetadata", "lora_apply_noalloc", "lora_expand",
+           "lora_prepare_metadata", "lora_read_status", "lora_shrink", "lora_shrink_expand",
+           "lora_workspace_size"]

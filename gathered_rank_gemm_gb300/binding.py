@@ -26,7 +26,8 @@ LORA_MAX_NUM_TOKENS = 1 << 22
 LORA_NOALLOC_SCRATCH_BYTES = 384 * 1024
 
 EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora_expand",
-            "lora_read_status", "lora_error_string", "lora_apply_noalloc")
+            "lora_read_status", "lora_error_string", "lora_apply_noalloc",
+            "lora_shrink_expand", "lora_shrink_expand_kernels")
 
 _lib = None
 
@@ -62,6 +63,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_read_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32), p]
     lib.lora_error_string.restype = ctypes.c_char_p
     lib.lora_error_string.argtypes = [i32]
+    lib.lora_shrink_expand.restype = i32
+    lib.lora_shrink_expand.argtypes = [p, i64, i64, p, p, p, i32, i32, ctypes.c_float, p, p, i64,
+                                       p, p, i64, i64, p, sz, p]
+    lib.lora_shrink_expand_kernels.restype = i32
+    lib.lora_shrink_expand_kernels.argtypes = [i64, i64, i64, p, i32, i32]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, i64, p, p, p, p, p]
@@ -141,6 +147,35 @@ def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace,
     _check("lora_expand", rc)
 
 
+def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
+                       lora_token_start_loc, workspace, stream=None):
+    """Shrink then expand in one call (one fused kernel for decode-sized batches)."""
+    lora_a, lora_b = list(lora_a), list(lora_b)
+    arr_a = _ptr_array(lora_a, "lora_a")
+    arr_b = _ptr_array(lora_b, "lora_b")
+    widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
+    num_loras, rank, hidden = lora_a[0].shape
+    rc = load().lora_shrink_expand(
+        _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr_a), ctypes.addressof(arr_b),
+        ctypes.addressof(widths), len(lora_a), rank, float(scale), _dev(u, "u"), _dev(y, "y"),
+        y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, x.device))
+    _check("lora_shrink_expand", rc)
+
+
+def lora_shrink_expand_kernels(max_num_tokens: int, max_loras: int, hidden: int, slice_widths,
+                               rank: int) -> int:
+    """Kernels lora_shrink_expand launches for a shape (1 fused, 2 separate)."""
+    w = (ctypes.c_int64 * len(slice_widths))(*[int(v) for v in slice_widths])
+    rc = load().lora_shrink_expand_kernels(int(max_num_tokens), int(max_loras), int(hidden),
+                                           ctypes.addressof(w), len(slice_widths), int(rank))
+    if rc < 0:
+        _check("lora_shrink_expand_kernels", rc)
+    return int(rc)
+
+
 def lora_read_status(workspace, stream=None) -> int:
     """Status bits OR-ed since the last read (synchronises the stream, clears them)."""
     out = ctypes.c_uint32(0)
@@ -208,6 +243,10 @@ class LoraMetadata:
     def expand(self, u, lora_b, y, stream=None):
         lora_expand(u, lora_b, y, self.sorted_token_ids, self.lora_token_start_loc,
                     self.workspace, stream)
+
+    def shrink_expand(self, x, lora_a, lora_b, scale, u, y, stream=None):
+        lora_shrink_expand(x, lora_a, lora_b, scale, u, y, self.sorted_token_ids,
+                           self.lora_token_start_loc, self.workspace, stream)
 
     def read_status(self, stream=None) -> int:
         return lora_read_status(self.workspace, stream)

@@ -22,6 +22,86 @@ bool rank_ok(int rank) {
 constexpr int64_t kMaxHidden = 1 << 20;
 constexpr int64_t kMaxWidth = 1 << 20;
 
+// Argument checks of lora_shrink; fills the launcher's arguments.
+int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                const uint16_t* const* lora_a, int num_slices, int rank, float scale, float* u,
+                const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                size_t workspace_bytes, grg::ShrinkArgs* out) {
+  if (!x || !lora_a || !u || !sorted_token_ids || !lora_token_start_loc || !workspace)
+    return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+  for (int s = 0; s < num_slices; ++s)
+    if (!lora_a[s]) return LORA_ERR_NULL;
+  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || hidden < 8 ||
+      hidden > kMaxHidden || (hidden % 8) != 0 || x_row_stride < hidden)
+    return LORA_ERR_SHAPE;
+  if (!aligned16(x) || (x_row_stride % 8) != 0 || !aligned16(u) || !aligned16(workspace))
+    return LORA_ERR_ALIGN;
+  for (int s = 0; s < num_slices; ++s)
+    if (!aligned16(lora_a[s])) return LORA_ERR_ALIGN;
+  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_WORKSPACE;
+  grg::ShrinkArgs& a = *out;
+  a.x = x;
+  a.x_row_stride = x_row_stride;
+  a.hidden = static_cast<int>(hidden);
+  for (int s = 0; s < 3; ++s) a.lora_a[s] = s < num_slices ? lora_a[s] : lora_a[0];
+  a.num_slices = num_slices;
+  a.rank = rank;
+  a.scale = scale;
+  a.u = u;
+  a.sorted_ids = sorted_token_ids;
+  a.starts = lora_token_start_loc;
+  a.max_num_tokens = static_cast<int>(max_num_tokens);
+  a.num_loras = static_cast<int>(max_loras);
+  a.workspace = workspace;
+  return LORA_OK;
+}
+
+// Argument checks of lora_expand; fills the launcher's arguments.
+int expand_args(const float* u, const uint16_t* const* lora_b, const int64_t* slice_width,
+                int num_slices, int rank, uint16_t* y, int64_t y_row_stride,
+                const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                size_t workspace_bytes, grg::ExpandArgs* out) {
+  if (!u || !lora_b || !slice_width || !y || !sorted_token_ids || !lora_token_start_loc ||
+      !workspace)
+    return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
+  int64_t total = 0;
+  for (int s = 0; s < num_slices; ++s) {
+    if (!lora_b[s]) return LORA_ERR_NULL;
+    if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0)
+      return LORA_ERR_SHAPE;
+    total += slice_width[s];
+  }
+  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || y_row_stride < total)
+    return LORA_ERR_SHAPE;
+  if (!aligned16(u) || !aligned16(y) || (y_row_stride % 8) != 0 || !aligned16(workspace))
+    return LORA_ERR_ALIGN;
+  for (int s = 0; s < num_slices; ++s)
+    if (!aligned16(lora_b[s])) return LORA_ERR_ALIGN;
+  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_WORKSPACE;
+  grg::ExpandArgs& a = *out;
+  a.u = u;
+  for (int s = 0; s < 3; ++s) {
+    a.lora_b[s] = s < num_slices ? lora_b[s] : lora_b[0];
+    a.slice_width[s] = s < num_slices ? static_cast<int>(slice_width[s]) : 0;
+  }
+  a.num_slices = num_slices;
+  a.rank = rank;
+  a.y = y;
+  a.y_row_stride = y_row_stride;
+  a.sorted_ids = sorted_token_ids;
+  a.starts = lora_token_start_loc;
+  a.max_num_tokens = static_cast<int>(max_num_tokens);
+  a.num_loras = static_cast<int>(max_loras);
+  a.workspace = workspace;
+  return LORA_OK;
+}
+
 }  // namespace
 
 #pragma GCC visibility push(default)
@@ -58,34 +138,11 @@ int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, void* stream) {
-  if (!x || !lora_a || !u || !sorted_token_ids || !lora_token_start_loc || !workspace)
-    return LORA_ERR_NULL;
-  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
-  for (int s = 0; s < num_slices; ++s)
-    if (!lora_a[s]) return LORA_ERR_NULL;
-  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || hidden < 8 ||
-      hidden > kMaxHidden || (hidden % 8) != 0 || x_row_stride < hidden)
-    return LORA_ERR_SHAPE;
-  if (!aligned16(x) || (x_row_stride % 8) != 0 || !aligned16(u) || !aligned16(workspace))
-    return LORA_ERR_ALIGN;
-  for (int s = 0; s < num_slices; ++s)
-    if (!aligned16(lora_a[s])) return LORA_ERR_ALIGN;
-  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
-    return LORA_ERR_WORKSPACE;
   grg::ShrinkArgs a;
-  a.x = x;
-  a.x_row_stride = x_row_stride;
-  a.hidden = static_cast<int>(hidden);
-  for (int s = 0; s < 3; ++s) a.lora_a[s] = s < num_slices ? lora_a[s] : lora_a[0];
-  a.num_slices = num_slices;
-  a.rank = rank;
-  a.scale = scale;
-  a.u = u;
-  a.sorted_ids = sorted_token_ids;
-  a.starts = lora_token_start_loc;
-  a.max_num_tokens = static_cast<int>(max_num_tokens);
-  a.num_loras = static_cast<int>(max_loras);
-  a.workspace = workspace;
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, u,
+                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
   return grg::launch_shrink(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -94,41 +151,56 @@ int lora_expand(const float* u, const uint16_t* const* lora_b, const int64_t* sl
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, void* stream) {
-  if (!u || !lora_b || !slice_width || !y || !sorted_token_ids || !lora_token_start_loc ||
-      !workspace)
-    return LORA_ERR_NULL;
-  if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
-  int64_t total = 0;
+  grg::ExpandArgs a;
+  const int rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride,
+                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
+  return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                       const uint16_t* const* lora_a, const uint16_t* const* lora_b,
+                       const int64_t* slice_width, int num_slices, int rank, float scale,
+                       float* u, uint16_t* y, int64_t y_row_stride,
+                       const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                       int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  grg::ShrinkArgs sa;
+  grg::ExpandArgs ea;
+  int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, u,
+                       sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                       workspace, workspace_bytes, &sa);
+  if (rc != LORA_OK) return rc;
+  rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride, sorted_token_ids,
+                   lora_token_start_loc, max_num_tokens, max_loras, workspace, workspace_bytes,
+                   &ea);
+  if (rc != LORA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = grg::launch_fused(sa, ea, s);
+  if (rc < 0) return rc;
+  if (rc == 1) return LORA_OK;
+  rc = grg::launch_shrink(sa, s);
+  if (rc != LORA_OK) return rc;
+  return grg::launch_expand(ea, s);
+}
+
+int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,
+                               const int64_t* slice_width, int num_slices, int rank) {
+  if (!slice_width) return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES || !sizes_ok(max_num_tokens, max_loras) ||
+      !rank_ok(rank) || hidden < 8 || hidden > kMaxHidden || (hidden % 8) != 0)
+    return LORA_ERR_SHAPE;
+  int w[3] = {0, 0, 0};
   for (int s = 0; s < num_slices; ++s) {
-    if (!lora_b[s]) return LORA_ERR_NULL;
     if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0)
       return LORA_ERR_SHAPE;
-    total += slice_width[s];
+    w[s] = static_cast<int>(slice_width[s]);
   }
-  if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || y_row_stride < total)
-    return LORA_ERR_SHAPE;
-  if (!aligned16(u) || !aligned16(y) || (y_row_stride % 8) != 0 || !aligned16(workspace))
-    return LORA_ERR_ALIGN;
-  for (int s = 0; s < num_slices; ++s)
-    if (!aligned16(lora_b[s])) return LORA_ERR_ALIGN;
-  if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
-    return LORA_ERR_WORKSPACE;
-  grg::ExpandArgs a;
-  a.u = u;
-  for (int s = 0; s < 3; ++s) {
-    a.lora_b[s] = s < num_slices ? lora_b[s] : lora_b[0];
-    a.slice_width[s] = s < num_slices ? static_cast<int>(slice_width[s]) : 0;
-  }
-  a.num_slices = num_slices;
-  a.rank = rank;
-  a.y = y;
-  a.y_row_stride = y_row_stride;
-  a.sorted_ids = sorted_token_ids;
-  a.starts = lora_token_start_loc;
-  a.max_num_tokens = static_cast<int>(max_num_tokens);
-  a.num_loras = static_cast<int>(max_loras);
-  a.workspace = workspace;
-  return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
+  return grg::fused_fits(static_cast<int>(max_num_tokens), static_cast<int>(max_loras),
+                         static_cast<int>(hidden), w, num_slices, rank)
+             ? 1
+             : 2;
 }
 
 int lora_read_status(void* workspace, uint32_t* status, void* stream) {

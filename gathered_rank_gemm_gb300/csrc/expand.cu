@@ -319,8 +319,8 @@ static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long ma
                     &p);
 }
 
-int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
-  constexpr int BM = 32;
+template <int BM>
+static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   ExpandParams p;
   p.u = a.u;
   p.max_num_tokens = a.max_num_tokens;
@@ -367,6 +367,13 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
     case 128: return run_expand<BM, 128>(p, stream, max_items);
     default: return -3;
   }
+}
+
+int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
+  // small batches: 16-token tiles give more, shorter items (latency); large
+  // batches: 32-token tiles amortise each item's B block over more rows
+  if (a.max_num_tokens <= 1024) return launch_expand_bm<16>(a, stream);
+  return launch_expand_bm<32>(a, stream);
 }
 
 }  // namespace grg

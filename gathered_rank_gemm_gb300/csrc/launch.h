@@ -72,4 +72,12 @@ struct ExpandArgs {
 };
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
 
+// Fused shrink -> expand: 1 when launched, 0 when the shape does not fit the
+// fused kernel (run launch_shrink + launch_expand instead), < 0 on error.
+int launch_fused(const ShrinkArgs& s, const ExpandArgs& e, cudaStream_t stream);
+// 1 when lora_shrink_expand would run the fused kernel for this shape on the
+// current device.
+int fused_fits(int max_num_tokens, int num_loras, int hidden, const int* widths, int num_slices,
+               int rank);
+
 }  // namespace grg

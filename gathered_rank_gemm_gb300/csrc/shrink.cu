@@ -10,25 +10,27 @@
 // contiguous ranges; clusters walk the list with a stride of the cluster
 // count, so the grid depends only on the device.
 //
-// Data movement, per 64-column k-block, into a ring of NST stages:
-//  - the adapter's R x 64 block of every slice with one TMA tile load each
-//    (tensor map, 128-byte swizzle), completing on the stage's mbarrier;
-//  - the BM gathered x rows with 16-byte cp.async (zero-filled past the
-//    tile's tokens and past H), one commit group per stage.
+// Warp-specialised pipeline over 64-column k-blocks and a ring of NST stages:
+//  - a producer warp fills a stage with the adapter's R x 64 block of every
+//    slice (one TMA tile load each: tensor map, 128-byte swizzle) and the BM
+//    gathered x rows (16-byte cp.async, zero-filled past the tile's tokens and
+//    past H); TMA bytes and the lanes' cp.async arrivals complete the stage's
+//    "full" mbarrier;
+//  - four consumer warps wait on "full", run the tensor-core MMAs (mma.sync
+//    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
+//    mbarrier; no block-wide barrier inside the k-loop.
 // The adapter blocks of the first tile are requested before
 // griddepcontrol.wait (weights are never written by the preceding kernel) and
-// the first x rows are prefetched into L2 there.
-//
-// Compute: tensor cores (mma.sync m16n8k16, bf16 in, fp32 accumulate); warps
-// split the S*R columns and/or the k-steps.  The C partial tiles are summed in
-// rank order through distributed shared memory (no atomics, no global
-// scratch), scaled once and stored to u.
+// the first x rows are prefetched into L2 there.  The C partial tiles are
+// summed in rank order through distributed shared memory (no atomics, no
+// global scratch), scaled once and stored to u.
 #include "common.cuh"
 #include "launch.h"
 
 namespace grg {
 
-constexpr int kShrinkThreads = 128;
+constexpr int kConsumerWarps = 4;
+constexpr int kShrinkThreads = 32 * (kConsumerWarps + 1);  // + one producer warp
 constexpr int kBK = 64;  // bf16 columns per k-block: one 128-byte (swizzled) row chunk
 
 struct ShrinkParams {
@@ -50,15 +52,15 @@ struct ShrinkParams {
   uint32_t* status;
   int tile_capacity;  // records the list can hold
   int num_loras;
-  int warps_n;     // warps splitting the S*R columns (1, 2 or 4)
-  int ntw;         // n8 column tiles per warp
+  int warps_n;     // consumer warps splitting the S*R columns (1, 2 or 4)
+  int ntw;         // n8 column tiles per consumer warp
   int stage_bytes;
   int rec_offset;  // byte offsets from the 1024-aligned base
-  int bar_offset;
+  int bar_offset;  // full[NST] then empty[NST]
 };
 
 template <int BM, int NTW, int NST>
-__global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
+__global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW > 8) ? 3 : 4)
     lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // TMA's 128-byte swizzle is laid out on 1024-byte boundaries
@@ -66,12 +68,14 @@ __global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (sbase - raw);
   int32_t* rec = reinterpret_cast<int32_t*>(smem + p.rec_offset);
-  const uint32_t bars = sbase + p.bar_offset;
+  const uint32_t full_bar = sbase + p.bar_offset;
+  const uint32_t empty_bar = full_bar + 8 * NST;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool producer = warp == kConsumerWarps;
   const int SR = p.sr;
   const int NT = SR >> 3;
-  const int WK = 4 / p.warps_n;
+  const int WK = kConsumerWarps / p.warps_n;
   const int wn = warp % p.warps_n, wk = warp / p.warps_n;
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
@@ -87,7 +91,10 @@ __global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
   const int nkb = max(kb1 - kb0, 0);
 
   if (tid == 0) {
-    for (int s = 0; s < NST; ++s) mbar_init(bars + 8 * s, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full_bar + 8 * s, 1 + kShrinkThreads);  // expect_tx + one per thread
+      mbar_init(empty_bar + 8 * s, kConsumerWarps);  // one arrival per consumer warp
+    }
     fence_mbar_init();
     for (int s = 0; s < p.num_slices; ++s) prefetch_tmap(&p.tmap[s]);
   }
@@ -95,56 +102,53 @@ __global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
 
   // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
-  uint32_t phase = 0;  // bit s: parity of the next phase of stage s
   bool waited = false, timed_out = false;
-
-  // this thread's x chunks: rows (tid >> 3) + 16 j, chunk tid & 7
-  constexpr int XJ = BM / 16;
-  const int xch = tid & 7;
+  int kb_global = 0;  // k-blocks processed by this CTA so far (stage phases)
 
   for (int item = cluster_id; item < ntiles; item += nclusters) {
     load_record<BM>(p.records, item, rec);
     __syncthreads();
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     const int lora = tv.lora, cnt = tv.count;
-    const __nv_bfloat16* xrow[XJ];
-#pragma unroll
-    for (int j = 0; j < XJ; ++j) {
-      const int t = record_token(rec, (tid >> 3) + 16 * j, cnt, p.max_num_tokens);
-      xrow[j] = t >= 0 ? p.x + static_cast<long long>(t) * p.x_stride + xch * 8 : nullptr;
-    }
+    const int npro = min(nkb, NST);
 
-    // A blocks of all slices for k-block kb -> stage st (thread 0)
-    auto fill_a = [&](int st, int kb) {
-      const uint32_t bar = bars + 8 * st;
+    // x chunk (row, 16-byte chunk) c of k-block kb -> stage st
+    auto x_chunk = [&](int st, int kb, int c) {
+      const int row = c >> 3, ch = c & 7;
+      const int t = record_token(rec, row, cnt, p.max_num_tokens);
+      const int kcol = kb * kBK + ch * 8;
+      const bool ok = t >= 0 && kcol < p.hidden;
+      cp_async_16(sbase + st * p.stage_bytes + swz128(row, ch),
+                  ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
+    };
+    // the adapter blocks of k-block kb -> stage st, by TMA (one thread)
+    auto issue_a = [&](int st, int kb) {
+      const uint32_t bar = full_bar + 8 * st;
       mbar_arrive_expect_tx(bar, static_cast<uint32_t>(SR * 128));
       const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
       for (int s = 0; s < p.num_slices; ++s)
         tma_load_2d(sa + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
     };
-    // gathered x rows for k-block kb -> stage st (every thread, one group)
-    auto fill_x = [&](int st, int kb) {
-      const uint32_t sx = sbase + st * p.stage_bytes;
-      const int kcol = kb * kBK + xch * 8;
-#pragma unroll
-      for (int j = 0; j < XJ; ++j) {
-        const int row = (tid >> 3) + 16 * j;
-        const bool ok = xrow[j] != nullptr && kcol < p.hidden;
-        cp_async_16(sx + swz128(row, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
-      }
-      cp_async_commit();
+    auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
+      const int st = g % NST, use = g / NST;
+      if (use > 0 && !mbar_wait(empty_bar + 8 * st, (use - 1) & 1)) timed_out = true;
     };
 
-    const int npro = min(nkb, NST);
-    if (tid == 0)
-      for (int s = 0; s < npro; ++s) fill_a(s, kb0 + s);
+    // first stages: the weights before the dependency wait, then every thread
+    // issues its share of the x rows and arrives on the stage's barrier
+    if (producer && lane == 0) {
+      for (int i = 0; i < npro; ++i) {
+        wait_empty(kb_global + i);
+        issue_a((kb_global + i) % NST, kb0 + i);
+      }
+    }
     if (!waited) {
-      if (npro > 0) {
+      if (producer && npro > 0) {
         // warm L2 (and the TLB) with this CTA's first x rows while the
         // previous kernel finishes; the copies below then hit L2
         const int kcol = kb0 * kBK;
         const int bytes = min(npro * kBK, p.hidden - kcol) * 2;
-        for (int r = tid; r < cnt; r += kShrinkThreads) {
+        for (int r = lane; r < cnt; r += 32) {
           const int t = record_token(rec, r, cnt, p.max_num_tokens);
           if (t >= 0) prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + kcol, bytes);
         }
@@ -153,68 +157,95 @@ __global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
       pdl_launch_dependents();
       waited = true;
     }
-    for (int s = 0; s < npro; ++s) fill_x(s, kb0 + s);
-    int issued = npro;
+    for (int i = 0; i < npro; ++i) {
+      const int st = (kb_global + i) % NST;
+      for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb0 + i, c);
+      cp_async_mbar_arrive(full_bar + 8 * st);
+    }
 
-    float acc[BM / 16][NTW][4];
+    if (producer) {
+      // refills: the producer warp alone; lane 0 also arrives for the 128
+      // consumer threads so that every phase counts 1 + kShrinkThreads arrivals.
+      // Each lane's rows (lane >> 3) + 4 j and chunk lane & 7 are fixed per tile.
+      constexpr int XJ = BM / 4;
+      const int xch = lane & 7;
+      const __nv_bfloat16* xrow[XJ];
 #pragma unroll
-    for (int mi = 0; mi < BM / 16; ++mi)
+      for (int j = 0; j < XJ; ++j) {
+        const int t = record_token(rec, (lane >> 3) + 4 * j, cnt, p.max_num_tokens);
+        xrow[j] = t >= 0 ? p.x + static_cast<long long>(t) * p.x_stride + xch * 8 : nullptr;
+      }
+      for (int i = npro; i < nkb; ++i) {
+        const int g = kb_global + i;
+        const int st = g % NST;
+        wait_empty(g);  // every lane: the consumers released the stage
+        __syncwarp();
+        if (lane == 0) {
+          issue_a(st, kb0 + i);
+          mbar_arrive_count(full_bar + 8 * st, kShrinkThreads - 32);
+        }
+        const uint32_t sx = sbase + st * p.stage_bytes;
+        const int kb = kb0 + i;
+        const bool kin = kb * kBK + xch * 8 < p.hidden;
 #pragma unroll
-      for (int j = 0; j < NTW; ++j)
+        for (int j = 0; j < XJ; ++j) {
+          const bool ok = xrow[j] != nullptr && kin;
+          cp_async_16(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
+        }
+        cp_async_mbar_arrive(full_bar + 8 * st);
+      }
+    } else {
+      float acc[BM / 16][NTW][4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
+      for (int mi = 0; mi < BM / 16; ++mi)
+#pragma unroll
+        for (int j = 0; j < NTW; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mi][j][e] = 0.f;
 
-    for (int i = 0; i < nkb; ++i) {
-      const int st = i % NST;
-      cp_async_wait_dyn(issued - 1 - i);
-      __syncthreads();  // everyone's x chunks of this stage are in
-      if (!mbar_wait(bars + 8 * st, (phase >> st) & 1u)) timed_out = true;
-      phase ^= 1u << st;
-      const uint32_t sx = sbase + st * p.stage_bytes;
-      const uint32_t sw = sx + BM * 128;
+      for (int i = 0; i < nkb; ++i) {
+        const int g = kb_global + i;
+        const int st = g % NST;
+        if (!mbar_wait(full_bar + 8 * st, (g / NST) & 1)) timed_out = true;
+        const uint32_t sx = sbase + st * p.stage_bytes;
+        const uint32_t sw = sx + BM * 128;
 #pragma unroll
-      for (int ks = 0; ks < kBK / 16; ++ks) {
-        if ((ks & (WK - 1)) != wk) continue;
-        uint32_t af[BM / 16][4];
+        for (int ks = 0; ks < kBK / 16; ++ks) {
+          if ((ks & (WK - 1)) != wk) continue;
+          uint32_t af[BM / 16][4];
 #pragma unroll
-        for (int mi = 0; mi < BM / 16; ++mi)
-          ldsm_x4(af[mi], sx + swz128(mi * 16 + (lane & 15), ks * 2 + (lane >> 4)));
+          for (int mi = 0; mi < BM / 16; ++mi)
+            ldsm_x4(af[mi], sx + swz128(mi * 16 + (lane & 15), ks * 2 + (lane >> 4)));
 #pragma unroll
-        for (int j = 0; j < NTW; j += 2) {
-          if (j < nt_cnt) {
-            const int n0 = (nt0 + j) * 8;
-            uint32_t bf[4];
-            if (j + 1 < nt_cnt) {
-              ldsm_x4(bf, sw + swz128(n0 + (lane & 7) + ((lane >> 4) << 3),
-                                      ks * 2 + ((lane >> 3) & 1)));
-            } else {
-              uint32_t b2[2];
-              ldsm_x2(b2, sw + swz128(n0 + (lane & 7), ks * 2 + ((lane >> 3) & 1)));
-              bf[0] = b2[0];
-              bf[1] = b2[1];
-              bf[2] = 0u;
-              bf[3] = 0u;
-            }
+          for (int j = 0; j < NTW; j += 2) {
+            if (j < nt_cnt) {
+              const int n0 = (nt0 + j) * 8;
+              uint32_t bf[4];
+              if (j + 1 < nt_cnt) {
+                ldsm_x4(bf, sw + swz128(n0 + (lane & 7) + ((lane >> 4) << 3),
+                                        ks * 2 + ((lane >> 3) & 1)));
+              } else {
+                uint32_t b2[2];
+                ldsm_x2(b2, sw + swz128(n0 + (lane & 7), ks * 2 + ((lane >> 3) & 1)));
+                bf[0] = b2[0];
+                bf[1] = b2[1];
+                bf[2] = 0u;
+                bf[3] = 0u;
+              }
 #pragma unroll
-            for (int mi = 0; mi < BM / 16; ++mi) {
-              mma_bf16(acc[mi][j], af[mi], bf[0], bf[1]);
-              if (j + 1 < NTW && j + 1 < nt_cnt) mma_bf16(acc[mi][j + 1], af[mi], bf[2], bf[3]);
+              for (int mi = 0; mi < BM / 16; ++mi) {
+                mma_bf16(acc[mi][j], af[mi], bf[0], bf[1]);
+                if (j + 1 < NTW && j + 1 < nt_cnt) mma_bf16(acc[mi][j + 1], af[mi], bf[2], bf[3]);
+              }
             }
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar + 8 * st);
       }
-      if (i + NST < nkb) {
-        __syncthreads();  // every warp is done with this stage
-        if (tid == 0) fill_a(st, kb0 + i + NST);
-        fill_x(st, kb0 + i + NST);
-        ++issued;
-      }
-    }
-    __syncthreads();  // the ring is free: it becomes the reduction buffer
-
-    // partial tile -> red[wk][row][col], then the k-split warps are summed into red[0]
-    float* red = reinterpret_cast<float*>(smem);
-    {
+      named_barrier_sync(1, 32 * kConsumerWarps);  // every consumer warp is done with the ring
+      // partial tile -> red[wk][row][col] (aliases the ring)
+      float* red = reinterpret_cast<float*>(smem);
       const int g = lane >> 2, q = lane & 3;
 #pragma unroll
       for (int mi = 0; mi < BM / 16; ++mi)
@@ -230,9 +261,13 @@ __global__ void __launch_bounds__(kShrinkThreads, BM == 32 ? 3 : 4)
           }
         }
     }
+    kb_global += nkb;
+    __syncthreads();  // all partials are in red[] (the producer has issued everything)
+
+    // sum the k-split warps into red[0]
+    float* red = reinterpret_cast<float*>(smem);
     const int e4 = (BM * SR) >> 2;
     if (WK > 1) {
-      __syncthreads();
       for (int idx = tid; idx < e4; idx += kShrinkThreads) {
         float4 v = reinterpret_cast<float4*>(red)[idx];
         for (int w = 1; w < WK; ++w) {
@@ -304,14 +339,17 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int NT = SR / 8;
   const int warps_n = NT <= 8 ? 1 : (NT <= 16 ? 2 : 4);
   const int ntw = (NT + warps_n - 1) / warps_n;
-  const int WK = 4 / warps_n;
+  const int WK = kConsumerWarps / warps_n;
   const int BM = (SR >= 192 || a.max_num_tokens <= 1024) ? 16 : 32;
   const int kblocks = (a.hidden + kBK - 1) / kBK;
   const long long max_tiles = tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM));
   const int sms = device_sm_count();
   // split the hidden dimension over a cluster until ~3 CTAs per SM have work
+  // (the rank-order reduction reads BM x S*R floats from every cluster CTA:
+  // wide tiles keep the cluster small)
+  const int max_cluster = SR <= 64 ? 8 : (SR <= 128 ? 4 : 2);
   int cluster = 1;
-  while (cluster < 8 && static_cast<long long>(cluster) * max_tiles < 3LL * sms &&
+  while (cluster < max_cluster && static_cast<long long>(cluster) * max_tiles < 3LL * sms &&
          kblocks >= 8 * cluster)
     cluster *= 2;
   const int kb_per = (kblocks + cluster - 1) / cluster;
@@ -355,16 +393,24 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int body = ((ring > red ? ring : red) + 127) / 128 * 128;
   p.rec_offset = body;
   p.bar_offset = body + record_ints(BM) * 4;
-  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 8 * 8;
+  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8;
 
   if (BM == 16) {
     if (ntw > 8) {
       if (nst == 4) return run_shrink<16, 12, 4>(p, cluster, smem, stream, max_tiles);
       return run_shrink<16, 12, 2>(p, cluster, smem, stream, max_tiles);
     }
+    if (ntw <= 4) {
+      if (nst == 8) return run_shrink<16, 4, 8>(p, cluster, smem, stream, max_tiles);
+      return run_shrink<16, 4, 4>(p, cluster, smem, stream, max_tiles);
+    }
     if (nst == 8) return run_shrink<16, 8, 8>(p, cluster, smem, stream, max_tiles);
     if (nst == 4) return run_shrink<16, 8, 4>(p, cluster, smem, stream, max_tiles);
     return run_shrink<16, 8, 2>(p, cluster, smem, stream, max_tiles);
+  }
+  if (ntw <= 4) {
+    if (nst == 8) return run_shrink<32, 4, 8>(p, cluster, smem, stream, max_tiles);
+    return run_shrink<32, 4, 4>(p, cluster, smem, stream, max_tiles);
   }
   if (nst == 8) return run_shrink<32, 8, 8>(p, cluster, smem, stream, max_tiles);
   if (nst == 4) return run_shrink<32, 8, 4>(p, cluster, smem, stream, max_tiles);

@@ -158,6 +158,32 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
                 size_t workspace_bytes, void *stream);
 
 /*
+ * Shrink then expand for one layer in one call: the same arguments, results
+ * and rules as lora_shrink followed by lora_expand (u is written too).  When
+ * the batch is small enough for a thread-block cluster to hold a tile's whole
+ * problem on chip (decode-sized batches: up to 16 k-blocks of 64 columns and
+ * 48 output units of 64 columns per CTA), one fused kernel does both steps and
+ * the expand reads u from shared memory; otherwise the two kernels of
+ * lora_shrink and lora_expand run back to back.  Either way the work stays on
+ * the GPU.
+ */
+int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                       const uint16_t *const *lora_a, const uint16_t *const *lora_b,
+                       const int64_t *slice_width, int num_slices, int rank, float scale,
+                       float *u, uint16_t *y, int64_t y_row_stride,
+                       const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                       int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * Kernels one lora_shrink_expand call launches for this shape on the current
+ * device: 1 (the fused kernel) or 2 (shrink, then expand); a negative
+ * LORA_ERR_* code for sizes the calls reject.  Host-only, no GPU work.
+ */
+int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,
+                               const int64_t *slice_width, int num_slices, int rank);
+
+/*
  * Copies the workspace's status word (LORA_STATUS_* bits OR-ed by every
  * lora_prepare_metadata since the last read) to *status, then clears it.
  * Synchronises `stream`.  Not capturable in a CUDA graph.

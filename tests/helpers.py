@@ -106,10 +106,18 @@ class DeviceCase:
         binding.lora_expand(self.u.view if u is None else u, self.b, self.y_view,
                             self.sorted.view, self.starts.view, self.ws.view, stream)
 
-    def run(self):
+    def shrink_expand(self, stream=None):
+        binding.lora_shrink_expand(self.x, self.a, self.b, self.shape.scale, self.u.view,
+                                   self.y_view, self.sorted.view, self.starts.view, self.ws.view,
+                                   stream)
+
+    def run(self, fused: bool = False):
         self.prepare()
-        self.shrink()
-        self.expand()
+        if fused:
+            self.shrink_expand()
+        else:
+            self.shrink()
+            self.expand()
         torch_mod().cuda.synchronize()
 
     def guards_intact(self):
@@ -130,12 +138,14 @@ def lora_rows(mapping: np.ndarray, n: int, L: int) -> np.ndarray:
     return np.nonzero((m >= 0) & (m < L))[0]
 
 
-def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None):
-    """Runs the path and checks metadata (bit-exact), u and y (tolerance),
-    untouched rows (bit-exact) and guard bands.  Returns diagnostics."""
+def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None,
+               fused: bool = False):
+    """Runs the path (shrink + expand, or the one-call shrink_expand) and checks
+    metadata (bit-exact), u and y (tolerance), untouched rows (bit-exact) and
+    guard bands.  Returns diagnostics."""
     sh, lay = case.shape, case.layer
     T, L, n = sh.max_num_tokens, sh.max_loras, sh.num_tokens
-    case.run()
+    case.run(fused=fused)
     s_ref, c_ref, st_ref, status_ref = oracle.prepare_metadata(case.mapping_np, n, L)
     assert np.array_equal(case.sorted.view.cpu().numpy(), s_ref), "sorted_token_ids differ"
     assert np.array_equal(case.counts.view.cpu().numpy(), c_ref), "num_tokens_per_lora differ"

@@ -312,3 +312,73 @@ def test_down_proj_workload_inside_a_graph(dev):
         assert np.all(tail == W.BF16_Y_SENTINEL)
         u_bits = case.u.view.cpu().numpy().view(np.uint32)
         assert np.all(u_bits[:, sh.num_tokens:] == U_SENTINEL_BITS)
+
+
+# ------------------------------------------------------------ one-call shrink + expand
+
+FUSED_SHAPES = [
+    ("decode_qkv", None),
+    ("tiny", None),
+    ("ragged3", (300, 211, 520, (264, 72, 136), 6, 8)),
+    ("rank16", (256, 256, 1024, (512, 512), 4, 16)),
+    ("rank64", (128, 120, 256, (256,), 3, 64)),
+    ("prefill_falls_back", (4096, 4000, 512, (512,), 8, 16)),
+]
+
+
+@pytest.mark.parametrize("name,spec", FUSED_SHAPES)
+def test_shrink_expand_one_call_matches_the_oracle(name, spec, dev):
+    if spec is None:
+        wl = W.make_workload(name)
+        case = DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev)
+    else:
+        T, n, H, widths, L, R = spec
+        shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                               max_loras=L, rank=R, neg_prob=0.15)
+        case = make_case(shape, dev, seed=T + R)
+    check_case(case, fused=True, sample_rows=400)
+
+
+def test_shrink_expand_one_call_equals_the_two_calls(dev):
+    wl = W.make_workload("decode_qkv")
+    a = DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev)
+    b = DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev)
+    a.run(fused=False)
+    b.run(fused=True)
+    ya, yb = a.y_view.float(), b.y_view.float()
+    assert torch.all((ya - yb).abs() <= 1e-2 + 1e-2 * ya.abs())
+    rows = lora_rows(wl.mapping, wl.shape.num_tokens, wl.shape.max_loras)
+    ua, ub = a.u.view[:, rows], b.u.view[:, rows]
+    assert torch.all((ua - ub).abs() <= 1e-2 + 1e-2 * ua.abs())
+
+
+def test_shrink_expand_one_call_in_a_graph_with_new_mappings(dev):
+    sh = W.custom_shape(max_num_tokens=256, num_tokens=256, hidden=2048,
+                        slice_widths=(1024, 1024, 1024), max_loras=8, rank=8, neg_prob=0.1)
+    rng = np.random.default_rng(21)
+    layer = W.make_layer(sh, rng)
+    g_case = DeviceCase(sh, W.make_mapping(sh, rng), layer, dev)
+    stream = torch.cuda.Stream()
+    y_clean = g_case.y.view.clone()
+    with torch.cuda.stream(stream):
+        g_case.prepare(stream); g_case.shrink_expand(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        g_case.prepare(stream)
+        g_case.shrink_expand(stream)
+    for trial, n_new in enumerate((256, 100, 17)):
+        sh2 = W.custom_shape(max_num_tokens=256, num_tokens=n_new, hidden=2048,
+                             slice_widths=(1024, 1024, 1024), max_loras=8, rank=8, neg_prob=0.2)
+        m_new = W.make_mapping(sh2, np.random.default_rng(300 + trial))
+        g_case.mapping.copy_(torch.from_numpy(m_new))
+        g_case.n.fill_(n_new)
+        g_case.y.view.copy_(y_clean)
+        g_case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = DeviceCase(sh2, m_new, layer, dev)
+        eager.run(fused=True)
+        assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
+        assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
