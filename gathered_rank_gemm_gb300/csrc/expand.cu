@@ -50,26 +50,33 @@ struct ExpandParams {
   int num_loras;
 };
 
-template <int BM, int RANK>
+template <int BM, int RANK, int NS>
 struct ExpandLayout {
   static constexpr int kUPitch = RANK * 4 + 16;  // staged u row bytes
   static constexpr int kB = 0;                   // 4 boxes of [RANK][128 B], 1024-aligned
   static constexpr int kY = 4 * RANK * 128;
   static constexpr int kU = kY + BM * kYPitch;
   static constexpr int kStage = (kU + BM * kUPitch + 1023) / 1024 * 1024;
-  static constexpr int kNStage = RANK <= 32 ? 2 : 1;
+  static constexpr int kRecSlots = NS + 1;
   static constexpr int kRecBytes = record_ints(BM) * 4;
-  static constexpr int kRec = kNStage * kStage;      // three record slots
-  static constexpr int kBar = kRec + 3 * kRecBytes;  // one mbarrier per stage
-  static constexpr int kSmem = 1024 + kBar + 8 * kNStage;
+  static constexpr int kRec = NS * kStage;
+  static constexpr int kBar = kRec + kRecSlots * kRecBytes;  // NS stage + kRecSlots record barriers
+  static constexpr int kSmem = 1024 + kBar + 8 * (NS + kRecSlots);
 };
 
-template <int BM, int RANK>
+// Stage count per rank (more stages cost occupancy: two stages at three
+// CTAs per SM beat three or four stages at two).
+template <int RANK>
+constexpr int expand_stages() {
+  return RANK <= 32 ? 2 : 1;
+}
+
+template <int BM, int RANK, int NS>
 __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     lora_expand_kernel(const __grid_constant__ ExpandParams p) {
-  using Lay = ExpandLayout<BM, RANK>;
-  constexpr int NS = Lay::kNStage;
+  using Lay = ExpandLayout<BM, RANK, NS>;
   constexpr int MT = BM / 16;
+  constexpr int RS = Lay::kRecSlots;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // TMA's 128-byte swizzle is laid out on 1024-byte boundaries
   const uint32_t raw = smem_u32(smem_raw);
@@ -77,32 +84,40 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   unsigned char* smem = smem_raw + (sbase - raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, q = lane & 3;
+  const uint32_t stage_bar = sbase + Lay::kBar;
+  const uint32_t rec_bar = stage_bar + 8 * NS;
 
   // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
   const int nitems = ntiles * p.cb_total;
+  // items in tile-major order with a stride of the grid: at any moment the
+  // CTAs cover every column block of a band of tiles, so whole y rows are
+  // read and written together (DRAM page locality)
   const int G = gridDim.x;
   const int nloc = static_cast<int>(blockIdx.x) < nitems
                        ? (nitems - 1 - static_cast<int>(blockIdx.x)) / G + 1
                        : 0;
-  if (nloc == 0) return;  // this CTA writes nothing
+  if (nloc <= 0) return;  // this CTA writes nothing
 
   if (tid == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(sbase + Lay::kBar + 8 * s, 1);
+    for (int s = 0; s < NS + RS; ++s) mbar_init(stage_bar + 8 * s, 1);
     fence_mbar_init();
+    for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
   }
+  __syncthreads();
 
   auto rec_of = [&](int k) {
-    return reinterpret_cast<int32_t*>(smem + Lay::kRec + (k % 3) * Lay::kRecBytes);
+    return reinterpret_cast<int32_t*>(smem + Lay::kRec + (k % RS) * Lay::kRecBytes);
   };
   struct Item {
-    int s, width, off, c0;
+    int s, width, off, c0, tile;
   };
   auto item_of = [&](int k) {
     const int item = static_cast<int>(blockIdx.x) + k * G;
-    const int tile = item / p.cb_total;
-    int cb = item - tile * p.cb_total;
+    const int tl = item / p.cb_total;
+    int cb = item - tl * p.cb_total;
     Item it;
+    it.tile = tl;
     it.s = 0;
     if (cb >= p.cb0) {
       cb -= p.cb0;
@@ -117,22 +132,32 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     it.c0 = cb * kEN;
     return it;
   };
-  auto tile_of = [&](int k) { return (static_cast<int>(blockIdx.x) + k * G) / p.cb_total; };
-
+  // tile record of item k -> its slot (thread 0, bulk copy on the slot's barrier)
+  auto issue_rec = [&](int k) {
+    const uint32_t bar = rec_bar + 8 * (k % RS);
+    mbar_arrive_expect_tx(bar, Lay::kRecBytes);
+    bulk_g2s(smem_u32(rec_of(k)),
+             p.records + static_cast<long long>(item_of(k).tile) * record_ints(BM), Lay::kRecBytes,
+             bar);
+  };
+  bool timed_out = false;
+  auto wait_rec = [&](int k) {
+    if (!mbar_wait(rec_bar + 8 * (k % RS), (k / RS) & 1)) timed_out = true;
+  };
   // B block of item k -> stage (thread 0): boxes starting past the slice are skipped
-  auto fill_b = [&](int k) {
+  auto issue_b = [&](int k) {
     const Item it = item_of(k);
     const TileView tv = TileView::of(rec_of(k), BM, p.num_loras);
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
-    const uint32_t bar = sbase + Lay::kBar + 8 * (k % NS);
+    const uint32_t bar = stage_bar + 8 * (k % NS);
     const int boxes = min(4, (it.width - it.c0 + 63) / 64);
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * RANK * 128));
     for (int b = 0; b < boxes; ++b)
       tma_load_2d(st + Lay::kB + b * RANK * 128, &p.tmap[it.s], it.c0 + 64 * b, tv.lora * RANK,
                   bar);
   };
-  // gathered y segments and u rows of item k -> stage (every thread)
-  auto fill_uy = [&](int k) {
+  // gathered y segments and u rows of item k -> stage (every thread, one group)
+  auto issue_uy = [&](int k) {
     const Item it = item_of(k);
     const int32_t* rec = rec_of(k);
     const TileView tv = TileView::of(rec, BM, p.num_loras);
@@ -157,17 +182,17 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
                      : p.u,
                   ok);
     }
+    cp_async_commit();
   };
 
-  // prologue: record 0 and the B block of item 0 before the wait, the rest after it
-  load_record_async<BM>(p.records, tile_of(0), rec_of(0));
-  cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();  // record 0 and the barrier initialisation are visible
+  // prologue: the records of the first items and the first B block before the
+  // dependency wait (metadata and weights), the activations after it
+  const int npro = min(nloc, NS);
   if (tid == 0) {
-    for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
-    fill_b(0);
+    for (int k = 0; k < min(nloc, RS); ++k) issue_rec(k);
   }
+  wait_rec(0);
+  if (tid == 0) issue_b(0);
   {
     // warm L2 (and the TLB) with item 0's y rows while the previous kernel finishes
     const Item it = item_of(0);
@@ -181,29 +206,24 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   }
   pdl_wait();
   pdl_launch_dependents();
-  fill_uy(0);
-  if (1 < nloc) load_record_async<BM>(p.records, tile_of(1), rec_of(1));
-  cp_async_commit();
+  issue_uy(0);
+  for (int k = 1; k < npro; ++k) {
+    wait_rec(k);
+    if (tid == 0) issue_b(k);
+    issue_uy(k);
+  }
 
-  bool timed_out = false;
   for (int k = 0; k < nloc; ++k) {
-    cp_async_wait<0>();
-    __syncthreads();  // item k's y/u and record k+1 have landed; item k-1 is finished
-    if (NS == 2) {
-      if (k + 1 < nloc) {
-        if (tid == 0) fill_b(k + 1);
-        fill_uy(k + 1);
-      }
-      if (k + 2 < nloc) load_record_async<BM>(p.records, tile_of(k + 2), rec_of(k + 2));
-      cp_async_commit();
-    }
+    // item k's copies: its cp.async group (later groups may stay pending) and its B block
+    cp_async_wait_dyn(min(NS, nloc - k) - 1);
+    __syncthreads();
+    if (!mbar_wait(stage_bar + 8 * (k % NS), (k / NS) & 1)) timed_out = true;
 
     const Item it = item_of(k);
     const int32_t* rec = rec_of(k);
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     unsigned char* stp = smem + (k % NS) * Lay::kStage;
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
-    if (!mbar_wait(sbase + Lay::kBar + 8 * (k % NS), (k / NS) & 1)) timed_out = true;
 
 #pragma unroll
     for (int mi = 0; mi < MT; ++mi) {
@@ -290,22 +310,24 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
               *reinterpret_cast<const int4*>(stp + Lay::kY + row * kYPitch + ych * 16);
       }
     }
+    __syncthreads();  // stage k % NS and record slot k % RS are free again
 
-    if (NS == 1 && k + 1 < nloc) {
-      __syncthreads();  // the single stage is free again
-      if (tid == 0) fill_b(k + 1);
-      fill_uy(k + 1);
-      if (k + 2 < nloc) load_record_async<BM>(p.records, tile_of(k + 2), rec_of(k + 2));
-      cp_async_commit();
+    // refill: item k + NS into the stage just freed, record k + RS into its slot
+    if (k + NS < nloc) {
+      wait_rec(k + NS);
+      if (tid == 0) issue_b(k + NS);
+      issue_uy(k + NS);
     }
+    if (tid == 0 && k + RS < nloc) issue_rec(k + RS);
   }
   if (timed_out) atomicOr(p.status, kStatusTimeout);
 }
 
 template <int BM, int RANK>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
-  const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK>);
-  const size_t smem = ExpandLayout<BM, RANK>::kSmem;
+  constexpr int NS = expand_stages<RANK>();
+  const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS>);
+  const size_t smem = ExpandLayout<BM, RANK, NS>::kSmem;
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;

@@ -353,9 +353,15 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
          kblocks >= 8 * cluster)
     cluster *= 2;
   const int kb_per = (kblocks + cluster - 1) / cluster;
-  // a deep ring keeps up to 8 k-blocks in flight per CTA (all of a short range)
+  // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
+  // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
+  // for the next kernel's CTAs to start under programmatic launch)
   const int stage = (BM + SR) * 128;  // a multiple of 1024: BM and S*R are multiples of 8
-  const int nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
+  int nst;
+  if (kb_per <= 8)
+    nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
+  else
+    nst = ((SR >= 128 && kb_per > 32) || 4 * stage > 96 * 1024) ? 2 : 4;
 
   ShrinkParams p;
   for (int s = 0; s < 3; ++s) {
