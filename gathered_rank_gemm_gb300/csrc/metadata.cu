@@ -12,8 +12,9 @@
 //      its tokens per bin (lanes with the same bin are grouped with
 //      __match_any_sync, the group leader adds the group size);
 //   2. per bin, an exclusive scan over the 16 warp counts gives each warp's
-//      offset inside the bin; a block scan over the bin totals gives
-//      lora_token_start_loc;
+//      offset inside the bin; one block scan over the bin totals (and, per
+//      tile height, the tiles per adapter) gives lora_token_start_loc and the
+//      first tile of every adapter;
 //   3. each warp walks its range again in order; a token's slot is
 //      start[bin] + warp offset + (earlier lanes of its group in this step).
 // Warp ranges are in token order and lanes are in token order, so equal ids
@@ -29,42 +30,61 @@ namespace grg {
 
 constexpr int kMetaThreads = 512;
 constexpr int kMetaWarps = kMetaThreads / 32;
+constexpr int kMetaChunk = 16;  // 32-token steps per warp whose bins stay in registers
+constexpr int kScanArrays = 1 + kNumTileSizes;  // bin starts + tile offsets per tile height
 
-// Exclusive scan of in[0..count) into out[0..count], out[count] = total.
-// Called by every thread of the block; in and out must not overlap.
-__device__ void block_exclusive_scan(const int32_t* in, int32_t* out, int count,
-                                     int32_t* warp_sums) {
+// Exclusive scans of kScanArrays arrays at once: in[a][0..count) ->
+// out[a][0..count], out[a][count] = total of array a.  `in` and `out` are
+// strided by in_stride / out_stride ints per array and must not overlap.
+// Called by every thread of the block.
+__device__ void block_exclusive_scan_multi(const int32_t* in, int in_stride, int32_t* out,
+                                           int out_stride, int count, int32_t* warp_sums) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x, nwarps = nthreads >> 5;
   const int per = (count + nthreads - 1) / nthreads;
   const int begin = min(tid * per, count), end = min(begin + per, count);
-  int local = 0;
-  for (int i = begin; i < end; ++i) local += in[i];
-  int incl = local;
+  int local[kScanArrays], incl[kScanArrays];
+#pragma unroll
+  for (int a = 0; a < kScanArrays; ++a) {
+    local[a] = 0;
+    for (int i = begin; i < end; ++i) local[a] += in[a * in_stride + i];
+    incl[a] = local[a];
+  }
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+#pragma unroll
+    for (int a = 0; a < kScanArrays; ++a) {
+      const int y = __shfl_up_sync(0xffffffffu, incl[a], o);
+      if (lane >= o) incl[a] += y;
+    }
   }
-  if (lane == 31) warp_sums[warp] = incl;
+  if (lane == 31)
+#pragma unroll
+    for (int a = 0; a < kScanArrays; ++a) warp_sums[a * 32 + warp] = incl[a];
   __syncthreads();
   if (warp == 0) {
-    int w = lane < nwarps ? warp_sums[lane] : 0;
-    int wi = w;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
+    for (int a = 0; a < kScanArrays; ++a) {
+      const int w = lane < nwarps ? warp_sums[a * 32 + lane] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += y;
+      }
+      if (lane < nwarps) warp_sums[a * 32 + lane] = wi - w;
     }
-    if (lane < nwarps) warp_sums[lane] = wi - w;
   }
   __syncthreads();
-  int run = warp_sums[warp] + incl - local;
-  for (int i = begin; i < end; ++i) {
-    out[i] = run;
-    run += in[i];
+#pragma unroll
+  for (int a = 0; a < kScanArrays; ++a) {
+    int run = warp_sums[a * 32 + warp] + incl[a] - local[a];
+    for (int i = begin; i < end; ++i) {
+      out[a * out_stride + i] = run;
+      run += in[a * in_stride + i];
+    }
+    if (tid == nthreads - 1) out[a * out_stride + count] = run;
   }
-  if (tid == nthreads - 1) out[count] = run;
   __syncthreads();
 }
 
@@ -81,7 +101,7 @@ struct MetaParams {
 
 __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaParams p) {
   extern __shared__ int32_t sm[];
-  __shared__ int32_t warp_sums[32];
+  __shared__ int32_t warp_sums[32 * kScanArrays];
   __shared__ int s_n;
   __shared__ uint32_t s_status;
 
@@ -90,8 +110,8 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   int32_t* hist = sm;                          // [kMetaWarps][nbins], then warp offsets
   int32_t* total = hist + kMetaWarps * nbins;  // [nbins]
   int32_t* start = total + nbins;              // [nbins + 1]
-  int32_t* ntile = start + nbins + 1;          // [L]
-  int32_t* toff = ntile + L;                   // [kNumTileSizes][L + 1]
+  int32_t* cnts = start + nbins + 1;           // [kScanArrays][nbins]: totals, tiles per height
+  int32_t* offs = cnts + kScanArrays * nbins;   // [kScanArrays][nbins + 1]: starts, tile offsets
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Dependents are released only at the very end, after a fence: kernels of
@@ -114,29 +134,53 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   const int lo = min(warp * seg, n), hi = min(lo + seg, n);
   int32_t* my_hist = hist + warp * nbins;
 
-  // pass 1: per-warp histogram
+  // Bins of this lane's tokens for one chunk of kMetaChunk 32-token steps:
+  // all loads are issued before any is used (one memory round trip).
+  int bins[kMetaChunk];
   bool bad = false;
-  for (int base = lo; base < hi; base += 32) {
-    const int t = base + lane;
-    const bool valid = t < hi;
-    int bin = nbins;  // never a real bin: groups the idle lanes
-    if (valid) {
-      const int id = p.mapping[t];
-      if (id >= 0 && id < L) {
-        bin = id;
-      } else {
-        bin = L;
-        bad |= (id != -1);
-      }
+  auto load_chunk = [&](int base0) {
+    int ids[kMetaChunk];
+#pragma unroll
+    for (int j = 0; j < kMetaChunk; ++j) {
+      const int t = base0 + 32 * j + lane;
+      ids[j] = t < hi ? p.mapping[t] : -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (valid && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < kMetaChunk; ++j) {
+      const int t = base0 + 32 * j + lane;
+      int bin = nbins;  // never a real bin: marks idle lanes
+      if (t < hi) {
+        const int id = ids[j];
+        if (id >= 0 && id < L) {
+          bin = id;
+        } else {
+          bin = L;
+          bad |= (id != -1);
+        }
+      }
+      bins[j] = bin;
+    }
+  };
+  const int chunk_tokens = 32 * kMetaChunk;
+  const bool one_chunk = hi - lo <= chunk_tokens;
+
+  // pass 1: per-warp histogram (lanes of a bin grouped with __match_any_sync)
+  for (int base0 = lo; base0 < hi; base0 += chunk_tokens) {
+    load_chunk(base0);
+#pragma unroll
+    for (int j = 0; j < kMetaChunk; ++j) {
+      if (base0 + 32 * j >= hi) break;
+      const int bin = bins[j];
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < nbins && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
+      __syncwarp();
+    }
   }
   if (bad) atomicOr(&s_status, 1u);
   __syncthreads();
 
-  // pass 2: warp offsets inside each bin, bin totals, bin starts
+  // pass 2: warp offsets inside each bin, bin totals; then one scan gives
+  // the bin starts and, per tile height, each adapter's first tile
   for (int b = tid; b < nbins; b += kMetaThreads) {
     int run = 0;
     for (int w = 0; w < kMetaWarps; ++w) {
@@ -145,44 +189,44 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
       run += c;
     }
     total[b] = run;
+    cnts[b] = run;
+#pragma unroll
+    for (int k = 0; k < kNumTileSizes; ++k) {
+      const int rows = tile_rows_of(k);
+      cnts[(1 + k) * nbins + b] = b < L ? (run + rows - 1) / rows : 0;
+    }
   }
   __syncthreads();
-  block_exclusive_scan(total, start, nbins, warp_sums);
-
-  // tiles per adapter and their offsets in each work list
-#pragma unroll
-  for (int k = 0; k < kNumTileSizes; ++k) {
-    const int rows = tile_rows_of(k);
-    for (int l = tid; l < L; l += kMetaThreads) ntile[l] = (total[l] + rows - 1) / rows;
-    __syncthreads();
-    block_exclusive_scan(ntile, toff + k * (L + 1), L, warp_sums);
-  }
+  block_exclusive_scan_multi(cnts, nbins, offs, nbins + 1, nbins, warp_sums);
+  for (int b = tid; b <= nbins; b += kMetaThreads) start[b] = offs[b];
+  __syncthreads();
+  const int32_t* toff = offs + (nbins + 1);  // [k][L + 1]: tile offsets, stride nbins + 1
 
   // pass 3: stable scatter into sorted_token_ids and into the tile records
-  for (int base = lo; base < hi; base += 32) {
-    const int t = base + lane;
-    const bool valid = t < hi;
-    int bin = nbins;
-    if (valid) {
-      const int id = p.mapping[t];
-      bin = (id >= 0 && id < L) ? id : L;
-    }
-    const unsigned peers = __match_any_sync(0xffffffffu, bin);
-    if (valid) {
-      const int rel = my_hist[bin] + __popc(peers & ((1u << lane) - 1u));
-      p.sorted_ids[start[bin] + rel] = t;
-      if (bin < L) {
+  for (int base0 = lo; base0 < hi; base0 += chunk_tokens) {
+    if (!one_chunk) load_chunk(base0);  // a single chunk still holds its bins
 #pragma unroll
-        for (int k = 0; k < kNumTileSizes; ++k) {
-          const int tile = toff[k * (L + 1) + bin] + (rel >> (4 + k));
-          p.ws.lists[k][static_cast<long long>(tile) * record_ints(tile_rows_of(k)) +
-                        kRecordHeaderInts + (rel & (tile_rows_of(k) - 1))] = t;
+    for (int j = 0; j < kMetaChunk; ++j) {
+      if (base0 + 32 * j >= hi) break;
+      const int t = base0 + 32 * j + lane;
+      const int bin = bins[j];
+      const unsigned peers = __match_any_sync(0xffffffffu, bin);
+      if (bin < nbins) {
+        const int rel = my_hist[bin] + __popc(peers & ((1u << lane) - 1u));
+        p.sorted_ids[start[bin] + rel] = t;
+        if (bin < L) {
+#pragma unroll
+          for (int k = 0; k < kNumTileSizes; ++k) {
+            const int tile = toff[k * (nbins + 1) + bin] + (rel >> (4 + k));
+            p.ws.lists[k][static_cast<long long>(tile) * record_ints(tile_rows_of(k)) +
+                          kRecordHeaderInts + (rel & (tile_rows_of(k) - 1))] = t;
+          }
         }
       }
+      __syncwarp();
+      if (bin < nbins && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
+      __syncwarp();
     }
-    __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) my_hist[bin] += __popc(peers);
-    __syncwarp();
   }
   for (int t = n + tid; t < p.max_num_tokens; t += kMetaThreads) p.sorted_ids[t] = -1;
   for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
@@ -192,7 +236,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
 #pragma unroll
   for (int k = 0; k < kNumTileSizes; ++k) {
     const int rows = tile_rows_of(k);
-    const int32_t* off = toff + k * (L + 1);
+    const int32_t* off = toff + k * (nbins + 1);
     const int count = off[L];
     int32_t* list = p.ws.lists[k];
     for (int i = tid; i < count; i += kMetaThreads) {
@@ -219,7 +263,8 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
 
 static size_t meta_smem_bytes(int num_loras) {
   const size_t nb = static_cast<size_t>(num_loras) + 1;
-  return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + (nb - 1) + kNumTileSizes * nb);
+  return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + kScanArrays * nb +
+                            kScanArrays * (nb + 1));
 }
 
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,

@@ -100,6 +100,13 @@ def test_all_tokens_without_adapter(dev):
     check_case(make_case(shape, dev))
 
 
+def test_long_batch_takes_several_register_chunks(dev):
+    # more than 32 warps x 512 tokens: the grouping reloads the mapping per chunk
+    shape = W.custom_shape(max_num_tokens=40000, num_tokens=39000, hidden=64, slice_widths=(64,),
+                           max_loras=7, rank=8, mapping="runs", neg_prob=0.0)
+    check_case(make_case(shape, dev, seed=40), sample_rows=500)
+
+
 def test_many_loras_uses_every_bin(dev):
     shape = W.custom_shape(max_num_tokens=4096, num_tokens=4096, hidden=64, slice_widths=(64,),
                            max_loras=1024, rank=8, neg_prob=0.05)
