@@ -11,7 +11,8 @@ replayed, as a serving engine does.
 value   = n * layers / step time * ranks  (tokens/s per LoRA layer, whole job)
 e2e     = the same metric with the per-step inputs (mapping, n, x, y of every
           layer) copied from pinned host memory and y copied back each step
-roofline: the dominant kernel's algorithmic bytes / its measured launch time
+roofline: the algorithmic bytes of the kernel with the largest share of the
+          layer's device time / its measured launch time
           against the measured HBM copy bandwidth
 
 ``--impl reference`` times the fp64 CPU oracle instead (the only reference
@@ -420,7 +421,8 @@ def run_ours(args, world, rank, local):
         dominant, kernel_name = "shrink_expand", "lora_fused_kernel"
         dom_bytes, t_dom = alg["shrink"] + alg["expand"], ms_one
     else:
-        dominant = "expand" if alg["expand"] >= alg["shrink"] else "shrink"
+        # the kernel that takes the larger share of the layer's device time
+        dominant = "expand" if ms_expand >= ms_shrink else "shrink"
         kernel_name = f"lora_{dominant}_kernel"
         dom_bytes = alg[dominant]
         t_dom = ms_expand if dominant == "expand" else ms_shrink
