@@ -401,26 +401,26 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.bar_offset = body + record_ints(BM) * 4;
   const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8;
 
-  if (BM == 16) {
-    if (ntw > 8) {
-      if (nst == 4) return run_shrink<16, 12, 4>(p, cluster, smem, stream, max_tiles);
-      return run_shrink<16, 12, 2>(p, cluster, smem, stream, max_tiles);
-    }
-    if (ntw <= 4) {
-      if (nst == 8) return run_shrink<16, 4, 8>(p, cluster, smem, stream, max_tiles);
-      return run_shrink<16, 4, 4>(p, cluster, smem, stream, max_tiles);
-    }
-    if (nst == 8) return run_shrink<16, 8, 8>(p, cluster, smem, stream, max_tiles);
-    if (nst == 4) return run_shrink<16, 8, 4>(p, cluster, smem, stream, max_tiles);
-    return run_shrink<16, 8, 2>(p, cluster, smem, stream, max_tiles);
-  }
-  if (ntw <= 4) {
-    if (nst == 8) return run_shrink<32, 4, 8>(p, cluster, smem, stream, max_tiles);
-    return run_shrink<32, 4, 4>(p, cluster, smem, stream, max_tiles);
-  }
-  if (nst == 8) return run_shrink<32, 8, 8>(p, cluster, smem, stream, max_tiles);
-  if (nst == 4) return run_shrink<32, 8, 4>(p, cluster, smem, stream, max_tiles);
-  return run_shrink<32, 8, 2>(p, cluster, smem, stream, max_tiles);
+  // Every (tile height, column tiles per warp, ring depth) the rules above can
+  // produce has its own instantiation; the shared-memory plan was sized for
+  // exactly that ring, so any other combination is refused, never rounded.
+  using Run = int (*)(const ShrinkParams&, int, size_t, cudaStream_t, long long);
+  Run run = nullptr;
+  const int ntw_t = ntw <= 4 ? 4 : (ntw <= 8 ? 8 : 12);
+  if (BM == 16 && ntw_t == 4 && nst == 8) run = run_shrink<16, 4, 8>;
+  if (BM == 16 && ntw_t == 4 && nst == 4) run = run_shrink<16, 4, 4>;
+  if (BM == 16 && ntw_t == 8 && nst == 8) run = run_shrink<16, 8, 8>;
+  if (BM == 16 && ntw_t == 8 && nst == 4) run = run_shrink<16, 8, 4>;
+  if (BM == 16 && ntw_t == 8 && nst == 2) run = run_shrink<16, 8, 2>;
+  if (BM == 16 && ntw_t == 12 && nst == 4) run = run_shrink<16, 12, 4>;
+  if (BM == 16 && ntw_t == 12 && nst == 2) run = run_shrink<16, 12, 2>;
+  if (BM == 32 && ntw_t == 4 && nst == 8) run = run_shrink<32, 4, 8>;
+  if (BM == 32 && ntw_t == 4 && nst == 4) run = run_shrink<32, 4, 4>;
+  if (BM == 32 && ntw_t == 8 && nst == 8) run = run_shrink<32, 8, 8>;
+  if (BM == 32 && ntw_t == 8 && nst == 4) run = run_shrink<32, 8, 4>;
+  if (BM == 32 && ntw_t == 8 && nst == 2) run = run_shrink<32, 8, 2>;
+  if (run == nullptr) return -6;
+  return run(p, cluster, smem, stream, max_tiles);
 }
 
 }  // namespace grg

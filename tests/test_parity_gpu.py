@@ -326,10 +326,15 @@ def test_down_proj_workload_inside_a_graph(dev):
 FUSED_SHAPES = [
     ("decode_qkv", None),
     ("tiny", None),
+    ("chunked_prefill", None),
+    ("mlp_gate_up", None),
+    ("down_proj_graph", None),
     ("ragged3", (300, 211, 520, (264, 72, 136), 6, 8)),
     ("rank16", (256, 256, 1024, (512, 512), 4, 16)),
+    ("rank32_two_slices", (1500, 1400, 776, (520, 264), 5, 32)),
     ("rank64", (128, 120, 256, (256,), 3, 64)),
-    ("prefill_falls_back", (4096, 4000, 512, (512,), 8, 16)),
+    ("rank128_three_slices", (96, 90, 512, (128, 64, 192), 2, 128)),
+    ("prefill_like", (4096, 4000, 512, (512,), 8, 16)),
 ]
 
 
