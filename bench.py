@@ -43,6 +43,8 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {"expand": "gathered_rank_gemm_gb300/csrc/expand.cu",
                   "shrink": "gathered_rank_gemm_gb300/csrc/shrink.cu",
+                  "expand-split": "gathered_rank_gemm_gb300/csrc/expand.cu",
+                  "shrink-split": "gathered_rank_gemm_gb300/csrc/shrink.cu",
                   "shrink_expand": "gathered_rank_gemm_gb300/csrc/fused.cu",
                   "metadata": "gathered_rank_gemm_gb300/csrc/metadata.cu"}
 
@@ -294,7 +296,10 @@ def run_ours(args, world, rank, local):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     stream = torch.cuda.Stream(dev)
-    meta = binding.LoraMetadata(T, L, dev)
+    # the larger workspace lets lora_shrink_expand take its split-K path
+    ws_bytes = binding.lora_shrink_expand_workspace_size(T, L, shape.hidden, shape.slice_widths,
+                                                         shape.rank)
+    meta = binding.LoraMetadata(T, L, dev, workspace_bytes=ws_bytes)
     mapping = torch.from_numpy(wl.mapping).to(dev)
     n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
     xs = [bf16(l.x) for l in wl.layers]
@@ -310,21 +315,34 @@ def run_ours(args, world, rank, local):
     per_layer_kernels = binding.lora_shrink_expand_kernels(T, L, shape.hidden,
                                                            shape.slice_widths, shape.rank)
 
+    # which kernels lora_shrink_expand runs here: the split-K path leaves its
+    # partial tiles behind the metadata part of the (zero-initialised) workspace
+    split_k = False
+
     def step(which="all"):
         if which in ("all", "metadata", "profile"):
             meta.prepare(mapping, n_dev, stream)
         for k in range(layers):
             if which in ("all", "one_call", "profile"):
                 meta.shrink_expand(xs[k], As[k], Bs[k], shape.scale, us[k], ys[k], stream)
+            # the kernels of the one call, timed one launch at a time
             if which == "shrink":
-                meta.shrink(xs[k], As[k], shape.scale, us[k], stream)
+                if split_k:
+                    meta.shrink_partials(xs[k], As[k], stream)
+                else:
+                    meta.shrink(xs[k], As[k], shape.scale, us[k], stream)
             if which == "expand":
-                meta.expand(us[k], Bs[k], ys[k], stream)
+                if split_k:
+                    meta.expand_partials(shape.hidden, Bs[k], shape.scale, us[k], ys[k], stream)
+                else:
+                    meta.expand(us[k], Bs[k], ys[k], stream)
 
     graphs = {}
     with torch.cuda.stream(stream):
         step()  # first call per device sets kernel attributes outside capture
     stream.synchronize()
+    ws_base = binding.lora_workspace_size(T, L)
+    split_k = per_layer_kernels == 2 and bool(meta.workspace[ws_base:].any().item())
     if args.mode == "profile":
         for _ in range(args.steps):
             with torch.cuda.stream(stream):
@@ -423,7 +441,7 @@ def run_ours(args, world, rank, local):
     else:
         # the kernel that takes the larger share of the layer's device time
         dominant = "expand" if ms_expand >= ms_shrink else "shrink"
-        kernel_name = f"lora_{dominant}_kernel"
+        kernel_name = f"lora_{dominant}_kernel" + (" (split-K)" if split_k else "")
         dom_bytes = alg[dominant]
         t_dom = ms_expand if dominant == "expand" else ms_shrink
     achieved = dom_bytes / (t_dom * 1e-3) / 1e9
@@ -450,8 +468,10 @@ def run_ours(args, world, rank, local):
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": dom_bytes,
-                         "traffic": recorded_traffic(dominant, shape.name)},
+                         "traffic": recorded_traffic(dominant + ("-split" if split_k else ""),
+                                                     shape.name)},
             "kernels_per_layer": per_layer_kernels,
+            "one_call_path": "fused" if per_layer_kernels == 1 else ("split-K" if split_k else "cluster"),
             "kernels_us": {"metadata": 1e3 * ms_meta, "shrink_expand_one_call": 1e3 * ms_one,
                            "shrink": 1e3 * ms_shrink, "expand": 1e3 * ms_expand,
                            "layer_in_graph": 1e3 * ms_step / layers},

@@ -5,9 +5,11 @@ The compute lives in the CUDA library ``libgathered_rank_gemm.so`` (C ABI in
 ``workloads`` draws seeded synthetic inputs.
 """
 from .binding import (LoraError, LoraMetadata, lora_apply_noalloc, lora_expand,  # noqa: F401
-                      lora_prepare_metadata, lora_read_status, lora_shrink, lora_shrink_expand,
-                      lora_workspace_size)
+                      lora_expand_partials, lora_prepare_metadata, lora_read_status, lora_shrink,
+                      lora_shrink_expand, lora_shrink_expand_workspace_size,
+                      lora_shrink_partials, lora_workspace_size)
 
 __all__ = ["LoraError", "LoraMetadata", "lora_apply_noalloc", "lora_expand",
            "lora_prepare_metadata", "lora_read_status", "lora_shrink", "lora_shrink_expand",
+           "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials",
            "lora_workspace_size"]

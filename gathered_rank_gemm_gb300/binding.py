@@ -27,7 +27,8 @@ LORA_NOALLOC_SCRATCH_BYTES = 384 * 1024
 
 EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora_expand",
             "lora_read_status", "lora_error_string", "lora_apply_noalloc",
-            "lora_shrink_expand", "lora_shrink_expand_kernels")
+            "lora_shrink_expand", "lora_shrink_expand_kernels",
+            "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials")
 
 _lib = None
 
@@ -68,6 +69,13 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
                                        p, p, i64, i64, p, sz, p]
     lib.lora_shrink_expand_kernels.restype = i32
     lib.lora_shrink_expand_kernels.argtypes = [i64, i64, i64, p, i32, i32]
+    lib.lora_shrink_expand_workspace_size.restype = sz
+    lib.lora_shrink_expand_workspace_size.argtypes = [i64, i64, i64, p, i32, i32]
+    lib.lora_shrink_partials.restype = i32
+    lib.lora_shrink_partials.argtypes = [p, i64, i64, p, i32, i32, p, p, i64, i64, p, sz, p]
+    lib.lora_expand_partials.restype = i32
+    lib.lora_expand_partials.argtypes = [i64, p, p, i32, i32, ctypes.c_float, p, p, i64, p, p,
+                                         i64, i64, p, sz, p]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, i64, p, p, p, p, p]
@@ -165,6 +173,38 @@ def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
     _check("lora_shrink_expand", rc)
 
 
+def lora_shrink_partials(x, lora_a, sorted_token_ids, lora_token_start_loc, workspace,
+                         stream=None):
+    """Split-K shrink: each CTA's partial tile of u into the workspace (u is not written)."""
+    lora_a = list(lora_a)
+    arr = _ptr_array(lora_a, "lora_a")
+    num_loras, rank, hidden = lora_a[0].shape
+    rc = load().lora_shrink_partials(
+        _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(lora_a), rank,
+        _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, x.device))
+    _check("lora_shrink_partials", rc)
+
+
+def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_ids,
+                         lora_token_start_loc, workspace, stream=None):
+    """Sums the split-K partials (scaled) into u, then y += u . B_s (in place)."""
+    lora_b = list(lora_b)
+    arr = _ptr_array(lora_b, "lora_b")
+    widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
+    num_loras, rank = lora_b[0].shape[:2]
+    rc = load().lora_expand_partials(
+        int(hidden), ctypes.addressof(arr), ctypes.addressof(widths), len(lora_b), rank,
+        float(scale), _dev(u, "u"), _dev(y, "y"), y.stride(0),
+        _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), y.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, y.device))
+    _check("lora_expand_partials", rc)
+
+
 def lora_shrink_expand_kernels(max_num_tokens: int, max_loras: int, hidden: int, slice_widths,
                                rank: int) -> int:
     """Kernels lora_shrink_expand launches for a shape (1 fused, 2 separate)."""
@@ -174,6 +214,15 @@ def lora_shrink_expand_kernels(max_num_tokens: int, max_loras: int, hidden: int,
     if rc < 0:
         _check("lora_shrink_expand_kernels", rc)
     return int(rc)
+
+
+def lora_shrink_expand_workspace_size(max_num_tokens: int, max_loras: int, hidden: int,
+                                      slice_widths, rank: int) -> int:
+    """Workspace bytes that let lora_shrink_expand take its split-K path."""
+    w = (ctypes.c_int64 * len(slice_widths))(*[int(v) for v in slice_widths])
+    return int(load().lora_shrink_expand_workspace_size(
+        int(max_num_tokens), int(max_loras), int(hidden), ctypes.addressof(w),
+        len(slice_widths), int(rank)))
 
 
 def lora_read_status(workspace, stream=None) -> int:
@@ -218,7 +267,9 @@ def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale:
 class LoraMetadata:
     """Device buffers of one batch's grouping (sized by max_num_tokens / max_loras)."""
 
-    def __init__(self, max_num_tokens: int, max_loras: int, device="cuda"):
+    def __init__(self, max_num_tokens: int, max_loras: int, device="cuda", workspace_bytes=None):
+        """workspace_bytes: None for lora_workspace_size, or a larger size such
+        as lora_shrink_expand_workspace_size for the one-call split-K path."""
         import torch
         self.max_num_tokens = int(max_num_tokens)
         self.max_loras = int(max_loras)
@@ -226,9 +277,10 @@ class LoraMetadata:
         self.sorted_token_ids = torch.empty(self.max_num_tokens, **i32)
         self.num_tokens_per_lora = torch.empty(self.max_loras + 1, **i32)
         self.lora_token_start_loc = torch.empty(self.max_loras + 2, **i32)
-        nbytes = lora_workspace_size(self.max_num_tokens, self.max_loras)
-        if nbytes == 0:
+        base = lora_workspace_size(self.max_num_tokens, self.max_loras)
+        if base == 0:
             raise ValueError("max_num_tokens / max_loras outside the supported range")
+        nbytes = base if workspace_bytes is None else max(int(workspace_bytes), base)
         self.workspace = torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
     def prepare(self, token_lora_mapping, num_tokens, stream=None):
@@ -247,6 +299,14 @@ class LoraMetadata:
     def shrink_expand(self, x, lora_a, lora_b, scale, u, y, stream=None):
         lora_shrink_expand(x, lora_a, lora_b, scale, u, y, self.sorted_token_ids,
                            self.lora_token_start_loc, self.workspace, stream)
+
+    def shrink_partials(self, x, lora_a, stream=None):
+        lora_shrink_partials(x, lora_a, self.sorted_token_ids, self.lora_token_start_loc,
+                             self.workspace, stream)
+
+    def expand_partials(self, hidden, lora_b, scale, u, y, stream=None):
+        lora_expand_partials(hidden, lora_b, scale, u, y, self.sorted_token_ids,
+                             self.lora_token_start_loc, self.workspace, stream)
 
     def read_status(self, stream=None) -> int:
         return lora_read_status(self.workspace, stream)

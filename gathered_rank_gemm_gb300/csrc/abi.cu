@@ -27,8 +27,8 @@ int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                 const uint16_t* const* lora_a, int num_slices, int rank, float scale, float* u,
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
-                size_t workspace_bytes, grg::ShrinkArgs* out) {
-  if (!x || !lora_a || !u || !sorted_token_ids || !lora_token_start_loc || !workspace)
+                size_t workspace_bytes, grg::ShrinkArgs* out, bool need_u = true) {
+  if (!x || !lora_a || (need_u && !u) || !sorted_token_ids || !lora_token_start_loc || !workspace)
     return LORA_ERR_NULL;
   if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
   for (int s = 0; s < num_slices; ++s)
@@ -36,7 +36,8 @@ int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
   if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || hidden < 8 ||
       hidden > kMaxHidden || (hidden % 8) != 0 || x_row_stride < hidden)
     return LORA_ERR_SHAPE;
-  if (!aligned16(x) || (x_row_stride % 8) != 0 || !aligned16(u) || !aligned16(workspace))
+  if (!aligned16(x) || (x_row_stride % 8) != 0 || (need_u && !aligned16(u)) ||
+      !aligned16(workspace))
     return LORA_ERR_ALIGN;
   for (int s = 0; s < num_slices; ++s)
     if (!aligned16(lora_a[s])) return LORA_ERR_ALIGN;
@@ -112,6 +113,91 @@ size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras) {
   return grg::workspace_bytes_needed(max_num_tokens, max_loras);
 }
 
+namespace {
+// Split-K one-call path: batches of up to 1024 tokens (16-token tiles) and
+// ranks up to 32.  Its partial tiles follow the metadata part of the
+// workspace: [16-token tile][split <= 8][16][S*R] fp32.
+constexpr int64_t kSplitMaxTokens = 1024;
+constexpr int kSplitMaxRank = 32;
+constexpr int kSplitMax = 8;
+bool split_shape(int64_t max_num_tokens, int rank) {
+  return max_num_tokens <= kSplitMaxTokens && rank <= kSplitMaxRank;
+}
+size_t split_scratch_bytes(int64_t max_num_tokens, int64_t max_loras, int num_slices, int rank) {
+  return static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) * kSplitMax *
+         16 * num_slices * rank * 4;
+}
+}  // namespace
+
+size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_loras,
+                                         int64_t hidden, const int64_t* slice_width,
+                                         int num_slices, int rank) {
+  const size_t base = lora_workspace_size(max_num_tokens, max_loras);
+  if (base == 0 || !slice_width || num_slices < 1 || num_slices > LORA_MAX_SLICES ||
+      !rank_ok(rank) || hidden < 8 || hidden > kMaxHidden || (hidden % 8) != 0)
+    return 0;
+  for (int s = 0; s < num_slices; ++s)
+    if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0) return 0;
+  if (!split_shape(max_num_tokens, rank)) return base;
+  return base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank);
+}
+
+namespace {
+// CTAs per tile of the split-K shrink for a shape (the shrink's cluster rule).
+int split_of(int64_t max_num_tokens, int64_t max_loras, int64_t hidden, int num_slices,
+             int rank) {
+  grg::ShrinkArgs a;
+  a.hidden = static_cast<int>(hidden);
+  a.num_slices = num_slices;
+  a.rank = rank;
+  a.max_num_tokens = static_cast<int>(max_num_tokens);
+  a.num_loras = static_cast<int>(max_loras);
+  return grg::shrink_split(a);
+}
+}  // namespace
+
+int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                         const uint16_t* const* lora_a, int num_slices, int rank,
+                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  grg::ShrinkArgs sa;
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, 1.0f, nullptr,
+                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             workspace, workspace_bytes, &sa, false);
+  if (rc != LORA_OK) return rc;
+  if (!split_shape(max_num_tokens, rank)) return LORA_ERR_SHAPE;
+  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
+  if (workspace_bytes < base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank))
+    return LORA_ERR_WORKSPACE;
+  sa.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + base);
+  return grg::launch_shrink(sa, static_cast<cudaStream_t>(stream));
+}
+
+int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
+                         const int64_t* slice_width, int num_slices, int rank, float scale,
+                         float* u, uint16_t* y, int64_t y_row_stride,
+                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  grg::ExpandArgs ea;
+  const int rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride,
+                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             workspace, workspace_bytes, &ea);
+  if (rc != LORA_OK) return rc;
+  if (hidden < 8 || hidden > kMaxHidden || (hidden % 8) != 0 ||
+      !split_shape(max_num_tokens, rank))
+    return LORA_ERR_SHAPE;
+  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
+  if (workspace_bytes < base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank))
+    return LORA_ERR_WORKSPACE;
+  ea.partials =
+      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + base);
+  ea.split = split_of(max_num_tokens, max_loras, hidden, num_slices, rank);
+  ea.scale = scale;
+  return grg::launch_expand(ea, static_cast<cudaStream_t>(stream));
+}
+
 int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
                           int64_t max_num_tokens, int64_t max_loras, int32_t* sorted_token_ids,
                           int32_t* num_tokens_per_lora, int32_t* lora_token_start_loc,
@@ -180,6 +266,20 @@ int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
   rc = grg::launch_fused(sa, ea, s);
   if (rc < 0) return rc;
   if (rc == 1) return LORA_OK;
+  // split-K: with the larger workspace, the shrink's CTAs write partial tiles
+  // and the expand sums them in rank order (no cluster-wide steps)
+  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
+  if (split_shape(max_num_tokens, rank) &&
+      workspace_bytes >= base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank) &&
+      grg::shrink_split(sa) >= 2) {
+    rc = lora_shrink_partials(x, x_row_stride, hidden, lora_a, num_slices, rank,
+                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                              const_cast<void*>(workspace), workspace_bytes, stream);
+    if (rc != LORA_OK) return rc;
+    return lora_expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
+                                y_row_stride, sorted_token_ids, lora_token_start_loc,
+                                max_num_tokens, max_loras, workspace, workspace_bytes, stream);
+  }
   rc = grg::launch_shrink(sa, s);
   if (rc != LORA_OK) return rc;
   return grg::launch_expand(ea, s);

@@ -35,7 +35,11 @@ constexpr int kYPitch = 528; // staged y row bytes (512 + 16)
 
 struct ExpandParams {
   CUtensorMap tmap[3];  // B_s viewed as [L * R][N_s], boxes of R x 64
-  const float* u;
+  const float* u;        // u to read, or (partial mode) u to write
+  const float* partials; // partial mode: the shrink's [tile][split][BM][S*R] partial tiles
+  int split;
+  int sr;
+  float scale;
   int max_num_tokens;
   int w0, w1, w2;        // slice widths
   int off0, off1, off2;  // slice column offsets in y
@@ -50,13 +54,18 @@ struct ExpandParams {
   int num_loras;
 };
 
-template <int BM, int RANK, int NS>
+// Largest split of the hidden dimension whose partial tiles the expand sums.
+constexpr int kMaxSplit = 8;
+
+template <int BM, int RANK, int NS, bool PARTIAL>
 struct ExpandLayout {
   static constexpr int kUPitch = RANK * 4 + 16;  // staged u row bytes
   static constexpr int kB = 0;                   // 4 boxes of [RANK][128 B], 1024-aligned
   static constexpr int kY = 4 * RANK * 128;
   static constexpr int kU = kY + BM * kYPitch;
-  static constexpr int kStage = (kU + BM * kUPitch + 1023) / 1024 * 1024;
+  static constexpr int kP = kU + BM * kUPitch;   // partial mode: [split][BM][RANK] fp32
+  static constexpr int kPBytes = PARTIAL ? kMaxSplit * BM * RANK * 4 : 0;
+  static constexpr int kStage = (kP + kPBytes + 1023) / 1024 * 1024;
   static constexpr int kRecSlots = NS + 1;
   static constexpr int kRecBytes = record_ints(BM) * 4;
   static constexpr int kRec = NS * kStage;
@@ -71,10 +80,10 @@ constexpr int expand_stages() {
   return RANK <= 32 ? 2 : 1;
 }
 
-template <int BM, int RANK, int NS>
+template <int BM, int RANK, int NS, bool PARTIAL>
 __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     lora_expand_kernel(const __grid_constant__ ExpandParams p) {
-  using Lay = ExpandLayout<BM, RANK, NS>;
+  using Lay = ExpandLayout<BM, RANK, NS, PARTIAL>;
   constexpr int MT = BM / 16;
   constexpr int RS = Lay::kRecSlots;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -173,14 +182,28 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
                   ok ? p.y + static_cast<long long>(t) * p.y_stride + it.off + col : p.y, ok);
     }
     constexpr int UCH = RANK / 4;  // 16-byte chunks per u row
-    for (int c = tid; c < BM * UCH; c += kExpandThreads) {
-      const int row = c / UCH, ch = c - row * UCH;
-      const int t = record_token(rec, row, tv.count, p.max_num_tokens);
-      const bool ok = t >= 0;
-      cp_async_16(st + Lay::kU + row * Lay::kUPitch + ch * 16,
-                  ok ? p.u + (static_cast<long long>(it.s) * p.max_num_tokens + t) * RANK + ch * 4
-                     : p.u,
-                  ok);
+    if constexpr (PARTIAL) {
+      // the split's partial rows of this slice (the valid rows only)
+      const float* base = p.partials + static_cast<long long>(it.tile) * p.split * BM * p.sr +
+                          it.s * RANK;
+      for (int c = tid; c < p.split * BM * UCH; c += kExpandThreads) {
+        const int ch = c % UCH;
+        const int row = (c / UCH) % BM;
+        const int part = c / (UCH * BM);
+        if (row < tv.count)
+          cp_async_16(st + Lay::kP + ((part * BM + row) * RANK + ch * 4) * 4,
+                      base + (static_cast<long long>(part) * BM + row) * p.sr + ch * 4, true);
+      }
+    } else {
+      for (int c = tid; c < BM * UCH; c += kExpandThreads) {
+        const int row = c / UCH, ch = c - row * UCH;
+        const int t = record_token(rec, row, tv.count, p.max_num_tokens);
+        const bool ok = t >= 0;
+        cp_async_16(st + Lay::kU + row * Lay::kUPitch + ch * 16,
+                    ok ? p.u + (static_cast<long long>(it.s) * p.max_num_tokens + t) * RANK + ch * 4
+                       : p.u,
+                    ok);
+      }
     }
     cp_async_commit();
   };
@@ -224,6 +247,36 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     unsigned char* stp = smem + (k % NS) * Lay::kStage;
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
+
+    if constexpr (PARTIAL) {
+      // u = scale * (sum of the split's partial tiles in rank order), the same
+      // operations in the same order as the shrink's cluster reduction; the
+      // slice's first column block also stores its rows of u
+      constexpr int UCH = RANK / 4;
+      const float* P = reinterpret_cast<const float*>(stp + Lay::kP);
+      for (int e = tid; e < BM * UCH; e += kExpandThreads) {
+        const int row = e / UCH, ch = e - row * UCH;
+        float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (row < tv.count) {
+          sum = *reinterpret_cast<const float4*>(P + row * RANK + ch * 4);
+          for (int c = 1; c < p.split; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(P + (c * BM + row) * RANK + ch * 4);
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+          }
+          sum = make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
+        }
+        *reinterpret_cast<float4*>(stp + Lay::kU + row * Lay::kUPitch + ch * 16) = sum;
+        const int t = record_token(rec, row, tv.count, p.max_num_tokens);
+        if (it.c0 == 0 && t >= 0)
+          *reinterpret_cast<float4*>(const_cast<float*>(p.u) +
+                                     (static_cast<long long>(it.s) * p.max_num_tokens + t) * RANK +
+                                     ch * 4) = sum;
+      }
+      __syncthreads();
+    }
 
 #pragma unroll
     for (int mi = 0; mi < MT; ++mi) {
@@ -323,11 +376,11 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   if (timed_out) atomicOr(p.status, kStatusTimeout);
 }
 
-template <int BM, int RANK>
+template <int BM, int RANK, bool PARTIAL>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
   constexpr int NS = expand_stages<RANK>();
-  const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS>);
-  const size_t smem = ExpandLayout<BM, RANK, NS>::kSmem;
+  const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL>);
+  const size_t smem = ExpandLayout<BM, RANK, NS, PARTIAL>::kSmem;
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -345,6 +398,10 @@ template <int BM>
 static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   ExpandParams p;
   p.u = a.u;
+  p.partials = a.partials;
+  p.split = a.split;
+  p.sr = a.num_slices * a.rank;
+  p.scale = a.scale;
   p.max_num_tokens = a.max_num_tokens;
   int w[3] = {0, 0, 0}, off[3] = {0, 0, 0}, cbs[3] = {0, 0, 0};
   int acc_off = 0, cb_total = 0;
@@ -381,12 +438,25 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
       static_cast<int>(tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM)));
   p.num_loras = a.num_loras;
   const long long max_items = static_cast<long long>(p.tile_capacity) * cb_total;
+  if (a.partials != nullptr) {
+    // partial mode: 16-token tiles and ranks up to 32 only
+    if constexpr (BM == 16) {
+      if (a.split < 1 || a.split > kMaxSplit) return -3;
+      switch (a.rank) {
+        case 8: return run_expand<BM, 8, true>(p, stream, max_items);
+        case 16: return run_expand<BM, 16, true>(p, stream, max_items);
+        case 32: return run_expand<BM, 32, true>(p, stream, max_items);
+        default: return -3;
+      }
+    }
+    return -3;
+  }
   switch (a.rank) {
-    case 8: return run_expand<BM, 8>(p, stream, max_items);
-    case 16: return run_expand<BM, 16>(p, stream, max_items);
-    case 32: return run_expand<BM, 32>(p, stream, max_items);
-    case 64: return run_expand<BM, 64>(p, stream, max_items);
-    case 128: return run_expand<BM, 128>(p, stream, max_items);
+    case 8: return run_expand<BM, 8, false>(p, stream, max_items);
+    case 16: return run_expand<BM, 16, false>(p, stream, max_items);
+    case 32: return run_expand<BM, 32, false>(p, stream, max_items);
+    case 64: return run_expand<BM, 64, false>(p, stream, max_items);
+    case 128: return run_expand<BM, 128, false>(p, stream, max_items);
     default: return -3;
   }
 }
@@ -395,6 +465,7 @@ int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
   // small batches: 16-token tiles give more, shorter items (latency); large
   // batches: 32-token tiles amortise each item's B block over more rows
   if (a.max_num_tokens <= 1024) return launch_expand_bm<16>(a, stream);
+  if (a.partials != nullptr) return -3;
   return launch_expand_bm<32>(a, stream);
 }
 

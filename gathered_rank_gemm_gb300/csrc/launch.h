@@ -53,8 +53,14 @@ struct ShrinkArgs {
   int max_num_tokens;
   int num_loras;
   const void* workspace;
+  // split-K mode: each CTA's partial tile goes to partials[tile][split][16][S*R]
+  // (no cluster reduction, u is not written); null for the normal mode
+  float* partials = nullptr;
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
+// CTAs sharing one tile's hidden dimension (the cluster size of the normal
+// mode, the split of split-K mode) for this shape on the current device.
+int shrink_split(const ShrinkArgs& a);
 
 struct ExpandArgs {
   const float* u;
@@ -69,6 +75,11 @@ struct ExpandArgs {
   int max_num_tokens;
   int num_loras;
   const void* workspace;
+  // split-K mode: sum the shrink's partial tiles (split of them), scale, and
+  // write u instead of reading it; null for the normal mode
+  const float* partials = nullptr;
+  int split = 0;
+  float scale = 1.0f;
 };
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
 

@@ -57,6 +57,8 @@ struct ShrinkParams {
   int stage_bytes;
   int rec_offset;  // byte offsets from the 1024-aligned base
   int bar_offset;  // full[NST] then empty[NST]
+  float* partials;  // split-K mode: [tile][split][BM][S*R] partial tiles; null otherwise
+  int split;        // split-K mode: CTAs per tile (consecutive blocks, no cluster)
 };
 
 template <int BM, int NTW, int NST>
@@ -82,8 +84,10 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
 
   uint32_t cl_size;
   asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cl_size));
-  const int C = static_cast<int>(cl_size);
-  const int crank = static_cast<int>(cluster_ctarank());
+  const bool split_k = p.partials != nullptr;
+  const int C = split_k ? p.split : static_cast<int>(cl_size);
+  const int crank = split_k ? static_cast<int>(blockIdx.x % p.split)
+                            : static_cast<int>(cluster_ctarank());
   const int cluster_id = blockIdx.x / C;
   const int nclusters = gridDim.x / C;
   const int kb0 = crank * p.kb_per_rank;
@@ -267,6 +271,26 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     // sum the k-split warps into red[0]
     float* red = reinterpret_cast<float*>(smem);
     const int e4 = (BM * SR) >> 2;
+    if (split_k) {
+      // split-K mode: this CTA's partial tile (its warps summed in the same
+      // order) goes to the workspace; the expand sums the split in rank order
+      float4* dst = reinterpret_cast<float4*>(p.partials) +
+                    (static_cast<long long>(item) * C + crank) * e4;
+      for (int idx = tid; idx < e4; idx += kShrinkThreads) {
+        float4 v = reinterpret_cast<float4*>(red)[idx];
+        for (int w = 1; w < WK; ++w) {
+          const float4 o = reinterpret_cast<float4*>(red + w * BM * SR)[idx];
+          v.x += o.x;
+          v.y += o.y;
+          v.z += o.z;
+          v.w += o.w;
+        }
+        dst[idx] = v;
+      }
+      fence_proxy_async();  // generic use of the ring before the next item's TMA writes
+      __syncthreads();
+      continue;
+    }
     if (WK > 1) {
       for (int idx = tid; idx < e4; idx += kShrinkThreads) {
         float4 v = reinterpret_cast<float4*>(red)[idx];
@@ -330,17 +354,18 @@ static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStr
   if (grid > useful) grid = useful;
   if (grid < cluster) grid = cluster;
   ShrinkParams p = prm;
+  // split-K mode: a tile's CTAs are consecutive blocks, no cluster launch
   return launch_pdl(fn, dim3(static_cast<unsigned>(grid)), dim3(kShrinkThreads), smem, stream,
-                    cluster, &p);
+                    p.partials != nullptr ? 0 : cluster, &p);
 }
 
-int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
+static int shrink_tile_rows(const ShrinkArgs& a) {
+  return (a.num_slices * a.rank >= 192 || a.max_num_tokens <= 1024) ? 16 : 32;
+}
+
+int shrink_split(const ShrinkArgs& a) {
   const int SR = a.num_slices * a.rank;
-  const int NT = SR / 8;
-  const int warps_n = NT <= 8 ? 1 : (NT <= 16 ? 2 : 4);
-  const int ntw = (NT + warps_n - 1) / warps_n;
-  const int WK = kConsumerWarps / warps_n;
-  const int BM = (SR >= 192 || a.max_num_tokens <= 1024) ? 16 : 32;
+  const int BM = shrink_tile_rows(a);
   const int kblocks = (a.hidden + kBK - 1) / kBK;
   const long long max_tiles = tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM));
   const int sms = device_sm_count();
@@ -352,6 +377,20 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   while (cluster < max_cluster && static_cast<long long>(cluster) * max_tiles < 3LL * sms &&
          kblocks >= 8 * cluster)
     cluster *= 2;
+  return cluster;
+}
+
+int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
+  const int SR = a.num_slices * a.rank;
+  const int NT = SR / 8;
+  const int warps_n = NT <= 8 ? 1 : (NT <= 16 ? 2 : 4);
+  const int ntw = (NT + warps_n - 1) / warps_n;
+  const int WK = kConsumerWarps / warps_n;
+  const int BM = shrink_tile_rows(a);
+  const int kblocks = (a.hidden + kBK - 1) / kBK;
+  const long long max_tiles = tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM));
+  const int cluster = shrink_split(a);
+  if (a.partials != nullptr && BM != 16) return -3;
   const int kb_per = (kblocks + cluster - 1) / cluster;
   // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
   // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
@@ -391,6 +430,8 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.status = ws.status;
   p.tile_capacity = static_cast<int>(max_tiles);
   p.num_loras = a.num_loras;
+  p.partials = a.partials;
+  p.split = cluster;
   p.warps_n = warps_n;
   p.ntw = ntw;
   p.stage_bytes = stage;

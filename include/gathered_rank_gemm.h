@@ -162,10 +162,15 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
  * and rules as lora_shrink followed by lora_expand (u is written too).  When
  * the batch is small enough for a thread-block cluster to hold a tile's whole
  * problem on chip (decode-sized batches: up to 16 k-blocks of 64 columns and
- * 48 output units of 64 columns per CTA), one fused kernel does both steps and
- * the expand reads u from shared memory; otherwise the two kernels of
- * lora_shrink and lora_expand run back to back.  Either way the work stays on
- * the GPU.
+ * 48 output units of 64 columns per CTA) and every tile's cluster fits in one
+ * wave, one fused kernel does both steps and the expand reads u from shared
+ * memory.  Otherwise two kernels run back to back: with a workspace of at
+ * least lora_shrink_expand_workspace_size bytes and a batch of up to 1024
+ * tokens with rank <= 32, the shrink's CTAs write partial tiles of u into the
+ * workspace and the expand adds them up (same operations in the same order
+ * as the cluster reduction of lora_shrink, so u and y are bit-identical to
+ * the two separate calls); else the kernels of lora_shrink and lora_expand
+ * run unchanged.  Either way the work stays on the GPU.
  */
 int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t *const *lora_a, const uint16_t *const *lora_b,
@@ -174,6 +179,49 @@ int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
                        int64_t max_num_tokens, int64_t max_loras, const void *workspace,
                        size_t workspace_bytes, void *stream);
+
+/*
+ * Workspace bytes that let lora_shrink_expand take its split-K path for this
+ * shape: lora_workspace_size plus 8 * 16 * num_slices * rank * 4 bytes per
+ * 16-token tile of the batch when max_num_tokens <= 1024 and rank <= 32
+ * (else just lora_workspace_size); 0 for sizes the calls reject.  A smaller
+ * workspace (at least lora_workspace_size) is still valid for every call.
+ */
+size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_loras,
+                                         int64_t hidden, const int64_t *slice_width,
+                                         int num_slices, int rank);
+
+/*
+ * The two halves of lora_shrink_expand's split-K path, for callers that want
+ * to place other work between them (and for timing each kernel).  Same
+ * arguments and rules as lora_shrink / lora_expand, with these differences:
+ *   - the shape must have max_num_tokens <= 1024 and rank <= 32, and the
+ *     workspace must hold lora_shrink_expand_workspace_size bytes
+ *     (LORA_ERR_SHAPE / LORA_ERR_WORKSPACE otherwise);
+ *   - lora_shrink_partials splits each 16-token tile's hidden dimension over
+ *     up to 8 CTAs (the cluster size lora_shrink would use) and writes each
+ *     CTA's fp32 partial tile (its warps summed) into the workspace behind the
+ *     metadata: [tile][split][16][num_slices * rank].  It does not scale and
+ *     does not write u.
+ *   - lora_expand_partials takes `hidden` (it fixes the split) and `scale`,
+ *     sums each tile's partials in CTA order, multiplies by scale, writes the
+ *     result to u (rows of tokens with an adapter) and adds u * B into y.
+ * Run back to back on one stream they give bit for bit the u and y of
+ * lora_shrink followed by lora_expand.  The partials of one call pair live in
+ * the workspace: a second pair on the same workspace must be ordered after
+ * the first expand (same stream, or an event).
+ */
+int lora_shrink_partials(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                         const uint16_t *const *lora_a, int num_slices, int rank,
+                         const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, void *workspace,
+                         size_t workspace_bytes, void *stream);
+int lora_expand_partials(int64_t hidden, const uint16_t *const *lora_b,
+                         const int64_t *slice_width, int num_slices, int rank, float scale,
+                         float *u, uint16_t *y, int64_t y_row_stride,
+                         const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /*
  * Kernels one lora_shrink_expand call launches for this shape on the current

@@ -64,7 +64,7 @@ class DeviceCase:
     """One layer's inputs on the device plus the metadata buffers (guarded)."""
 
     def __init__(self, shape: W.LayerShape, mapping: np.ndarray, layer: W.Layer, dev,
-                 x_pad: int = 0, y_pad: int = 0):
+                 x_pad: int = 0, y_pad: int = 0, split_workspace: bool = False):
         torch = torch_mod()
         self.shape, self.mapping_np, self.layer, self.dev = shape, mapping, layer, dev
         T, L = shape.max_num_tokens, shape.max_loras
@@ -90,7 +90,11 @@ class DeviceCase:
         self.sorted = Guarded((T,), torch.int32, dev, fill_bits=0x11111111)
         self.counts = Guarded((L + 1,), torch.int32, dev, fill_bits=0x22222222)
         self.starts = Guarded((L + 2,), torch.int32, dev, fill_bits=0x33333333)
-        ws_bytes = binding.lora_workspace_size(T, L)
+        self.ws_base = binding.lora_workspace_size(T, L)
+        ws_bytes = self.ws_base
+        if split_workspace:
+            ws_bytes = binding.lora_shrink_expand_workspace_size(
+                T, L, shape.hidden, shape.slice_widths, shape.rank)
         self.ws = Guarded((ws_bytes,), torch.uint8, dev, fill_bits=0)
 
     def prepare(self, stream=None):

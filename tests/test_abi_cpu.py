@@ -61,6 +61,23 @@ def test_workspace_size(lib):
     assert small >= 64 + 8 * entries
 
 
+def test_shrink_expand_workspace_size(lib):
+    base = binding.lora_workspace_size(256, 4)
+    # split-K path: 8 partial tiles of 16 rows x S*R floats per 16-token tile
+    tiles = 256 // 16 + 4
+    assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4096,) * 3, 8) == \
+        base + tiles * 8 * 16 * 24 * 4
+    # beyond 1024 tokens or rank 32 only the metadata part
+    assert binding.lora_shrink_expand_workspace_size(2048, 4, 4096, (4096,), 16) == \
+        binding.lora_workspace_size(2048, 4)
+    assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4096,), 64) == base
+    # rejected sizes
+    assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4096,), 12) == 0
+    assert binding.lora_shrink_expand_workspace_size(256, 4, 100, (4096,), 8) == 0
+    assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4095,), 8) == 0
+    assert binding.lora_shrink_expand_workspace_size(0, 4, 4096, (4096,), 8) == 0
+
+
 def test_error_strings(lib):
     for code in range(0, -7, -1):
         assert lib.lora_error_string(code)
@@ -134,6 +151,39 @@ def test_expand_validation(lib):
     bad_w = (ctypes.c_int64 * 2)(512, 500)
     assert call(wp=ctypes.addressof(bad_w)) == -3
     assert call(wsb=8) == -4
+
+
+def test_split_halves_validation(lib):
+    """Every call here is rejected before anything is enqueued."""
+    big = binding.lora_shrink_expand_workspace_size(64, 4, 512, (512,), 8)
+    small = binding.lora_workspace_size(64, 4)
+    assert big > small
+    a = _arr(P16)
+    fs = lib.lora_shrink_partials
+
+    def shrink(x=P16, stride=512, hidden=512, s=1, r=8, T=64, L=4, wsb=big):
+        return fs(x, stride, hidden, ctypes.addressof(a), s, r, P16, P16, T, L, P16, wsb, None)
+
+    assert shrink(x=None) == -1
+    assert shrink(x=PODD) == -2
+    assert shrink(r=12) == -3
+    assert shrink(r=64) == -3           # split-K path: rank <= 32
+    assert shrink(T=2048, wsb=1 << 24) == -3  # split-K path: up to 1024 tokens
+    assert shrink(wsb=small) == -4      # no room for the partial tiles
+    b = _arr(P16)
+    w = (ctypes.c_int64 * 1)(512)
+    fe = lib.lora_expand_partials
+
+    def expand(hidden=512, r=8, u=P16, y=P16, T=64, wsb=big):
+        return fe(hidden, ctypes.addressof(b), ctypes.addressof(w), 1, r, 1.0, u, y, 512, P16,
+                  P16, T, 4, P16, wsb, None)
+
+    assert expand(u=None) == -1
+    assert expand(y=PODD) == -2
+    assert expand(hidden=500) == -3
+    assert expand(r=64) == -3
+    assert expand(T=2048, wsb=1 << 24) == -3
+    assert expand(wsb=small) == -4
 
 
 def test_read_status_validation(lib):

@@ -394,3 +394,95 @@ def test_shrink_expand_one_call_in_a_graph_with_new_mappings(dev):
         eager.run(fused=True)
         assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
         assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
+
+
+# ------------------------------------------------------------ one-call split-K path
+
+# hidden sizes above 8192 keep these shapes off the single-wave fused kernel
+# (more than 16 k-blocks per CTA), so the one call takes the split-K path
+SPLIT_SHAPES = [
+    ("decode_qkv", None),
+    ("ragged3", (300, 211, 8208, (264, 72, 136), 6, 8)),
+    ("rank16", (256, 256, 9216, (512, 512), 4, 16)),
+    ("rank32", (1000, 977, 8264, (1032, 520, 264), 5, 32)),
+    ("many_loras", (512, 500, 8200, (1024,), 64, 8)),
+]
+
+
+def _split_case(name, spec, dev):
+    if spec is None:
+        wl = W.make_workload(name)
+        return DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev, split_workspace=True)
+    T, n, H, widths, L, R = spec
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, neg_prob=0.15)
+    rng = np.random.default_rng(T + R + 7)
+    return DeviceCase(shape, W.make_mapping(shape, rng), W.make_layer(shape, rng), dev,
+                      split_workspace=True)
+
+
+@pytest.mark.parametrize("name,spec", SPLIT_SHAPES)
+def test_split_k_one_call_matches_the_oracle(name, spec, dev):
+    case = _split_case(name, spec, dev)
+    assert case.ws.view.numel() > case.ws_base  # the larger workspace was offered
+    check_case(case, fused=True, sample_rows=400)
+    # the split-K path ran: its partial tiles landed behind the metadata
+    assert torch.any(case.ws.view[case.ws_base:] != 0)
+
+
+@pytest.mark.parametrize("name,spec", SPLIT_SHAPES[:3])
+def test_split_k_one_call_is_bit_identical_to_the_two_calls(name, spec, dev):
+    a = _split_case(name, spec, dev)
+    b = _split_case(name, spec, dev)
+    a.run(fused=False)
+    b.run(fused=True)
+    assert torch.any(b.ws.view[b.ws_base:] != 0)
+    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
+    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
+
+
+def test_split_k_one_call_in_a_graph_with_new_mappings(dev):
+    sh = W.custom_shape(max_num_tokens=256, num_tokens=256, hidden=8200,
+                        slice_widths=(1024, 1024, 1024), max_loras=8, rank=8, neg_prob=0.1)
+    rng = np.random.default_rng(23)
+    layer = W.make_layer(sh, rng)
+    g_case = DeviceCase(sh, W.make_mapping(sh, rng), layer, dev, split_workspace=True)
+    stream = torch.cuda.Stream()
+    y_clean = g_case.y.view.clone()
+    with torch.cuda.stream(stream):
+        g_case.prepare(stream); g_case.shrink_expand(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        g_case.prepare(stream)
+        g_case.shrink_expand(stream)
+    for trial, n_new in enumerate((256, 100, 17, 0)):
+        sh2 = W.custom_shape(max_num_tokens=256, num_tokens=n_new, hidden=8200,
+                             slice_widths=(1024, 1024, 1024), max_loras=8, rank=8, neg_prob=0.2)
+        m_new = W.make_mapping(sh2, np.random.default_rng(400 + trial))
+        g_case.mapping.copy_(torch.from_numpy(m_new))
+        g_case.n.fill_(n_new)
+        g_case.y.view.copy_(y_clean)
+        g_case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        eager = DeviceCase(sh2, m_new, layer, dev)
+        eager.run(fused=False)
+        assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
+        assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
+
+
+@pytest.mark.parametrize("name,spec", SPLIT_SHAPES[:2])
+def test_split_k_halves_equal_the_one_call(name, spec, dev):
+    a = _split_case(name, spec, dev)
+    b = _split_case(name, spec, dev)
+    a.run(fused=True)
+    b.prepare()
+    binding.lora_shrink_partials(b.x, b.a, b.sorted.view, b.starts.view, b.ws.view)
+    binding.lora_expand_partials(b.shape.hidden, b.b, b.shape.scale, b.u.view, b.y_view,
+                                 b.sorted.view, b.starts.view, b.ws.view)
+    torch.cuda.synchronize()
+    assert b.guards_intact()
+    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
+    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
