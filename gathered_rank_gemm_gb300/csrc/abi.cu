@@ -116,16 +116,15 @@ size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras) {
 namespace {
 // Split-K one-call path: batches of up to 1024 tokens (16-token tiles) and
 // ranks up to 32.  Its partial tiles follow the metadata part of the
-// workspace: [16-token tile][split <= 8][16][S*R] fp32.
+// workspace: [16-token tile][split <= split_k_max(rank)][16][S*R] fp32.
 constexpr int64_t kSplitMaxTokens = 1024;
 constexpr int kSplitMaxRank = 32;
-constexpr int kSplitMax = 8;
 bool split_shape(int64_t max_num_tokens, int rank) {
   return max_num_tokens <= kSplitMaxTokens && rank <= kSplitMaxRank;
 }
 size_t split_scratch_bytes(int64_t max_num_tokens, int64_t max_loras, int num_slices, int rank) {
-  return static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) * kSplitMax *
-         16 * num_slices * rank * 4;
+  return static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) *
+         grg::split_k_max(rank) * 16 * num_slices * rank * 4;
 }
 }  // namespace
 
@@ -152,7 +151,7 @@ int split_of(int64_t max_num_tokens, int64_t max_loras, int64_t hidden, int num_
   a.rank = rank;
   a.max_num_tokens = static_cast<int>(max_num_tokens);
   a.num_loras = static_cast<int>(max_loras);
-  return grg::shrink_split(a);
+  return grg::shrink_split(a, true);
 }
 }  // namespace
 
@@ -174,12 +173,13 @@ int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden
   return grg::launch_shrink(sa, static_cast<cudaStream_t>(stream));
 }
 
-int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
-                         const int64_t* slice_width, int num_slices, int rank, float scale,
-                         float* u, uint16_t* y, int64_t y_row_stride,
-                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
-                         int64_t max_num_tokens, int64_t max_loras, const void* workspace,
-                         size_t workspace_bytes, void* stream) {
+namespace {
+int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t* slice_width,
+                    int num_slices, int rank, float scale, float* u, uint16_t* y,
+                    int64_t y_row_stride, const int32_t* sorted_token_ids,
+                    const int32_t* lora_token_start_loc, int64_t max_num_tokens,
+                    int64_t max_loras, const void* workspace, size_t workspace_bytes,
+                    void* stream, bool y_early) {
   grg::ExpandArgs ea;
   const int rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride,
                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
@@ -195,7 +195,21 @@ int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + base);
   ea.split = split_of(max_num_tokens, max_loras, hidden, num_slices, rank);
   ea.scale = scale;
+  ea.y_early = y_early;
   return grg::launch_expand(ea, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
+                         const int64_t* slice_width, int num_slices, int rank, float scale,
+                         float* u, uint16_t* y, int64_t y_row_stride,
+                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  // the caller may run anything between the halves: y only after the wait
+  return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
+                         y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                         max_loras, workspace, workspace_bytes, stream, false);
 }
 
 int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
@@ -271,17 +285,19 @@ int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
   const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
   if (split_shape(max_num_tokens, rank) &&
       workspace_bytes >= base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank) &&
-      grg::shrink_split(sa) >= 2) {
+      grg::shrink_split(sa, true) >= 2) {
     rc = lora_shrink_partials(x, x_row_stride, hidden, lora_a, num_slices, rank,
                               sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
                               const_cast<void*>(workspace), workspace_bytes, stream);
     if (rc != LORA_OK) return rc;
-    return lora_expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
-                                y_row_stride, sorted_token_ids, lora_token_start_loc,
-                                max_num_tokens, max_loras, workspace, workspace_bytes, stream);
+    // the expand directly follows the shrink, which never writes y
+    return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
+                           y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                           max_loras, workspace, workspace_bytes, stream, true);
   }
   rc = grg::launch_shrink(sa, s);
   if (rc != LORA_OK) return rc;
+  ea.y_early = true;  // the expand directly follows the shrink, which never writes y
   return grg::launch_expand(ea, s);
 }
 

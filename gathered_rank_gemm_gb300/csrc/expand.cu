@@ -40,6 +40,7 @@ struct ExpandParams {
   int split;
   int sr;
   float scale;
+  int y_early;  // y may be read before the dependency wait (the one-call path)
   int max_num_tokens;
   int w0, w1, w2;        // slice widths
   int off0, off1, off2;  // slice column offsets in y
@@ -54,8 +55,6 @@ struct ExpandParams {
   int num_loras;
 };
 
-// Largest split of the hidden dimension whose partial tiles the expand sums.
-constexpr int kMaxSplit = 8;
 
 template <int BM, int RANK, int NS, bool PARTIAL>
 struct ExpandLayout {
@@ -64,7 +63,7 @@ struct ExpandLayout {
   static constexpr int kY = 4 * RANK * 128;
   static constexpr int kU = kY + BM * kYPitch;
   static constexpr int kP = kU + BM * kUPitch;   // partial mode: [split][BM][RANK] fp32
-  static constexpr int kPBytes = PARTIAL ? kMaxSplit * BM * RANK * 4 : 0;
+  static constexpr int kPBytes = PARTIAL ? split_k_max(RANK) * BM * RANK * 4 : 0;
   static constexpr int kStage = (kP + kPBytes + 1023) / 1024 * 1024;
   static constexpr int kRecSlots = NS + 1;
   static constexpr int kRecBytes = record_ints(BM) * 4;
@@ -165,8 +164,8 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
       tma_load_2d(st + Lay::kB + b * RANK * 128, &p.tmap[it.s], it.c0 + 64 * b, tv.lora * RANK,
                   bar);
   };
-  // gathered y segments and u rows of item k -> stage (every thread, one group)
-  auto issue_uy = [&](int k) {
+  // gathered y segments of item k -> stage (every thread; part of the next group)
+  auto issue_y = [&](int k) {
     const Item it = item_of(k);
     const int32_t* rec = rec_of(k);
     const TileView tv = TileView::of(rec, BM, p.num_loras);
@@ -181,6 +180,13 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
       cp_async_16(st + Lay::kY + row * kYPitch + ych * 16,
                   ok ? p.y + static_cast<long long>(t) * p.y_stride + it.off + col : p.y, ok);
     }
+  };
+  // rows of u (or of the split's partial tiles) of item k -> stage, closing the group
+  auto issue_u = [&](int k) {
+    const Item it = item_of(k);
+    const int32_t* rec = rec_of(k);
+    const TileView tv = TileView::of(rec, BM, p.num_loras);
+    const uint32_t st = sbase + (k % NS) * Lay::kStage;
     constexpr int UCH = RANK / 4;  // 16-byte chunks per u row
     if constexpr (PARTIAL) {
       // the split's partial rows of this slice (the valid rows only)
@@ -207,6 +213,10 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     }
     cp_async_commit();
   };
+  auto issue_uy = [&](int k) {
+    issue_y(k);
+    issue_u(k);
+  };
 
   // prologue: the records of the first items and the first B block before the
   // dependency wait (metadata and weights), the activations after it
@@ -214,26 +224,41 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   if (tid == 0) {
     for (int k = 0; k < min(nloc, RS); ++k) issue_rec(k);
   }
-  wait_rec(0);
-  if (tid == 0) issue_b(0);
-  {
-    // warm L2 (and the TLB) with item 0's y rows while the previous kernel finishes
-    const Item it = item_of(0);
-    const int32_t* rec = rec_of(0);
-    const TileView tv = TileView::of(rec, BM, p.num_loras);
-    const int bytes = min(kEN, it.width - it.c0) * 2;
-    for (int r = tid; r < tv.count; r += kExpandThreads) {
-      const int t = record_token(rec, r, tv.count, p.max_num_tokens);
-      if (t >= 0) prefetch_l2(p.y + static_cast<long long>(t) * p.y_stride + it.off + it.c0, bytes);
+  if (p.y_early) {
+    // y is not written by the preceding shrink, and every kernel before that
+    // one had completed when the shrink triggered this launch: the first
+    // items' y segments load before the dependency wait, u / partials after
+    for (int k = 0; k < npro; ++k) {
+      wait_rec(k);
+      if (tid == 0) issue_b(k);
+      issue_y(k);
     }
-  }
-  pdl_wait();
-  pdl_launch_dependents();
-  issue_uy(0);
-  for (int k = 1; k < npro; ++k) {
-    wait_rec(k);
-    if (tid == 0) issue_b(k);
-    issue_uy(k);
+    pdl_wait();
+    pdl_launch_dependents();
+    for (int k = 0; k < npro; ++k) issue_u(k);
+  } else {
+    wait_rec(0);
+    if (tid == 0) issue_b(0);
+    {
+      // warm L2 (and the TLB) with item 0's y rows while the previous kernel finishes
+      const Item it = item_of(0);
+      const int32_t* rec = rec_of(0);
+      const TileView tv = TileView::of(rec, BM, p.num_loras);
+      const int bytes = min(kEN, it.width - it.c0) * 2;
+      for (int r = tid; r < tv.count; r += kExpandThreads) {
+        const int t = record_token(rec, r, tv.count, p.max_num_tokens);
+        if (t >= 0)
+          prefetch_l2(p.y + static_cast<long long>(t) * p.y_stride + it.off + it.c0, bytes);
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    issue_uy(0);
+    for (int k = 1; k < npro; ++k) {
+      wait_rec(k);
+      if (tid == 0) issue_b(k);
+      issue_uy(k);
+    }
   }
 
   for (int k = 0; k < nloc; ++k) {
@@ -402,6 +427,7 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   p.split = a.split;
   p.sr = a.num_slices * a.rank;
   p.scale = a.scale;
+  p.y_early = a.y_early ? 1 : 0;
   p.max_num_tokens = a.max_num_tokens;
   int w[3] = {0, 0, 0}, off[3] = {0, 0, 0}, cbs[3] = {0, 0, 0};
   int acc_off = 0, cb_total = 0;
@@ -441,7 +467,7 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   if (a.partials != nullptr) {
     // partial mode: 16-token tiles and ranks up to 32 only
     if constexpr (BM == 16) {
-      if (a.split < 1 || a.split > kMaxSplit) return -3;
+      if (a.split < 1 || a.split > split_k_max(a.rank)) return -3;
       switch (a.rank) {
         case 8: return run_expand<BM, 8, true>(p, stream, max_items);
         case 16: return run_expand<BM, 16, true>(p, stream, max_items);

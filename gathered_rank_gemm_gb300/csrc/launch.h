@@ -58,9 +58,13 @@ struct ShrinkArgs {
   float* partials = nullptr;
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
-// CTAs sharing one tile's hidden dimension (the cluster size of the normal
-// mode, the split of split-K mode) for this shape on the current device.
-int shrink_split(const ShrinkArgs& a);
+// CTAs sharing one tile's hidden dimension for this shape on the current
+// device: the cluster size of the normal mode (at most 8), or the split of
+// split-K mode (at most split_k_max(rank): no cluster, so no portable limit).
+int shrink_split(const ShrinkArgs& a, bool split_k);
+// Largest split-K split for a rank (bounds the expand's staging of partial
+// tiles and the workspace's partial-tile area).
+constexpr int split_k_max(int rank) { return rank <= 16 ? 16 : 8; }
 
 struct ExpandArgs {
   const float* u;
@@ -80,6 +84,9 @@ struct ExpandArgs {
   const float* partials = nullptr;
   int split = 0;
   float scale = 1.0f;
+  // y may be read before the dependency wait: only when the expand directly
+  // follows this library's shrink on the stream (the one-call path)
+  bool y_early = false;
 };
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
 

@@ -166,11 +166,11 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
  * wave, one fused kernel does both steps and the expand reads u from shared
  * memory.  Otherwise two kernels run back to back: with a workspace of at
  * least lora_shrink_expand_workspace_size bytes and a batch of up to 1024
- * tokens with rank <= 32, the shrink's CTAs write partial tiles of u into the
- * workspace and the expand adds them up (same operations in the same order
- * as the cluster reduction of lora_shrink, so u and y are bit-identical to
- * the two separate calls); else the kernels of lora_shrink and lora_expand
- * run unchanged.  Either way the work stays on the GPU.
+ * tokens with rank <= 32, the shrink's CTAs (up to 16 per tile, no cluster)
+ * write partial tiles of u into the workspace and the expand adds them up in
+ * CTA order (u and y then match the two separate calls up to the order of
+ * the fp32 partial sums); else the kernels of lora_shrink and lora_expand run
+ * unchanged.  Either way the work stays on the GPU.
  */
 int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t *const *lora_a, const uint16_t *const *lora_b,
@@ -182,10 +182,11 @@ int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
 
 /*
  * Workspace bytes that let lora_shrink_expand take its split-K path for this
- * shape: lora_workspace_size plus 8 * 16 * num_slices * rank * 4 bytes per
- * 16-token tile of the batch when max_num_tokens <= 1024 and rank <= 32
- * (else just lora_workspace_size); 0 for sizes the calls reject.  A smaller
- * workspace (at least lora_workspace_size) is still valid for every call.
+ * shape: lora_workspace_size plus P * 16 * num_slices * rank * 4 bytes per
+ * 16-token tile of the batch (P = 16 for rank <= 16, 8 for rank 32: the
+ * largest split) when max_num_tokens <= 1024 and rank <= 32 (else just
+ * lora_workspace_size); 0 for sizes the calls reject.  A smaller workspace
+ * (at least lora_workspace_size) is still valid for every call.
  */
 size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_loras,
                                          int64_t hidden, const int64_t *slice_width,
@@ -199,15 +200,17 @@ size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_lor
  *     workspace must hold lora_shrink_expand_workspace_size bytes
  *     (LORA_ERR_SHAPE / LORA_ERR_WORKSPACE otherwise);
  *   - lora_shrink_partials splits each 16-token tile's hidden dimension over
- *     up to 8 CTAs (the cluster size lora_shrink would use) and writes each
- *     CTA's fp32 partial tile (its warps summed) into the workspace behind the
- *     metadata: [tile][split][16][num_slices * rank].  It does not scale and
- *     does not write u.
+ *     up to P CTAs (as for the workspace size above; no cluster) and writes
+ *     each CTA's fp32 partial tile (its warps summed) into the workspace
+ *     behind the metadata: [tile][split][16][num_slices * rank].  It does not
+ *     scale and does not write u.
  *   - lora_expand_partials takes `hidden` (it fixes the split) and `scale`,
  *     sums each tile's partials in CTA order, multiplies by scale, writes the
  *     result to u (rows of tokens with an adapter) and adds u * B into y.
- * Run back to back on one stream they give bit for bit the u and y of
- * lora_shrink followed by lora_expand.  The partials of one call pair live in
+ * Run back to back on one stream they give the u and y of lora_shrink
+ * followed by lora_expand up to the order of the fp32 partial sums (bit for
+ * bit when the split equals lora_shrink's cluster size).  The partials of one
+ * call pair live in
  * the workspace: a second pair on the same workspace must be ordered after
  * the first expand (same stream, or an event).
  */

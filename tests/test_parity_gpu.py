@@ -430,15 +430,29 @@ def test_split_k_one_call_matches_the_oracle(name, spec, dev):
     assert torch.any(case.ws.view[case.ws_base:] != 0)
 
 
+def _close_to_the_two_calls(a, b):
+    """The split-K one call against lora_shrink + lora_expand: the same fp32
+    products summed in another grouping, so u agrees to fp32 rounding and y
+    to one bf16 rounding step; untouched rows stay bit-identical."""
+    ua, ub = a.u.view.double(), b.u.view.double()
+    rows = lora_rows(a.mapping_np, a.shape.num_tokens, a.shape.max_loras)
+    assert torch.all((ua[:, rows] - ub[:, rows]).abs() <= 1e-6 + 1e-5 * ua[:, rows].abs())
+    keep = np.ones(a.shape.max_num_tokens, bool)
+    keep[rows] = False
+    assert torch.equal(a.u.view.view(torch.int32)[:, keep], b.u.view.view(torch.int32)[:, keep])
+    ya, yb = a.y.view[rows].double(), b.y.view[rows].double()
+    assert torch.all((ya - yb).abs() <= 1e-3 + 2.0 ** -7 * ya.abs())
+    assert torch.equal(a.y.view.view(torch.int16)[keep], b.y.view.view(torch.int16)[keep])
+
+
 @pytest.mark.parametrize("name,spec", SPLIT_SHAPES[:3])
-def test_split_k_one_call_is_bit_identical_to_the_two_calls(name, spec, dev):
+def test_split_k_one_call_agrees_with_the_two_calls(name, spec, dev):
     a = _split_case(name, spec, dev)
     b = _split_case(name, spec, dev)
     a.run(fused=False)
     b.run(fused=True)
     assert torch.any(b.ws.view[b.ws_base:] != 0)
-    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
-    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
+    _close_to_the_two_calls(a, b)
 
 
 def test_split_k_one_call_in_a_graph_with_new_mappings(dev):
@@ -467,8 +481,8 @@ def test_split_k_one_call_in_a_graph_with_new_mappings(dev):
         torch.cuda.synchronize()
         graph.replay()
         torch.cuda.synchronize()
-        eager = DeviceCase(sh2, m_new, layer, dev)
-        eager.run(fused=False)
+        eager = DeviceCase(sh2, m_new, layer, dev, split_workspace=True)
+        eager.run(fused=True)
         assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
         assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
 
