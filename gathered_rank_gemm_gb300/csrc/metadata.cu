@@ -6,19 +6,22 @@
 // Enable CUDAGraphs for V1" (vLLM PR 14626): the map is a static buffer of
 // max_num_tokens entries and the pad rows past n hold garbage.
 //
-// One CTA of 16 warps runs a stable counting sort over bins 0..L (bin L = no
-// adapter):
-//   1. warp w takes the contiguous token range [w*seg, (w+1)*seg) and counts
-//      its tokens per bin (lanes with the same bin are grouped with
-//      __match_any_sync, the group leader adds the group size);
-//   2. per bin, an exclusive scan over the 16 warp counts gives each warp's
-//      offset inside the bin; one block scan over the bin totals (and, per
-//      tile height, the tiles per adapter) gives lora_token_start_loc and the
-//      first tile of every adapter;
+// A cluster of C CTAs of 16 warps (C = 1 up to 1024 tokens, up to 8 beyond:
+// a size known at capture time) runs a stable counting sort over bins 0..L
+// (bin L = no adapter):
+//   1. warp w of CTA c takes the contiguous token range [g*seg, (g+1)*seg),
+//      g = 16 c + w, and counts its tokens per bin (lanes with the same bin
+//      are grouped with __match_any_sync, the group leader adds the size);
+//   2. per bin, an exclusive scan over the CTA's 16 warp counts gives each
+//      warp's offset inside the CTA's share of the bin; the CTAs' totals are
+//      exchanged through distributed shared memory, giving every CTA the bin
+//      totals and its own offset (the sum over lower-ranked CTAs); one block
+//      scan over the bin totals (and, per tile height, the tiles per adapter)
+//      gives lora_token_start_loc and the first tile of every adapter;
 //   3. each warp walks its range again in order; a token's slot is
-//      start[bin] + warp offset + (earlier lanes of its group in this step).
-// Warp ranges are in token order and lanes are in token order, so equal ids
-// keep ascending token order (stable).  The grid is one CTA whatever the data,
+//      start[bin] + CTA offset + warp offset + (earlier lanes of its group).
+// Ranges are in token order (CTA, then warp, then lane), so equal ids keep
+// ascending token order (stable).  The grid depends only on max_num_tokens,
 // so the launch is graph-safe.  The kernel also writes, for each tile height
 // in {16, 32, 64, 128}, the list of tile records (adapter, count and the
 // tile's token ids inline) that the shrink and expand kernels walk with a
@@ -112,8 +115,17 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   int32_t* start = total + nbins;              // [nbins + 1]
   int32_t* cnts = start + nbins + 1;           // [kScanArrays][nbins]: totals, tiles per height
   int32_t* offs = cnts + kScanArrays * nbins;   // [kScanArrays][nbins + 1]: starts, tile offsets
+  int32_t* ctot = offs + kScanArrays * (nbins + 1);  // [nbins]: this CTA's tokens per bin
+  int32_t* coff = ctot + nbins;                      // [nbins]: lower-ranked CTAs' tokens per bin
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t cl_size;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cl_size));
+  const int C = static_cast<int>(cl_size);
+  const int crank = static_cast<int>(cluster_ctarank());
+  const int gwarp = crank * kMetaWarps + warp;
+  const int cthreads = C * kMetaThreads;  // threads of the whole cluster
+  const int ctid = crank * kMetaThreads + tid;
   // Dependents are released only at the very end, after a fence: kernels of
   // this library read the work list before their own dependency wait.
   pdl_wait();
@@ -130,8 +142,8 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   __syncthreads();
   const int n = s_n;
 
-  const int seg = ((n + kMetaWarps - 1) / kMetaWarps + 31) & ~31;
-  const int lo = min(warp * seg, n), hi = min(lo + seg, n);
+  const int seg = ((n + C * kMetaWarps - 1) / (C * kMetaWarps) + 31) & ~31;
+  const int lo = min(gwarp * seg, n), hi = min(lo + seg, n);
   int32_t* my_hist = hist + warp * nbins;
 
   // Bins of this lane's tokens for one chunk of kMetaChunk 32-token steps:
@@ -179,8 +191,10 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   if (bad) atomicOr(&s_status, 1u);
   __syncthreads();
 
-  // pass 2: warp offsets inside each bin, bin totals; then one scan gives
-  // the bin starts and, per tile height, each adapter's first tile
+  // pass 2: warp offsets inside the CTA's share of each bin, the CTA's bin
+  // counts; the cluster's counts give the bin totals and this CTA's offsets;
+  // then one scan gives the bin starts and, per tile height, each adapter's
+  // first tile
   for (int b = tid; b < nbins; b += kMetaThreads) {
     int run = 0;
     for (int w = 0; w < kMetaWarps; ++w) {
@@ -188,7 +202,35 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
       hist[w * nbins + b] = run;
       run += c;
     }
-    total[b] = run;
+    ctot[b] = run;
+  }
+  if (C > 1) {
+    cluster_sync_all();  // every CTA's counts are in its shared memory
+    const uint32_t ctot_addr = smem_u32(ctot);
+    for (int b = tid; b < nbins; b += kMetaThreads) {
+      int below = 0, all = 0;
+      for (int c = 0; c < C; ++c) {
+        int v;
+        asm volatile("ld.shared::cluster.s32 %0, [%1];\n"
+                     : "=r"(v)
+                     : "r"(mapa_shared(ctot_addr + 4u * b, static_cast<uint32_t>(c)))
+                     : "memory");
+        if (c < crank) below += v;
+        all += v;
+      }
+      coff[b] = below;
+      total[b] = all;
+    }
+  } else {
+    __syncthreads();
+    for (int b = tid; b < nbins; b += kMetaThreads) {
+      coff[b] = 0;
+      total[b] = ctot[b];
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < nbins; b += kMetaThreads) {
+    const int run = total[b];
     cnts[b] = run;
 #pragma unroll
     for (int k = 0; k < kNumTileSizes; ++k) {
@@ -212,7 +254,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
       const int bin = bins[j];
       const unsigned peers = __match_any_sync(0xffffffffu, bin);
       if (bin < nbins) {
-        const int rel = my_hist[bin] + __popc(peers & ((1u << lane) - 1u));
+        const int rel = coff[bin] + my_hist[bin] + __popc(peers & ((1u << lane) - 1u));
         p.sorted_ids[start[bin] + rel] = t;
         if (bin < L) {
 #pragma unroll
@@ -228,9 +270,11 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
       __syncwarp();
     }
   }
-  for (int t = n + tid; t < p.max_num_tokens; t += kMetaThreads) p.sorted_ids[t] = -1;
-  for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
-  for (int b = tid; b <= nbins; b += kMetaThreads) p.starts[b] = start[b];
+  for (int t = n + ctid; t < p.max_num_tokens; t += cthreads) p.sorted_ids[t] = -1;
+  if (crank == 0) {
+    for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
+    for (int b = tid; b <= nbins; b += kMetaThreads) p.starts[b] = start[b];
+  }
 
   // record headers
 #pragma unroll
@@ -239,7 +283,7 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
     const int32_t* off = toff + k * (nbins + 1);
     const int count = off[L];
     int32_t* list = p.ws.lists[k];
-    for (int i = tid; i < count; i += kMetaThreads) {
+    for (int i = ctid; i < count; i += cthreads) {
       // largest l with off[l] <= i (adapters with no tile share the next offset)
       int a = 0, b = L - 1;
       while (a < b) {
@@ -250,21 +294,25 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
       int4 h = make_int4(a, min(rows, total[a] - j * rows), start[a] + j * rows, 0);
       *reinterpret_cast<int4*>(list + static_cast<long long>(i) * record_ints(rows)) = h;
     }
-    if (tid == 0) p.ws.num_tiles[k] = count;
+    if (ctid == 0) p.ws.num_tiles[k] = count;
   }
   if (tid == 0) {
-    *p.ws.n = n;
+    if (crank == 0) *p.ws.n = n;
     if (s_status) atomicOr(p.ws.status, s_status);
   }
   __threadfence();
-  __syncthreads();
+  // no CTA exits while another may still read its counts
+  if (C > 1)
+    cluster_sync_all();
+  else
+    __syncthreads();
   pdl_launch_dependents();
 }
 
 static size_t meta_smem_bytes(int num_loras) {
   const size_t nb = static_cast<size_t>(num_loras) + 1;
   return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + kScanArrays * nb +
-                            kScanArrays * (nb + 1));
+                            kScanArrays * (nb + 1) + 2 * nb);
 }
 
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
@@ -282,8 +330,11 @@ int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_n
   const size_t smem = meta_smem_bytes(num_loras);
   if (ensure_smem_attr(reinterpret_cast<const void*>(lora_metadata_kernel), smem) != 0)
     return -6;
-  return launch_pdl(reinterpret_cast<const void*>(lora_metadata_kernel), dim3(1),
-                    dim3(kMetaThreads), smem, stream, 1, &p);
+  // one CTA per 1024 tokens of the buffer, a power of two up to 8: one cluster
+  int cluster = 1;
+  while (cluster < 8 && static_cast<long long>(cluster) * 1024 < max_num_tokens) cluster *= 2;
+  return launch_pdl(reinterpret_cast<const void*>(lora_metadata_kernel), dim3(cluster),
+                    dim3(kMetaThreads), smem, stream, cluster, &p);
 }
 
 }  // namespace grg
