@@ -219,6 +219,18 @@ def oracle_sample_size(wl: W.Workload, budget_s: float, threads: int):
     return max(1, min(n, int(budget_s / max(per_tok, 1e-9))))
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(wl: W.Workload, seconds: float = 10.0):
     import oracle
     threads = oracle.max_threads()
@@ -229,7 +241,15 @@ def cpu_baseline(wl: W.Workload, seconds: float = 10.0):
         tok += t
         el += dt
         reps += 1
+    # one thread, for about a quarter of the time (its own sample size)
+    k1 = oracle_sample_size(wl, min(2.0, seconds / 4), 1)
+    tok1, el1 = 0, 0.0
+    while el1 < seconds / 4 or tok1 == 0:
+        t, dt = oracle_sample_step(wl, k1, 1)
+        tok1 += t
+        el1 += dt
     return {"value": tok / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "single_thread_value": tok1 / el1, "cpu": cpu_model(),
             "sample": f"{reps} passes over the first {k} of {wl.shape.num_tokens} tokens of one "
                       f"{wl.shape.name} layer (grouping + shrink + expand, fp64), {el:.1f} s"}
 
@@ -467,6 +487,7 @@ def run_ours(args, world, rank, local):
             "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
+                         "frac_of_nominal_8tbs": achieved / 8000.0,
                          "algorithmic_bytes_per_launch": dom_bytes,
                          "traffic": recorded_traffic(dominant + ("-split" if split_k else ""),
                                                      shape.name)},
@@ -482,6 +503,7 @@ def run_ours(args, world, rank, local):
             "tflops": {"shrink": alg["flops"]["shrink"] / (ms_shrink * 1e-3) / 1e12,
                        "expand": alg["flops"]["expand"] / (ms_expand * 1e-3) / 1e12},
             "lora_tokens": alg["n_lora_tokens"], "active_loras": alg["active_loras"],
+            "lora_tokens_per_s": alg["n_lora_tokens"] * layers * world / (ms_step_max * 1e-3),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
