@@ -66,7 +66,7 @@ def _load():
         lib.oracle_prepare_metadata.restype = ctypes.c_uint32
         lib.oracle_prepare_metadata.argtypes = [p, i64, i64, i64, p, p, p]
         lib.oracle_shrink.restype = None
-        lib.oracle_shrink.argtypes = [p, i64, i64, p, i64, i64, ctypes.c_double, p, i64, i64,
+        lib.oracle_shrink.argtypes = [p, i64, i64, p, i64, i64, ctypes.c_double, p, p, i64, i64,
                                       p, i64, ctypes.c_int]
         lib.oracle_expand.restype = None
         lib.oracle_expand.argtypes = [p, p, p, i64, i64, p, i64, p, i64, i64, p, i64,
@@ -112,8 +112,9 @@ def prepare_metadata(token_lora_mapping: np.ndarray, num_tokens: int, max_loras:
 
 def shrink(x_bits: np.ndarray, lora_a_bits, scale: float, token_lora_mapping: np.ndarray,
            num_tokens: int, max_loras: int, u_init: np.ndarray | None = None,
-           num_threads: int = 0) -> np.ndarray:
-    """u[s][t][r] = scale * sum_h x[t][h] A_s[m[t]][r][h] in fp64.
+           num_threads: int = 0, lora_scales=None) -> np.ndarray:
+    """u[s][t][r] = c(m[t]) * sum_h x[t][h] A_s[m[t]][r][h] in fp64, with
+    c(l) = scale, or scale * lora_scales[l] when per-adapter factors are given.
 
     ``x_bits``: uint16 bf16 bits ``[T_max, H]``; ``lora_a_bits``: list of S
     uint16 arrays ``[L, R, H]``.  Rows of tokens without an adapter (and
@@ -135,8 +136,14 @@ def shrink(x_bits: np.ndarray, lora_a_bits, scale: float, token_lora_mapping: np
     else:
         u = np.array(u_init, dtype=np.float64, copy=True, order="C")
     ptrs = (ctypes.c_void_p * num_slices)(*[_ptr(a) for a in a_list])
+    ls = None
+    if lora_scales is not None:
+        ls = _c(np.asarray(lora_scales, dtype=np.float64), np.float64)
+        if ls.shape != (max_loras,):
+            raise ValueError("lora_scales must have max_loras entries")
     _load().oracle_shrink(_ptr(x), hidden, hidden, ctypes.addressof(ptrs), num_slices, rank,
-                          float(scale), _ptr(m), int(num_tokens), int(max_loras), _ptr(u), t_max,
+                          float(scale), None if ls is None else _ptr(ls), _ptr(m),
+                          int(num_tokens), int(max_loras), _ptr(u), t_max,
                           int(num_threads) or max_threads())
     return u
 

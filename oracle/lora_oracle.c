@@ -21,6 +21,7 @@
  *
  *   metadata:  stable grouping of t in [0, n) by m[t] (bin L = no adapter)
  *   shrink:    u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]
+ *              (times lora_scales[m[t]] when a per-adapter factor is given)
  *   expand:    y[t][off_s + j] += sum_r u[s][t][r] * B_s[m[t]][r][j]
  *
  * for t < n with 0 <= m[t] < L only.  Everything is plain loops in the
@@ -96,7 +97,9 @@ uint32_t oracle_prepare_metadata(const int32_t *token_lora_mapping, int64_t num_
 }
 
 /*
- * Shrink: u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]   (fp64)
+ * Shrink: u[s][t][r] = c(m[t]) * sum_h x[t][h] * A_s[m[t]][r][h]   (fp64)
+ *   c(l)          scale, or scale * lora_scales[l] when lora_scales is given
+ *                 (a per-adapter factor; the pages are silent on it)
  *   x             bf16 bits, row t at x + t * x_row_stride, hidden entries
  *   lora_a[s]     bf16 bits, [L][R][hidden] row-major
  *   u             double, [S][max_num_tokens][R]; only rows of tokens
@@ -104,8 +107,9 @@ uint32_t oracle_prepare_metadata(const int32_t *token_lora_mapping, int64_t num_
  */
 void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                    const uint16_t *const *lora_a, int64_t num_slices, int64_t rank,
-                   double scale, const int32_t *token_lora_mapping, int64_t num_tokens,
-                   int64_t num_loras, double *u, int64_t max_num_tokens, int num_threads)
+                   double scale, const double *lora_scales, const int32_t *token_lora_mapping,
+                   int64_t num_tokens, int64_t num_loras, double *u, int64_t max_num_tokens,
+                   int num_threads)
 {
     int64_t t;
 #pragma omp parallel for schedule(dynamic, 4) num_threads(num_threads)
@@ -113,13 +117,14 @@ void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
         int32_t id = token_lora_mapping[t];
         if (id < 0 || (int64_t)id >= num_loras) continue;
         const uint16_t *xrow = x + t * x_row_stride;
+        const double c = lora_scales ? scale * lora_scales[id] : scale;
         for (int64_t s = 0; s < num_slices; ++s) {
             const uint16_t *a = lora_a[s] + (int64_t)id * rank * hidden;
             for (int64_t r = 0; r < rank; ++r) {
                 double acc = 0.0;
                 for (int64_t h = 0; h < hidden; ++h)
                     acc += bf16_bits_to_double(xrow[h]) * bf16_bits_to_double(a[r * hidden + h]);
-                u[(s * max_num_tokens + t) * rank + r] = scale * acc;
+                u[(s * max_num_tokens + t) * rank + r] = c * acc;
             }
         }
     }

@@ -211,6 +211,26 @@ def test_shrink_scale_is_linear_and_zero_scale_gives_zero():
     assert np.all(u0 == 0.0)
 
 
+def test_shrink_per_adapter_scales_match_dense_rows_and_the_scalar_path():
+    """Per-adapter factors: each row equals the dense numpy product scaled
+    by scale * factor of its adapter; factors of 1 give the scalar result."""
+    rng = np.random.default_rng(15)
+    T, H, widths, L, R = 40, 72, (16, 24), 4, 8
+    x, a, _, _ = _random_layer(rng, T, H, widths, L, R)
+    m = rng.integers(-1, L, size=T).astype(np.int32)
+    f = np.array([0.5, -2.0, 0.0, 3.25])
+    u = oracle.shrink(x, a, 0.75, m, T, L, lora_scales=f)
+    for t in range(T):
+        for s in range(len(widths)):
+            if m[t] < 0:
+                assert np.all(np.isnan(u[s, t]))
+            else:
+                ref = 0.75 * f[m[t]] * (val(a[s][m[t]]) @ val(x[t]))
+                np.testing.assert_allclose(u[s, t], ref, rtol=1e-12, atol=1e-12)
+    ones = oracle.shrink(x, a, 0.75, m, T, L, lora_scales=np.ones(L))
+    assert np.array_equal(ones, oracle.shrink(x, a, 0.75, m, T, L), equal_nan=True)
+
+
 def test_shrink_leaves_unmapped_and_pad_rows_untouched():
     rng = np.random.default_rng(15)
     T, n, H, L, R = 16, 11, 32, 2, 8
