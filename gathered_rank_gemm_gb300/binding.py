@@ -56,8 +56,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_prepare_metadata.restype = i32
     lib.lora_prepare_metadata.argtypes = [p, p, i64, i64, p, p, p, p, sz, p]
     lib.lora_shrink.restype = i32
-    lib.lora_shrink.argtypes = [p, i64, i64, p, i32, i32, ctypes.c_float, p, p, p, i64, i64, p,
-                                sz, p]
+    lib.lora_shrink.argtypes = [p, i64, i64, p, i32, i32, ctypes.c_float, p, p, p, p, i64, i64,
+                                p, sz, p]
     lib.lora_expand.restype = i32
     lib.lora_expand.argtypes = [p, p, p, i32, i32, p, i64, p, p, i64, i64, p, sz, p]
     lib.lora_read_status.restype = i32
@@ -65,8 +65,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_error_string.restype = ctypes.c_char_p
     lib.lora_error_string.argtypes = [i32]
     lib.lora_shrink_expand.restype = i32
-    lib.lora_shrink_expand.argtypes = [p, i64, i64, p, p, p, i32, i32, ctypes.c_float, p, p, i64,
-                                       p, p, i64, i64, p, sz, p]
+    lib.lora_shrink_expand.argtypes = [p, i64, i64, p, p, p, i32, i32, ctypes.c_float, p, p, p,
+                                       i64, p, p, i64, i64, p, sz, p]
     lib.lora_shrink_expand_kernels.restype = i32
     lib.lora_shrink_expand_kernels.argtypes = [i64, i64, i64, p, i32, i32]
     lib.lora_shrink_expand_workspace_size.restype = sz
@@ -74,11 +74,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_shrink_partials.restype = i32
     lib.lora_shrink_partials.argtypes = [p, i64, i64, p, i32, i32, p, p, i64, i64, p, sz, p]
     lib.lora_expand_partials.restype = i32
-    lib.lora_expand_partials.argtypes = [i64, p, p, i32, i32, ctypes.c_float, p, p, i64, p, p,
-                                         i64, i64, p, sz, p]
+    lib.lora_expand_partials.argtypes = [i64, p, p, i32, i32, ctypes.c_float, p, p, p, i64, p,
+                                         p, i64, i64, p, sz, p]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
-                                       ctypes.c_float, p, p, i64, p, p, p, p, p]
+                                       ctypes.c_float, p, p, p, i64, p, p, p, p, p]
     _lib = lib
     return lib
 
@@ -99,6 +99,18 @@ def _dev(t, name: str):
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
     return t.data_ptr()
+
+
+def _scales(lora_scales, num_loras):
+    """Device pointer of the per-adapter factors (fp32 [max_loras]) or None."""
+    if lora_scales is None:
+        return None
+    import torch
+    if lora_scales.dtype != torch.float32 or lora_scales.numel() != num_loras:
+        raise ValueError("lora_scales must be a float32 CUDA tensor of max_loras entries")
+    if not lora_scales.is_contiguous():
+        raise ValueError("lora_scales must be contiguous")
+    return _dev(lora_scales, "lora_scales")
 
 
 def _ptr_array(tensors, name):
@@ -126,14 +138,14 @@ def lora_prepare_metadata(token_lora_mapping, num_tokens, max_loras: int, sorted
 
 
 def lora_shrink(x, lora_a, scale: float, u, sorted_token_ids, lora_token_start_loc, workspace,
-                stream=None):
-    """u[s][t][r] = scale * x[t] . A_s[m[t]][r] for the adapter tokens."""
+                stream=None, lora_scales=None):
+    """u[s][t][r] = scale (* lora_scales[m[t]]) * x[t] . A_s[m[t]][r] for the adapter tokens."""
     lora_a = list(lora_a)
     arr = _ptr_array(lora_a, "lora_a")
     num_loras, rank, hidden = lora_a[0].shape
     rc = load().lora_shrink(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(lora_a), rank,
-        float(scale), _dev(u, "u"), _dev(sorted_token_ids, "sorted_token_ids"),
+        float(scale), _scales(lora_scales, num_loras), _dev(u, "u"), _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream, x.device))
@@ -156,7 +168,7 @@ def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace,
 
 
 def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
-                       lora_token_start_loc, workspace, stream=None):
+                       lora_token_start_loc, workspace, stream=None, lora_scales=None):
     """Shrink then expand in one call (one fused kernel for decode-sized batches)."""
     lora_a, lora_b = list(lora_a), list(lora_b)
     arr_a = _ptr_array(lora_a, "lora_a")
@@ -165,7 +177,8 @@ def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
     num_loras, rank, hidden = lora_a[0].shape
     rc = load().lora_shrink_expand(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr_a), ctypes.addressof(arr_b),
-        ctypes.addressof(widths), len(lora_a), rank, float(scale), _dev(u, "u"), _dev(y, "y"),
+        ctypes.addressof(widths), len(lora_a), rank, float(scale),
+        _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"),
         y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -189,7 +202,7 @@ def lora_shrink_partials(x, lora_a, sorted_token_ids, lora_token_start_loc, work
 
 
 def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_ids,
-                         lora_token_start_loc, workspace, stream=None):
+                         lora_token_start_loc, workspace, stream=None, lora_scales=None):
     """Sums the split-K partials (scaled) into u, then y += u . B_s (in place)."""
     lora_b = list(lora_b)
     arr = _ptr_array(lora_b, "lora_b")
@@ -197,7 +210,7 @@ def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_i
     num_loras, rank = lora_b[0].shape[:2]
     rc = load().lora_expand_partials(
         int(hidden), ctypes.addressof(arr), ctypes.addressof(widths), len(lora_b), rank,
-        float(scale), _dev(u, "u"), _dev(y, "y"), y.stride(0),
+        float(scale), _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"), y.stride(0),
         _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), y.shape[0], num_loras,
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
@@ -236,7 +249,7 @@ def lora_read_status(workspace, stream=None) -> int:
 
 def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale: float, u, y,
                        sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
-                       status=None, stream=None):
+                       status=None, stream=None, lora_scales=None):
     """Grouping + shrink + expand of one layer without any allocation.
 
     For callers that cannot allocate device memory: the workspace is the
@@ -254,8 +267,8 @@ def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale:
         _dev(token_lora_mapping, "token_lora_mapping"), _dev(num_tokens, "num_tokens"),
         token_lora_mapping.shape[0], num_loras, _dev(x, "x"), x.stride(0), hidden,
         ctypes.addressof(arr_a), ctypes.addressof(arr_b), ctypes.addressof(widths), len(lora_a),
-        rank, float(scale), _dev(u, "u"), _dev(y, "y"), y.stride(0),
-        _dev(sorted_token_ids, "sorted_token_ids"),
+        rank, float(scale), _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"),
+        y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(num_tokens_per_lora, "num_tokens_per_lora"),
         _dev(lora_token_start_loc, "lora_token_start_loc"),
         None if status is None else _dev(status, "status"), _stream_ptr(stream, x.device))
@@ -288,25 +301,25 @@ class LoraMetadata:
                               self.sorted_token_ids, self.num_tokens_per_lora,
                               self.lora_token_start_loc, self.workspace, stream)
 
-    def shrink(self, x, lora_a, scale, u, stream=None):
+    def shrink(self, x, lora_a, scale, u, stream=None, lora_scales=None):
         lora_shrink(x, lora_a, scale, u, self.sorted_token_ids, self.lora_token_start_loc,
-                    self.workspace, stream)
+                    self.workspace, stream, lora_scales)
 
     def expand(self, u, lora_b, y, stream=None):
         lora_expand(u, lora_b, y, self.sorted_token_ids, self.lora_token_start_loc,
                     self.workspace, stream)
 
-    def shrink_expand(self, x, lora_a, lora_b, scale, u, y, stream=None):
+    def shrink_expand(self, x, lora_a, lora_b, scale, u, y, stream=None, lora_scales=None):
         lora_shrink_expand(x, lora_a, lora_b, scale, u, y, self.sorted_token_ids,
-                           self.lora_token_start_loc, self.workspace, stream)
+                           self.lora_token_start_loc, self.workspace, stream, lora_scales)
 
     def shrink_partials(self, x, lora_a, stream=None):
         lora_shrink_partials(x, lora_a, self.sorted_token_ids, self.lora_token_start_loc,
                              self.workspace, stream)
 
-    def expand_partials(self, hidden, lora_b, scale, u, y, stream=None):
+    def expand_partials(self, hidden, lora_b, scale, u, y, stream=None, lora_scales=None):
         lora_expand_partials(hidden, lora_b, scale, u, y, self.sorted_token_ids,
-                             self.lora_token_start_loc, self.workspace, stream)
+                             self.lora_token_start_loc, self.workspace, stream, lora_scales)
 
     def read_status(self, stream=None) -> int:
         return lora_read_status(self.workspace, stream)

@@ -24,7 +24,8 @@ constexpr int64_t kMaxWidth = 1 << 20;
 
 // Argument checks of lora_shrink; fills the launcher's arguments.
 int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
-                const uint16_t* const* lora_a, int num_slices, int rank, float scale, float* u,
+                const uint16_t* const* lora_a, int num_slices, int rank, float scale,
+                const float* lora_scales, float* u,
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, grg::ShrinkArgs* out, bool need_u = true) {
@@ -51,6 +52,7 @@ int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
   a.num_slices = num_slices;
   a.rank = rank;
   a.scale = scale;
+  a.lora_scales = lora_scales;
   a.u = u;
   a.sorted_ids = sorted_token_ids;
   a.starts = lora_token_start_loc;
@@ -162,7 +164,7 @@ int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden
                          size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs sa;
   const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, 1.0f, nullptr,
-                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             nullptr, sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
                              workspace, workspace_bytes, &sa, false);
   if (rc != LORA_OK) return rc;
   if (!split_shape(max_num_tokens, rank)) return LORA_ERR_SHAPE;
@@ -175,7 +177,8 @@ int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden
 
 namespace {
 int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t* slice_width,
-                    int num_slices, int rank, float scale, float* u, uint16_t* y,
+                    int num_slices, int rank, float scale, const float* lora_scales, float* u,
+                    uint16_t* y,
                     int64_t y_row_stride, const int32_t* sorted_token_ids,
                     const int32_t* lora_token_start_loc, int64_t max_num_tokens,
                     int64_t max_loras, const void* workspace, size_t workspace_bytes,
@@ -195,6 +198,7 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
       reinterpret_cast<const float*>(static_cast<const char*>(workspace) + base);
   ea.split = split_of(max_num_tokens, max_loras, hidden, num_slices, rank);
   ea.scale = scale;
+  ea.lora_scales = lora_scales;
   ea.y_early = y_early;
   return grg::launch_expand(ea, static_cast<cudaStream_t>(stream));
 }
@@ -202,12 +206,12 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
 
 int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
                          const int64_t* slice_width, int num_slices, int rank, float scale,
-                         float* u, uint16_t* y, int64_t y_row_stride,
+                         const float* lora_scales, float* u, uint16_t* y, int64_t y_row_stride,
                          const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                          int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                          size_t workspace_bytes, void* stream) {
   // the caller may run anything between the halves: y only after the wait
-  return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
+  return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, lora_scales, u, y,
                          y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
                          max_loras, workspace, workspace_bytes, stream, false);
 }
@@ -234,14 +238,15 @@ int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_
 }
 
 int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
-                const uint16_t* const* lora_a, int num_slices, int rank, float scale, float* u,
+                const uint16_t* const* lora_a, int num_slices, int rank, float scale,
+                const float* lora_scales, float* u,
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs a;
-  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, u,
-                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
-                             workspace, workspace_bytes, &a);
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale,
+                             lora_scales, u, sorted_token_ids, lora_token_start_loc,
+                             max_num_tokens, max_loras, workspace, workspace_bytes, &a);
   if (rc != LORA_OK) return rc;
   return grg::launch_shrink(a, static_cast<cudaStream_t>(stream));
 }
@@ -262,13 +267,13 @@ int lora_expand(const float* u, const uint16_t* const* lora_b, const int64_t* sl
 int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t* const* lora_a, const uint16_t* const* lora_b,
                        const int64_t* slice_width, int num_slices, int rank, float scale,
-                       float* u, uint16_t* y, int64_t y_row_stride,
+                       const float* lora_scales, float* u, uint16_t* y, int64_t y_row_stride,
                        const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                        int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                        size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs sa;
   grg::ExpandArgs ea;
-  int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, u,
+  int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, lora_scales, u,
                        sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
                        workspace, workspace_bytes, &sa);
   if (rc != LORA_OK) return rc;
@@ -291,9 +296,9 @@ int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                               const_cast<void*>(workspace), workspace_bytes, stream);
     if (rc != LORA_OK) return rc;
     // the expand directly follows the shrink, which never writes y
-    return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, u, y,
-                           y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
-                           max_loras, workspace, workspace_bytes, stream, true);
+    return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, lora_scales, u,
+                           y, y_row_stride, sorted_token_ids, lora_token_start_loc,
+                           max_num_tokens, max_loras, workspace, workspace_bytes, stream, true);
   }
   rc = grg::launch_shrink(sa, s);
   if (rc != LORA_OK) return rc;

@@ -40,6 +40,7 @@ struct ExpandParams {
   int split;
   int sr;
   float scale;
+  const float* lora_scales;  // partial mode: per-adapter factors on scale, or null
   int y_early;  // y may be read before the dependency wait (the one-call path)
   int max_num_tokens;
   int w0, w1, w2;        // slice widths
@@ -291,7 +292,8 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
             sum.z += v.z;
             sum.w += v.w;
           }
-          sum = make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
+          const float c = p.lora_scales != nullptr ? p.scale * p.lora_scales[tv.lora] : p.scale;
+          sum = make_float4(sum.x * c, sum.y * c, sum.z * c, sum.w * c);
         }
         *reinterpret_cast<float4*>(stp + Lay::kU + row * Lay::kUPitch + ch * 16) = sum;
         const int t = record_token(rec, row, tv.count, p.max_num_tokens);
@@ -427,6 +429,7 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   p.split = a.split;
   p.sr = a.num_slices * a.rank;
   p.scale = a.scale;
+  p.lora_scales = a.lora_scales;
   p.y_early = a.y_early ? 1 : 0;
   p.max_num_tokens = a.max_num_tokens;
   int w[3] = {0, 0, 0}, off[3] = {0, 0, 0}, cbs[3] = {0, 0, 0};

@@ -47,6 +47,7 @@ struct FusedParams {
   int rank_shift;
   int sr;
   float scale;
+  const float* lora_scales;  // per-adapter factors on scale, or null
   float* u;
   int max_num_tokens;
   __nv_bfloat16* y;
@@ -269,7 +270,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           sum.w += part[c].w;
         }
       }
-      sum = make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
+      const float sc = p.lora_scales != nullptr ? p.scale * p.lora_scales[lora] : p.scale;
+      sum = make_float4(sum.x * sc, sum.y * sc, sum.z * sc, sum.w * sc);
       reinterpret_cast<float4*>(utile)[idx] = sum;
       const int e = idx << 2;
       const int row = e / SR;
@@ -509,6 +511,7 @@ int launch_fused(const ShrinkArgs& sa, const ExpandArgs& ea, cudaStream_t stream
   p.rank_shift = __builtin_ctz(static_cast<unsigned>(R));
   p.sr = SR;
   p.scale = sa.scale;
+  p.lora_scales = sa.lora_scales;
   p.u = sa.u;
   p.max_num_tokens = sa.max_num_tokens;
   p.y = static_cast<__nv_bfloat16*>(ea.y);

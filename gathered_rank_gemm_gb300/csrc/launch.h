@@ -47,6 +47,7 @@ struct ShrinkArgs {
   int num_slices;
   int rank;
   float scale;
+  const float* lora_scales = nullptr;  // per-adapter factors on scale (device, [num_loras])
   float* u;
   const int32_t* sorted_ids;
   const int32_t* starts;
@@ -84,6 +85,7 @@ struct ExpandArgs {
   const float* partials = nullptr;
   int split = 0;
   float scale = 1.0f;
+  const float* lora_scales = nullptr;
   // y may be read before the dependency wait: only when the expand directly
   // follows this library's shrink on the stream (the one-call path)
   bool y_early = false;

@@ -47,7 +47,8 @@ extern "C" int lora_apply_noalloc(const int32_t* token_lora_mapping, const int32
                                   int64_t x_row_stride, int64_t hidden,
                                   const uint16_t* const* lora_a, const uint16_t* const* lora_b,
                                   const int64_t* slice_width, int num_slices, int rank,
-                                  float scale, float* u, uint16_t* y, int64_t y_row_stride,
+                                  float scale, const float* lora_scales, float* u, uint16_t* y,
+                                  int64_t y_row_stride,
                                   int32_t* sorted_token_ids, int32_t* num_tokens_per_lora,
                                   int32_t* lora_token_start_loc, uint32_t* status, void* stream) {
   const size_t need = lora_workspace_size(max_num_tokens, max_loras);
@@ -63,7 +64,8 @@ extern "C" int lora_apply_noalloc(const int32_t* token_lora_mapping, const int32
                                  sorted_token_ids, num_tokens_per_lora, lora_token_start_loc, ws,
                                  kScratchBytes, stream);
   if (rc != LORA_OK) return rc;
-  rc = lora_shrink(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, u, sorted_token_ids,
+  rc = lora_shrink(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, lora_scales, u,
+                   sorted_token_ids,
                    lora_token_start_loc, max_num_tokens, max_loras, ws, kScratchBytes, stream);
   if (rc != LORA_OK) return rc;
   rc = lora_expand(u, lora_b, slice_width, num_slices, rank, y, y_row_stride, sorted_token_ids,

@@ -44,6 +44,7 @@ struct ShrinkParams {
   int rank_shift;  // log2(rank)
   int sr;          // num_slices * rank: stacked A rows
   float scale;
+  const float* lora_scales;  // per-adapter factors on scale, or null
   float* u;
   int max_num_tokens;
   const int32_t* records;  // tile records of height BM
@@ -341,8 +342,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       const int s = col >> p.rank_shift;
       const int r = col - (s << p.rank_shift);
       float* dst = p.u + (static_cast<long long>(s) * p.max_num_tokens + t) * p.rank + r;
-      *reinterpret_cast<float4*>(dst) =
-          make_float4(sum.x * p.scale, sum.y * p.scale, sum.z * p.scale, sum.w * p.scale);
+      const float c = p.lora_scales != nullptr ? p.scale * p.lora_scales[lora] : p.scale;
+      *reinterpret_cast<float4*>(dst) = make_float4(sum.x * c, sum.y * c, sum.z * c, sum.w * c);
     }
     fence_proxy_async();  // generic use of the ring before the next item's TMA writes
     cluster_sync_all();
@@ -434,6 +435,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.rank_shift = __builtin_ctz(static_cast<unsigned>(a.rank));
   p.sr = SR;
   p.scale = a.scale;
+  p.lora_scales = a.lora_scales;
   p.u = a.u;
   p.max_num_tokens = a.max_num_tokens;
   WsView ws = ws_view(const_cast<void*>(a.workspace), a.max_num_tokens, a.num_loras);

@@ -114,11 +114,15 @@ int lora_prepare_metadata(const int32_t *token_lora_mapping, const int32_t *num_
 /*
  * Shrink ("[V1] LoRA - Add triton kernels for V1": gather each token's input
  * row through the token -> LoRA information and multiply by its adapter's A):
- *   u[s][t][r] = scale * sum_h x[t][h] * A_s[m[t]][r][h]     (bf16 in, fp32 out)
+ *   u[s][t][r] = c(m[t]) * sum_h x[t][h] * A_s[m[t]][r][h]  (bf16 in, fp32 out)
+ *   c(l) = scale, or scale * lora_scales[l] (in fp32) when lora_scales is given
  *
  *   x                bf16[max_num_tokens][x_row_stride], hidden columns used
  *   lora_a           HOST array of num_slices device pointers, each
  *                    bf16[max_loras][rank][hidden] row-major
+ *   lora_scales      NULL, or device fp32[max_loras]: a per-adapter factor on
+ *                    scale (the pages are silent on per-LoRA scales); read
+ *                    after the preceding kernel on the stream has finished
  *   u                fp32[num_slices][max_num_tokens][rank] out; only rows of
  *                    adapter tokens t < n are written
  *   sorted_token_ids, lora_token_start_loc, workspace: from lora_prepare_metadata
@@ -129,7 +133,8 @@ int lora_prepare_metadata(const int32_t *token_lora_mapping, const int32_t *num_
  */
 int lora_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                 const uint16_t *const *lora_a, int num_slices, int rank, float scale,
-                float *u, const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                const float *lora_scales, float *u, const int32_t *sorted_token_ids,
+                const int32_t *lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void *workspace,
                 size_t workspace_bytes, void *stream);
 
@@ -175,7 +180,7 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
 int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t *const *lora_a, const uint16_t *const *lora_b,
                        const int64_t *slice_width, int num_slices, int rank, float scale,
-                       float *u, uint16_t *y, int64_t y_row_stride,
+                       const float *lora_scales, float *u, uint16_t *y, int64_t y_row_stride,
                        const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
                        int64_t max_num_tokens, int64_t max_loras, const void *workspace,
                        size_t workspace_bytes, void *stream);
@@ -204,9 +209,10 @@ size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_lor
  *     each CTA's fp32 partial tile (its warps summed) into the workspace
  *     behind the metadata: [tile][split][16][num_slices * rank].  It does not
  *     scale and does not write u.
- *   - lora_expand_partials takes `hidden` (it fixes the split) and `scale`,
- *     sums each tile's partials in CTA order, multiplies by scale, writes the
- *     result to u (rows of tokens with an adapter) and adds u * B into y.
+ *   - lora_expand_partials takes `hidden` (it fixes the split), `scale` and
+ *     `lora_scales`, sums each tile's partials in CTA order, multiplies by
+ *     c(lora) as lora_shrink does, writes the result to u (rows of tokens
+ *     with an adapter) and adds u * B into y.
  * Run back to back on one stream they give the u and y of lora_shrink
  * followed by lora_expand up to the order of the fp32 partial sums (bit for
  * bit when the split equals lora_shrink's cluster size).  The partials of one
@@ -221,7 +227,7 @@ int lora_shrink_partials(const uint16_t *x, int64_t x_row_stride, int64_t hidden
                          size_t workspace_bytes, void *stream);
 int lora_expand_partials(int64_t hidden, const uint16_t *const *lora_b,
                          const int64_t *slice_width, int num_slices, int rank, float scale,
-                         float *u, uint16_t *y, int64_t y_row_stride,
+                         const float *lora_scales, float *u, uint16_t *y, int64_t y_row_stride,
                          const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
                          int64_t max_num_tokens, int64_t max_loras, const void *workspace,
                          size_t workspace_bytes, void *stream);
@@ -271,8 +277,8 @@ int lora_apply_noalloc(const int32_t *token_lora_mapping, const int32_t *num_tok
                        int64_t max_num_tokens, int64_t max_loras, const uint16_t *x,
                        int64_t x_row_stride, int64_t hidden, const uint16_t *const *lora_a,
                        const uint16_t *const *lora_b, const int64_t *slice_width,
-                       int num_slices, int rank, float scale, float *u, uint16_t *y,
-                       int64_t y_row_stride, int32_t *sorted_token_ids,
+                       int num_slices, int rank, float scale, const float *lora_scales,
+                       float *u, uint16_t *y, int64_t y_row_stride, int32_t *sorted_token_ids,
                        int32_t *num_tokens_per_lora, int32_t *lora_token_start_loc,
                        uint32_t *status, void *stream);
 

@@ -64,9 +64,14 @@ class DeviceCase:
     """One layer's inputs on the device plus the metadata buffers (guarded)."""
 
     def __init__(self, shape: W.LayerShape, mapping: np.ndarray, layer: W.Layer, dev,
-                 x_pad: int = 0, y_pad: int = 0, split_workspace: bool = False):
+                 x_pad: int = 0, y_pad: int = 0, split_workspace: bool = False,
+                 lora_scales=None):
         torch = torch_mod()
         self.shape, self.mapping_np, self.layer, self.dev = shape, mapping, layer, dev
+        # per-adapter factors on the scale (float32 values, also given to the oracle)
+        self.lora_scales_np = None if lora_scales is None else np.asarray(lora_scales, np.float32)
+        self.lora_scales = (None if lora_scales is None else
+                            torch_mod().from_numpy(self.lora_scales_np.copy()).to(dev))
         T, L = shape.max_num_tokens, shape.max_loras
         self.mapping = torch.from_numpy(mapping).to(dev)
         self.n = torch.tensor([shape.num_tokens], dtype=torch.int32, device=dev)
@@ -104,7 +109,7 @@ class DeviceCase:
 
     def shrink(self, stream=None):
         binding.lora_shrink(self.x, self.a, self.shape.scale, self.u.view, self.sorted.view,
-                            self.starts.view, self.ws.view, stream)
+                            self.starts.view, self.ws.view, stream, self.lora_scales)
 
     def expand(self, stream=None, u=None):
         binding.lora_expand(self.u.view if u is None else u, self.b, self.y_view,
@@ -113,7 +118,7 @@ class DeviceCase:
     def shrink_expand(self, stream=None):
         binding.lora_shrink_expand(self.x, self.a, self.b, self.shape.scale, self.u.view,
                                    self.y_view, self.sorted.view, self.starts.view, self.ws.view,
-                                   stream)
+                                   stream, self.lora_scales)
 
     def run(self, fused: bool = False):
         self.prepare()
@@ -170,7 +175,9 @@ def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None,
     m_sel = np.full(T, -1, np.int32)
     m_sel[rows] = case.mapping_np[rows]
     u_ref = oracle.shrink(lay.x, lay.lora_a, sh.scale, m_sel, n, L,
-                          u_init=np.zeros((sh.num_slices, T, sh.rank)))
+                          u_init=np.zeros((sh.num_slices, T, sh.rank)),
+                          lora_scales=None if case.lora_scales_np is None
+                          else case.lora_scales_np.astype(np.float64))
     ok_u, r_u = within_tol(u_gpu[:, rows].astype(np.float64), u_ref[:, rows])
     assert ok_u, f"u differs from the oracle (worst err/bound {r_u:.3f})"
 

@@ -115,7 +115,7 @@ def test_shrink_validation(lib):
 
     def call(**kw):
         d = dict(args, **kw)
-        return f(d["x"], d["stride"], d["hidden"], d["a"], d["s"], d["r"], d["scale"], d["u"],
+        return f(d["x"], d["stride"], d["hidden"], d["a"], d["s"], d["r"], d["scale"], None, d["u"],
                  d["sorted"], d["starts"], d["T"], d["L"], d["ws"], d["wsb"], None)
 
     assert call(x=None) == -1
@@ -178,7 +178,7 @@ def test_split_halves_validation(lib):
     fe = lib.lora_expand_partials
 
     def expand(hidden=512, r=8, u=P16, y=P16, T=64, wsb=big):
-        return fe(hidden, ctypes.addressof(b), ctypes.addressof(w), 1, r, 1.0, u, y, 512, P16,
+        return fe(hidden, ctypes.addressof(b), ctypes.addressof(w), 1, r, 1.0, None, u, y, 512, P16,
                   P16, T, 4, P16, wsb, None)
 
     assert expand(u=None) == -1

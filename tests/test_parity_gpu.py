@@ -500,3 +500,44 @@ def test_split_k_halves_equal_the_one_call(name, spec, dev):
     assert b.guards_intact()
     assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
     assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
+
+
+# ------------------------------------------------------------ per-adapter scales
+
+def _scaled_case(spec, dev, split_workspace=False, seed=31):
+    T, n, H, widths, L, R = spec
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, scale=0.5, neg_prob=0.15)
+    rng = np.random.default_rng(seed)
+    factors = rng.uniform(-2.0, 2.0, L).astype(np.float32)
+    factors[0] = 0.0  # one adapter switched off
+    return DeviceCase(shape, W.make_mapping(shape, rng), W.make_layer(shape, rng), dev,
+                      split_workspace=split_workspace, lora_scales=factors)
+
+
+SCALED_SHAPES = [
+    ("two_calls_cluster", (300, 280, 1032, (520, 264), 6, 16), False, False),
+    ("one_call_fused", (64, 64, 512, (512,), 4, 8), False, True),
+    ("one_call_split_k", (256, 240, 8200, (1024, 1024, 1024), 4, 8), True, True),
+    ("one_call_cluster_large", (2048, 2000, 1024, (2048,), 8, 64), False, True),
+]
+
+
+@pytest.mark.parametrize("name,spec,split_ws,one_call", SCALED_SHAPES)
+def test_per_adapter_scales_match_the_oracle(name, spec, split_ws, one_call, dev):
+    case = _scaled_case(spec, dev, split_workspace=split_ws)
+    check_case(case, fused=one_call, sample_rows=300)
+    if split_ws:
+        assert torch.any(case.ws.view[case.ws_base:] != 0)
+
+
+def test_per_adapter_scales_of_one_equal_no_scales(dev):
+    spec = (256, 240, 1024, (512, 512, 512), 4, 8)
+    a = _scaled_case(spec, dev)
+    b = _scaled_case(spec, dev)
+    a.lora_scales.fill_(1.0)
+    b.lora_scales = None
+    a.run()
+    b.run()
+    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
+    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))

@@ -94,7 +94,7 @@ def test_noalloc_refuses_sizes_beyond_the_static_array():
     arr = (ctypes.c_void_p * 1)(P)
     w = (ctypes.c_int64 * 1)(64)
     rc = lib.lora_apply_noalloc(P, P, big_t, big_l, P, 64, 64, ctypes.addressof(arr),
-                                ctypes.addressof(arr), ctypes.addressof(w), 1, 8, 1.0, P, P, 64,
-                                P, P, P, None, None)
+                                ctypes.addressof(arr), ctypes.addressof(w), 1, 8, 1.0, None, P,
+                                P, 64, P, P, P, None, None)
     assert rc == -4   # LORA_ERR_WORKSPACE
     assert binding.lora_workspace_size(8192, 128) <= binding.LORA_NOALLOC_SCRATCH_BYTES
