@@ -19,6 +19,7 @@ LORA_OK = 0
 LORA_STATUS_BAD_LORA_ID = 0x1
 LORA_STATUS_BAD_NUM_TOKENS = 0x2
 LORA_STATUS_TIMEOUT = 0x4
+LORA_STATUS_BAD_WEIGHT = 0x8
 LORA_MAX_SLICES = 3
 LORA_MAX_LORAS = 1024
 LORA_MAX_NUM_TOKENS = 1 << 22
@@ -28,7 +29,8 @@ LORA_NOALLOC_SCRATCH_BYTES = 384 * 1024
 EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora_expand",
             "lora_read_status", "lora_error_string", "lora_apply_noalloc",
             "lora_shrink_expand", "lora_shrink_expand_kernels",
-            "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials")
+            "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials",
+            "lora_shrink_paged", "lora_expand_paged", "lora_shrink_expand_paged")
 
 _lib = None
 
@@ -76,6 +78,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_expand_partials.restype = i32
     lib.lora_expand_partials.argtypes = [i64, p, p, i32, i32, ctypes.c_float, p, p, p, i64, p,
                                          p, i64, i64, p, sz, p]
+    lib.lora_shrink_paged.restype = i32
+    lib.lora_shrink_paged.argtypes = [p, i64, i64, p, i32, i32, ctypes.c_float, p, p, p, p, i64,
+                                      i64, p, sz, p]
+    lib.lora_expand_paged.restype = i32
+    lib.lora_expand_paged.argtypes = [p, p, p, i32, i32, p, i64, p, p, i64, i64, p, sz, p]
+    lib.lora_shrink_expand_paged.restype = i32
+    lib.lora_shrink_expand_paged.argtypes = [p, i64, i64, p, p, p, i32, i32, ctypes.c_float, p,
+                                             p, p, i64, p, p, i64, i64, p, sz, p]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, p, i64, p, p, p, p, p]
@@ -216,6 +226,68 @@ def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_i
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream_ptr(stream, y.device))
     _check("lora_expand_partials", rc)
+
+
+def _table_array(tables, name):
+    """Host array of the slices' device tables (int64 CUDA tensors of max_loras
+    weight addresses; 0 = an all-zero adapter)."""
+    import torch
+    for i, t in enumerate(tables):
+        if t.dtype != torch.int64 or t.dim() != 1 or not t.is_contiguous():
+            raise ValueError(f"{name}[{i}] must be a contiguous int64 CUDA tensor of max_loras entries")
+    return _ptr_array(tables, name)
+
+
+def lora_shrink_paged(x, a_tables, rank: int, scale: float, u, sorted_token_ids,
+                      lora_token_start_loc, workspace, stream=None, lora_scales=None):
+    """lora_shrink with paged adapter weights: a_tables[s][l] = address of A_s[l] ([rank][hidden])."""
+    a_tables = list(a_tables)
+    arr = _table_array(a_tables, "a_tables")
+    num_loras, hidden = a_tables[0].numel(), x.shape[1]
+    rc = load().lora_shrink_paged(
+        _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(a_tables), int(rank),
+        float(scale), _scales(lora_scales, num_loras), _dev(u, "u"),
+        _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, x.device))
+    _check("lora_shrink_paged", rc)
+
+
+def lora_expand_paged(u, b_tables, slice_widths, y, sorted_token_ids, lora_token_start_loc,
+                      workspace, stream=None):
+    """lora_expand with paged adapter weights: b_tables[s][l] = address of B_s[l] ([rank][N_s])."""
+    b_tables = list(b_tables)
+    arr = _table_array(b_tables, "b_tables")
+    widths = (ctypes.c_int64 * len(b_tables))(*[int(w) for w in slice_widths])
+    num_loras, rank = b_tables[0].numel(), u.shape[2]
+    rc = load().lora_expand_paged(
+        _dev(u, "u"), ctypes.addressof(arr), ctypes.addressof(widths), len(b_tables), rank,
+        _dev(y, "y"), y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), y.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, y.device))
+    _check("lora_expand_paged", rc)
+
+
+def lora_shrink_expand_paged(x, a_tables, b_tables, slice_widths, scale: float, u, y,
+                             sorted_token_ids, lora_token_start_loc, workspace, stream=None,
+                             lora_scales=None):
+    """lora_shrink_expand with paged adapter weights."""
+    a_tables, b_tables = list(a_tables), list(b_tables)
+    arr_a = _table_array(a_tables, "a_tables")
+    arr_b = _table_array(b_tables, "b_tables")
+    widths = (ctypes.c_int64 * len(b_tables))(*[int(w) for w in slice_widths])
+    num_loras, hidden, rank = a_tables[0].numel(), x.shape[1], u.shape[2]
+    rc = load().lora_shrink_expand_paged(
+        _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr_a), ctypes.addressof(arr_b),
+        ctypes.addressof(widths), len(a_tables), rank, float(scale),
+        _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"), y.stride(0),
+        _dev(sorted_token_ids, "sorted_token_ids"),
+        _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream_ptr(stream, x.device))
+    _check("lora_shrink_expand_paged", rc)
 
 
 def lora_shrink_expand_kernels(max_num_tokens: int, max_loras: int, hidden: int, slice_widths,

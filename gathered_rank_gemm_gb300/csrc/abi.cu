@@ -23,17 +23,21 @@ constexpr int64_t kMaxHidden = 1 << 20;
 constexpr int64_t kMaxWidth = 1 << 20;
 
 // Argument checks of lora_shrink; fills the launcher's arguments.
+// Weights come either stacked (lora_a) or paged (a_tables: per slice a device
+// table of max_loras addresses); exactly one of the two is given.
 int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
-                const uint16_t* const* lora_a, int num_slices, int rank, float scale,
-                const float* lora_scales, float* u,
+                const uint16_t* const* lora_a, const uint64_t* const* a_tables, int num_slices,
+                int rank, float scale, const float* lora_scales, float* u,
                 const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, grg::ShrinkArgs* out, bool need_u = true) {
-  if (!x || !lora_a || (need_u && !u) || !sorted_token_ids || !lora_token_start_loc || !workspace)
+  const bool paged = a_tables != nullptr;
+  if (!x || (!lora_a && !paged) || (need_u && !u) || !sorted_token_ids ||
+      !lora_token_start_loc || !workspace)
     return LORA_ERR_NULL;
   if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
   for (int s = 0; s < num_slices; ++s)
-    if (!lora_a[s]) return LORA_ERR_NULL;
+    if (paged ? !a_tables[s] : !lora_a[s]) return LORA_ERR_NULL;
   if (!sizes_ok(max_num_tokens, max_loras) || !rank_ok(rank) || hidden < 8 ||
       hidden > kMaxHidden || (hidden % 8) != 0 || x_row_stride < hidden)
     return LORA_ERR_SHAPE;
@@ -41,14 +45,18 @@ int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
       !aligned16(workspace))
     return LORA_ERR_ALIGN;
   for (int s = 0; s < num_slices; ++s)
-    if (!aligned16(lora_a[s])) return LORA_ERR_ALIGN;
+    if (paged ? (reinterpret_cast<uintptr_t>(a_tables[s]) % 8) != 0 : !aligned16(lora_a[s]))
+      return LORA_ERR_ALIGN;
   if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
     return LORA_ERR_WORKSPACE;
   grg::ShrinkArgs& a = *out;
   a.x = x;
   a.x_row_stride = x_row_stride;
   a.hidden = static_cast<int>(hidden);
-  for (int s = 0; s < 3; ++s) a.lora_a[s] = s < num_slices ? lora_a[s] : lora_a[0];
+  for (int s = 0; s < 3; ++s) {
+    a.lora_a[s] = paged ? nullptr : (s < num_slices ? lora_a[s] : lora_a[0]);
+    a.a_tables[s] = paged ? (s < num_slices ? a_tables[s] : a_tables[0]) : nullptr;
+  }
   a.num_slices = num_slices;
   a.rank = rank;
   a.scale = scale;
@@ -63,18 +71,19 @@ int shrink_args(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
 }
 
 // Argument checks of lora_expand; fills the launcher's arguments.
-int expand_args(const float* u, const uint16_t* const* lora_b, const int64_t* slice_width,
-                int num_slices, int rank, uint16_t* y, int64_t y_row_stride,
-                const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
-                int64_t max_num_tokens, int64_t max_loras, const void* workspace,
-                size_t workspace_bytes, grg::ExpandArgs* out) {
-  if (!u || !lora_b || !slice_width || !y || !sorted_token_ids || !lora_token_start_loc ||
-      !workspace)
+int expand_args(const float* u, const uint16_t* const* lora_b, const uint64_t* const* b_tables,
+                const int64_t* slice_width, int num_slices, int rank, uint16_t* y,
+                int64_t y_row_stride, const int32_t* sorted_token_ids,
+                const int32_t* lora_token_start_loc, int64_t max_num_tokens, int64_t max_loras,
+                const void* workspace, size_t workspace_bytes, grg::ExpandArgs* out) {
+  const bool paged = b_tables != nullptr;
+  if (!u || (!lora_b && !paged) || !slice_width || !y || !sorted_token_ids ||
+      !lora_token_start_loc || !workspace)
     return LORA_ERR_NULL;
   if (num_slices < 1 || num_slices > LORA_MAX_SLICES) return LORA_ERR_SHAPE;
   int64_t total = 0;
   for (int s = 0; s < num_slices; ++s) {
-    if (!lora_b[s]) return LORA_ERR_NULL;
+    if (paged ? !b_tables[s] : !lora_b[s]) return LORA_ERR_NULL;
     if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0)
       return LORA_ERR_SHAPE;
     total += slice_width[s];
@@ -84,13 +93,15 @@ int expand_args(const float* u, const uint16_t* const* lora_b, const int64_t* sl
   if (!aligned16(u) || !aligned16(y) || (y_row_stride % 8) != 0 || !aligned16(workspace))
     return LORA_ERR_ALIGN;
   for (int s = 0; s < num_slices; ++s)
-    if (!aligned16(lora_b[s])) return LORA_ERR_ALIGN;
+    if (paged ? (reinterpret_cast<uintptr_t>(b_tables[s]) % 8) != 0 : !aligned16(lora_b[s]))
+      return LORA_ERR_ALIGN;
   if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
     return LORA_ERR_WORKSPACE;
   grg::ExpandArgs& a = *out;
   a.u = u;
   for (int s = 0; s < 3; ++s) {
-    a.lora_b[s] = s < num_slices ? lora_b[s] : lora_b[0];
+    a.lora_b[s] = paged ? nullptr : (s < num_slices ? lora_b[s] : lora_b[0]);
+    a.b_tables[s] = paged ? (s < num_slices ? b_tables[s] : b_tables[0]) : nullptr;
     a.slice_width[s] = s < num_slices ? static_cast<int>(slice_width[s]) : 0;
   }
   a.num_slices = num_slices;
@@ -163,9 +174,9 @@ int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden
                          int64_t max_num_tokens, int64_t max_loras, void* workspace,
                          size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs sa;
-  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, 1.0f, nullptr,
-                             nullptr, sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
-                             workspace, workspace_bytes, &sa, false);
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, 1.0f,
+                             nullptr, nullptr, sorted_token_ids, lora_token_start_loc,
+                             max_num_tokens, max_loras, workspace, workspace_bytes, &sa, false);
   if (rc != LORA_OK) return rc;
   if (!split_shape(max_num_tokens, rank)) return LORA_ERR_SHAPE;
   const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
@@ -184,7 +195,7 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
                     int64_t max_loras, const void* workspace, size_t workspace_bytes,
                     void* stream, bool y_early) {
   grg::ExpandArgs ea;
-  const int rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride,
+  const int rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
                              workspace, workspace_bytes, &ea);
   if (rc != LORA_OK) return rc;
@@ -244,7 +255,7 @@ int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs a;
-  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale,
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, scale,
                              lora_scales, u, sorted_token_ids, lora_token_start_loc,
                              max_num_tokens, max_loras, workspace, workspace_bytes, &a);
   if (rc != LORA_OK) return rc;
@@ -257,12 +268,76 @@ int lora_expand(const float* u, const uint16_t* const* lora_b, const int64_t* sl
                 int64_t max_num_tokens, int64_t max_loras, const void* workspace,
                 size_t workspace_bytes, void* stream) {
   grg::ExpandArgs a;
-  const int rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride,
+  const int rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
                              workspace, workspace_bytes, &a);
   if (rc != LORA_OK) return rc;
   return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
 }
+
+int lora_shrink_paged(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                      const uint64_t* const* lora_a_tables, int num_slices, int rank,
+                      float scale, const float* lora_scales, float* u,
+                      const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                      int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (!lora_a_tables) return LORA_ERR_NULL;
+  grg::ShrinkArgs a;
+  const int rc = shrink_args(x, x_row_stride, hidden, nullptr, lora_a_tables, num_slices, rank,
+                             scale, lora_scales, u, sorted_token_ids, lora_token_start_loc,
+                             max_num_tokens, max_loras, workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
+  return grg::launch_shrink(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_expand_paged(const float* u, const uint64_t* const* lora_b_tables,
+                      const int64_t* slice_width, int num_slices, int rank, uint16_t* y,
+                      int64_t y_row_stride, const int32_t* sorted_token_ids,
+                      const int32_t* lora_token_start_loc, int64_t max_num_tokens,
+                      int64_t max_loras, const void* workspace, size_t workspace_bytes,
+                      void* stream) {
+  if (!lora_b_tables) return LORA_ERR_NULL;
+  grg::ExpandArgs a;
+  const int rc = expand_args(u, nullptr, lora_b_tables, slice_width, num_slices, rank, y,
+                             y_row_stride, sorted_token_ids, lora_token_start_loc,
+                             max_num_tokens, max_loras, workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
+  return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+// One layer in one call, for validated arguments (stacked or paged weights):
+// the fused kernel when the batch fits it, else the split-K pair when the
+// workspace has room for the partial tiles, else the two kernels.
+int shrink_expand(grg::ShrinkArgs& sa, grg::ExpandArgs& ea, int64_t hidden,
+                  const void* workspace, size_t workspace_bytes, cudaStream_t s) {
+  int rc = grg::launch_fused(sa, ea, s);
+  if (rc < 0) return rc;
+  if (rc == 1) return LORA_OK;
+  // the expand directly follows the shrink, which never writes y
+  ea.y_early = true;
+  // split-K: with the larger workspace, the shrink's CTAs write partial tiles
+  // and the expand sums them in rank order (no cluster-wide steps)
+  const int64_t T = sa.max_num_tokens, L = sa.num_loras;
+  const size_t base = grg::workspace_bytes_needed(T, L);
+  if (split_shape(T, sa.rank) &&
+      workspace_bytes >= base + split_scratch_bytes(T, L, sa.num_slices, sa.rank) &&
+      grg::shrink_split(sa, true) >= 2) {
+    char* ws = static_cast<char*>(const_cast<void*>(workspace));
+    sa.partials = reinterpret_cast<float*>(ws + base);
+    rc = grg::launch_shrink(sa, s);
+    if (rc != LORA_OK) return rc;
+    ea.partials = sa.partials;
+    ea.split = split_of(T, L, hidden, sa.num_slices, sa.rank);
+    ea.scale = sa.scale;
+    ea.lora_scales = sa.lora_scales;
+    return grg::launch_expand(ea, s);
+  }
+  rc = grg::launch_shrink(sa, s);
+  if (rc != LORA_OK) return rc;
+  return grg::launch_expand(ea, s);
+}
+}  // namespace
 
 int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t* const* lora_a, const uint16_t* const* lora_b,
@@ -273,37 +348,39 @@ int lora_shrink_expand(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
                        size_t workspace_bytes, void* stream) {
   grg::ShrinkArgs sa;
   grg::ExpandArgs ea;
-  int rc = shrink_args(x, x_row_stride, hidden, lora_a, num_slices, rank, scale, lora_scales, u,
-                       sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
-                       workspace, workspace_bytes, &sa);
+  int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, scale,
+                       lora_scales, u, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                       max_loras, workspace, workspace_bytes, &sa);
   if (rc != LORA_OK) return rc;
-  rc = expand_args(u, lora_b, slice_width, num_slices, rank, y, y_row_stride, sorted_token_ids,
-                   lora_token_start_loc, max_num_tokens, max_loras, workspace, workspace_bytes,
-                   &ea);
+  rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
+                   sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                   workspace_bytes, &ea);
   if (rc != LORA_OK) return rc;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = grg::launch_fused(sa, ea, s);
-  if (rc < 0) return rc;
-  if (rc == 1) return LORA_OK;
-  // split-K: with the larger workspace, the shrink's CTAs write partial tiles
-  // and the expand sums them in rank order (no cluster-wide steps)
-  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
-  if (split_shape(max_num_tokens, rank) &&
-      workspace_bytes >= base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank) &&
-      grg::shrink_split(sa, true) >= 2) {
-    rc = lora_shrink_partials(x, x_row_stride, hidden, lora_a, num_slices, rank,
-                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
-                              const_cast<void*>(workspace), workspace_bytes, stream);
-    if (rc != LORA_OK) return rc;
-    // the expand directly follows the shrink, which never writes y
-    return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, lora_scales, u,
-                           y, y_row_stride, sorted_token_ids, lora_token_start_loc,
-                           max_num_tokens, max_loras, workspace, workspace_bytes, stream, true);
-  }
-  rc = grg::launch_shrink(sa, s);
+  return shrink_expand(sa, ea, hidden, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink_expand_paged(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                             const uint64_t* const* lora_a_tables,
+                             const uint64_t* const* lora_b_tables, const int64_t* slice_width,
+                             int num_slices, int rank, float scale, const float* lora_scales,
+                             float* u, uint16_t* y, int64_t y_row_stride,
+                             const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                             int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  if (!lora_a_tables || !lora_b_tables) return LORA_ERR_NULL;
+  grg::ShrinkArgs sa;
+  grg::ExpandArgs ea;
+  int rc = shrink_args(x, x_row_stride, hidden, nullptr, lora_a_tables, num_slices, rank, scale,
+                       lora_scales, u, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                       max_loras, workspace, workspace_bytes, &sa);
   if (rc != LORA_OK) return rc;
-  ea.y_early = true;  // the expand directly follows the shrink, which never writes y
-  return grg::launch_expand(ea, s);
+  rc = expand_args(u, nullptr, lora_b_tables, slice_width, num_slices, rank, y, y_row_stride,
+                   sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                   workspace_bytes, &ea);
+  if (rc != LORA_OK) return rc;
+  return shrink_expand(sa, ea, hidden, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
 }
 
 int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,

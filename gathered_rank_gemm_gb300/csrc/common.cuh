@@ -195,6 +195,7 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
 // many nanoseconds of %globaltimer gives up and reports LORA_STATUS_TIMEOUT.
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 constexpr uint32_t kStatusTimeout = 0x4u;
+constexpr uint32_t kStatusBadWeight = 0x8u;  // a paged weight address was not 16-byte aligned
 
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;

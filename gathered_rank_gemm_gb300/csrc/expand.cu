@@ -24,6 +24,8 @@
 // 16 significant bits of the fp32 u reach the product.  The sum is added to
 // the staged y in fp32, rounded once to bf16, written back into the stage and
 // stored with coalesced 16-byte stores.
+#include <cstring>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -42,6 +44,10 @@ struct ExpandParams {
   float scale;
   const float* lora_scales;  // partial mode: per-adapter factors on scale, or null
   int y_early;  // y may be read before the dependency wait (the one-call path)
+  // paged weights: per slice a device table of max_loras addresses of B_s[l]
+  // ([R][N_s] bf16), loaded by cp.async; null for stacked weights (tensor maps)
+  const uint64_t* b_tab[3];
+  int paged;
   int max_num_tokens;
   int w0, w1, w2;        // slice widths
   int off0, off1, off2;  // slice column offsets in y
@@ -80,7 +86,7 @@ constexpr int expand_stages() {
   return RANK <= 32 ? 2 : 1;
 }
 
-template <int BM, int RANK, int NS, bool PARTIAL>
+template <int BM, int RANK, int NS, bool PARTIAL, bool PAGED>
 __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     lora_expand_kernel(const __grid_constant__ ExpandParams p) {
   using Lay = ExpandLayout<BM, RANK, NS, PARTIAL>;
@@ -111,7 +117,8 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   if (tid == 0) {
     for (int s = 0; s < NS + RS; ++s) mbar_init(stage_bar + 8 * s, 1);
     fence_mbar_init();
-    for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
+    if constexpr (!PAGED)
+      for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
   }
   __syncthreads();
 
@@ -159,6 +166,10 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     const TileView tv = TileView::of(rec_of(k), BM, p.num_loras);
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
     const uint32_t bar = stage_bar + 8 * (k % NS);
+    if constexpr (PAGED) {  // the rows come with the item's cp.async group (issue_y)
+      mbar_arrive(bar);
+      return;
+    }
     const int boxes = min(4, (it.width - it.c0 + 63) / 64);
     mbar_arrive_expect_tx(bar, static_cast<uint32_t>(boxes * RANK * 128));
     for (int b = 0; b < boxes; ++b)
@@ -180,6 +191,23 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
       const bool ok = t >= 0 && col < it.width;
       cp_async_16(st + Lay::kY + row * kYPitch + ych * 16,
                   ok ? p.y + static_cast<long long>(t) * p.y_stride + it.off + col : p.y, ok);
+    }
+    if constexpr (PAGED) {
+      // paged weights: B_s[lora] rows of the item's 256 columns, into the
+      // layout of the four TMA boxes (a null or misaligned table entry reads
+      // as an all-zero adapter and sets LORA_STATUS_BAD_WEIGHT)
+      const uint64_t a = p.b_tab[it.s][tv.lora];
+      const __nv_bfloat16* base =
+          (a & 15u) == 0 ? reinterpret_cast<const __nv_bfloat16*>(a) : nullptr;
+      if (a != 0 && base == nullptr && tid == 0) atomicOr(p.status, kStatusBadWeight);
+      for (int c = tid; c < 4 * RANK * 8; c += kExpandThreads) {
+        const int box = c / (RANK * 8), rem = c - box * RANK * 8;
+        const int r = rem >> 3, ch = rem & 7;
+        const int bcol = it.c0 + box * 64 + ch * 8;
+        const bool ok = base != nullptr && bcol < it.width;
+        cp_async_16(st + Lay::kB + box * RANK * 128 + swz128(r, ch),
+                    ok ? base + static_cast<long long>(r) * it.width + bcol : p.y, ok);
+      }
     }
   };
   // rows of u (or of the split's partial tiles) of item k -> stage, closing the group
@@ -406,7 +434,9 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
 template <int BM, int RANK, bool PARTIAL>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
   constexpr int NS = expand_stages<RANK>();
-  const void* fn = reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL>);
+  const void* fn =
+      prm.paged ? reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, true>)
+                : reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, false>);
   const size_t smem = ExpandLayout<BM, RANK, NS, PARTIAL>::kSmem;
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
@@ -424,6 +454,9 @@ static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long ma
 template <int BM>
 static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   ExpandParams p;
+  memset(&p, 0, sizeof(p));
+  p.paged = a.b_tables[0] != nullptr;
+  for (int s = 0; s < 3; ++s) p.b_tab[s] = s < a.num_slices ? a.b_tables[s] : a.b_tables[0];
   p.u = a.u;
   p.partials = a.partials;
   p.split = a.split;
@@ -441,8 +474,8 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
       acc_off += w[s];
       cbs[s] = (w[s] + kEN - 1) / kEN;
       cb_total += cbs[s];
-      if (make_weight_tmap(&p.tmap[s], a.lora_b[s], w[s],
-                           static_cast<long long>(a.num_loras) * a.rank, a.rank) != 0)
+      if (!p.paged && make_weight_tmap(&p.tmap[s], a.lora_b[s], w[s],
+                                       static_cast<long long>(a.num_loras) * a.rank, a.rank) != 0)
         return -6;
     } else {
       p.tmap[s] = p.tmap[0];

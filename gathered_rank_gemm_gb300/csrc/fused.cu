@@ -477,6 +477,7 @@ int fused_fits(int max_num_tokens, int num_loras, int hidden, const int* widths,
 // Returns 1 when the fused kernel was launched, 0 when the shape does not fit
 // it (the caller then runs the separate kernels), or a negative error code.
 int launch_fused(const ShrinkArgs& sa, const ExpandArgs& ea, cudaStream_t stream) {
+  if (sa.a_tables[0] != nullptr || ea.b_tables[0] != nullptr) return 0;  // paged: tensor maps only
   const int S = sa.num_slices, R = sa.rank, SR = S * R;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;

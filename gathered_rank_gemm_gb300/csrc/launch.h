@@ -57,6 +57,9 @@ struct ShrinkArgs {
   // split-K mode: each CTA's partial tile goes to partials[tile][split][16][S*R]
   // (no cluster reduction, u is not written); null for the normal mode
   float* partials = nullptr;
+  // paged weights: per slice a device table of max_loras addresses of A_s[l]
+  // ([rank][hidden] bf16); all null for stacked weights (lora_a)
+  const uint64_t* a_tables[3] = {nullptr, nullptr, nullptr};
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
 // CTAs sharing one tile's hidden dimension for this shape on the current
@@ -86,6 +89,9 @@ struct ExpandArgs {
   int split = 0;
   float scale = 1.0f;
   const float* lora_scales = nullptr;
+  // paged weights: per slice a device table of max_loras addresses of B_s[l]
+  // ([rank][slice_width] bf16); all null for stacked weights (lora_b)
+  const uint64_t* b_tables[3] = {nullptr, nullptr, nullptr};
   // y may be read before the dependency wait: only when the expand directly
   // follows this library's shrink on the stream (the one-call path)
   bool y_early = false;

@@ -24,6 +24,8 @@
 // the first x rows are prefetched into L2 there.  The C partial tiles are
 // summed in rank order through distributed shared memory (no atomics, no
 // global scratch), scaled once and stored to u.
+#include <cstring>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -59,9 +61,13 @@ struct ShrinkParams {
   int bar_offset;  // full[NST] then empty[NST]
   float* partials;  // split-K mode: [tile][split][BM][S*R] partial tiles; null otherwise
   int split;        // split-K mode: CTAs per tile (consecutive blocks, no cluster)
+  // paged weights: per slice a device table of max_loras addresses of
+  // A_s[l] ([R][hidden] bf16); null for stacked weights (tensor maps)
+  const uint64_t* a_tab[3];
+  int paged;
 };
 
-template <int BM, int NTW, int NST>
+template <int BM, int NTW, int NST, bool PAGED>
 __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW > 8) ? 3 : 4)
     lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -107,7 +113,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       mbar_init(empty_bar + 8 * s, kConsumerWarps);  // one arrival per consumer warp
     }
     fence_mbar_init();
-    for (int s = 0; s < p.num_slices; ++s) prefetch_tmap(&p.tmap[s]);
+    if constexpr (!PAGED)
+      for (int s = 0; s < p.num_slices; ++s) prefetch_tmap(&p.tmap[s]);
   }
   __syncthreads();
 
@@ -132,6 +139,30 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       cp_async_16(sbase + st * p.stage_bytes + swz128(row, ch),
                   ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
     };
+    // paged weights: this adapter's A_s (a null or misaligned table entry
+    // reads as an all-zero adapter and sets LORA_STATUS_BAD_WEIGHT)
+    const __nv_bfloat16* abase[3] = {nullptr, nullptr, nullptr};
+    if constexpr (PAGED) {
+      for (int s = 0; s < p.num_slices; ++s) {
+        const uint64_t a = p.a_tab[s][lora];
+        if ((a & 15u) == 0) abase[s] = reinterpret_cast<const __nv_bfloat16*>(a);
+        else if (tid == 0) atomicOr(p.status, kStatusBadWeight);
+      }
+    }
+    // paged weights: the adapter rows of k-block kb -> stage st by cp.async,
+    // into the layout the TMA boxes would give (chunks first, first + step, ...)
+    auto a_chunks = [&](int st, int kb, int first, int step) {
+      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
+      for (int c = first; c < SR * 8; c += step) {
+        const int row = c >> 3, ch = c & 7;
+        const int s = row >> p.rank_shift, r = row - (s << p.rank_shift);
+        const int kcol = kb * kBK + ch * 8;
+        const __nv_bfloat16* base = abase[s];
+        const bool ok = base != nullptr && kcol < p.hidden;
+        cp_async_16(sa + swz128(row, ch), ok ? base + static_cast<long long>(r) * p.hidden + kcol : p.x,
+                    ok);
+      }
+    };
     // the adapter blocks of k-block kb -> stage st, by TMA (one thread)
     auto issue_a = [&](int st, int kb) {
       const uint32_t bar = full_bar + 8 * st;
@@ -150,8 +181,17 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     if (producer && lane == 0) {
       for (int i = 0; i < npro; ++i) {
         wait_empty(kb_global + i);
-        issue_a((kb_global + i) % NST, kb_of(i));
+        if constexpr (PAGED)
+          mbar_arrive(full_bar + 8 * ((kb_global + i) % NST));  // no transaction bytes
+        else
+          issue_a((kb_global + i) % NST, kb_of(i));
       }
+    }
+    if constexpr (PAGED) {
+      // every stage is free here (the previous tile ended with a block-wide
+      // barrier); each thread's adapter chunks complete with its x chunks
+      for (int i = 0; i < npro; ++i)
+        a_chunks((kb_global + i) % NST, kb_of(i), tid, kShrinkThreads);
     }
     if (!waited) {
       if (producer && npro > 0) {
@@ -196,9 +236,13 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         wait_empty(g);  // every lane: the consumers released the stage
         __syncwarp();
         if (lane == 0) {
-          issue_a(st, kb_of(i));
+          if constexpr (PAGED)
+            mbar_arrive(full_bar + 8 * st);
+          else
+            issue_a(st, kb_of(i));
           mbar_arrive_count(full_bar + 8 * st, kShrinkThreads - 32);
         }
+        if constexpr (PAGED) a_chunks(st, kb_of(i), lane, 32);
         const uint32_t sx = sbase + st * p.stage_bytes;
         const int kb = kb_of(i);
         const bool kin = kb * kBK + xch * 8 < p.hidden;
@@ -354,7 +398,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
 template <int BM, int NTW, int NST>
 static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStream_t stream,
                       long long max_tiles) {
-  const void* fn = reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST>);
+  const void* fn = prm.paged ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, true>)
+                             : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false>);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -417,7 +462,11 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
     nst = ((SR >= 128 && kb_per > 32) || 4 * stage > 96 * 1024) ? 2 : 4;
 
   ShrinkParams p;
+  memset(&p, 0, sizeof(p));
+  p.paged = a.a_tables[0] != nullptr;
   for (int s = 0; s < 3; ++s) {
+    p.a_tab[s] = s < a.num_slices ? a.a_tables[s] : a.a_tables[0];
+    if (p.paged) continue;
     if (s < a.num_slices) {
       if (make_weight_tmap(&p.tmap[s], a.lora_a[s], a.hidden,
                            static_cast<long long>(a.num_loras) * a.rank, a.rank) != 0)

@@ -67,6 +67,7 @@ extern "C" {
 #define LORA_STATUS_BAD_LORA_ID 0x1u     /* some m[t], t < n, was outside [-1, L) */
 #define LORA_STATUS_BAD_NUM_TOKENS 0x2u  /* n was outside [0, max_num_tokens]; clamped */
 #define LORA_STATUS_TIMEOUT 0x4u         /* a kernel's bounded wait for its own copies gave up */
+#define LORA_STATUS_BAD_WEIGHT 0x8u      /* a paged weight address was not 16-byte aligned */
 
 #define LORA_MAX_SLICES 3
 #define LORA_MAX_LORAS 1024
@@ -196,6 +197,46 @@ int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
 size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_loras,
                                          int64_t hidden, const int64_t *slice_width,
                                          int num_slices, int rank);
+
+/*
+ * Paged adapter weights (the S-LoRA idea of the pages' "[Tracking] Multi-LoRA
+ * Serving" overview: adapters live in separately allocated pages rather than
+ * one stacked tensor).  Same arguments, results and rules as lora_shrink,
+ * lora_expand and lora_shrink_expand, except that each slice's weights come
+ * as a table instead of a stacked tensor:
+ *   lora_a_tables   HOST array of num_slices device pointers, each to
+ *                   uint64[max_loras]: the device address of adapter l's
+ *                   A_s[l], bf16[rank][hidden] row-major
+ *   lora_b_tables   the same for B_s[l], bf16[rank][slice_width[s]]
+ * Table pointers must be 8-byte aligned.  An entry must be 16-byte aligned
+ * or 0; 0 reads as an all-zero adapter (its tokens get u = 0, y unchanged),
+ * and a misaligned entry reads the same way and sets LORA_STATUS_BAD_WEIGHT.
+ * The tables and the weights they point to are read before the kernel's
+ * dependency wait, like stacked weights: the kernel immediately before on
+ * the stream must not write them.  The weights move by 16-byte cp.async
+ * instead of TMA tensor maps; the one-call entry point never takes the
+ * fused kernel.
+ */
+int lora_shrink_paged(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                      const uint64_t *const *lora_a_tables, int num_slices, int rank,
+                      float scale, const float *lora_scales, float *u,
+                      const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                      int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                      size_t workspace_bytes, void *stream);
+int lora_expand_paged(const float *u, const uint64_t *const *lora_b_tables,
+                      const int64_t *slice_width, int num_slices, int rank, uint16_t *y,
+                      int64_t y_row_stride, const int32_t *sorted_token_ids,
+                      const int32_t *lora_token_start_loc, int64_t max_num_tokens,
+                      int64_t max_loras, const void *workspace, size_t workspace_bytes,
+                      void *stream);
+int lora_shrink_expand_paged(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                             const uint64_t *const *lora_a_tables,
+                             const uint64_t *const *lora_b_tables, const int64_t *slice_width,
+                             int num_slices, int rank, float scale, const float *lora_scales,
+                             float *u, uint16_t *y, int64_t y_row_stride,
+                             const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                             int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                             size_t workspace_bytes, void *stream);
 
 /*
  * The two halves of lora_shrink_expand's split-K path, for callers that want

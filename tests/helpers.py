@@ -65,7 +65,7 @@ class DeviceCase:
 
     def __init__(self, shape: W.LayerShape, mapping: np.ndarray, layer: W.Layer, dev,
                  x_pad: int = 0, y_pad: int = 0, split_workspace: bool = False,
-                 lora_scales=None):
+                 lora_scales=None, paged: bool = False):
         torch = torch_mod()
         self.shape, self.mapping_np, self.layer, self.dev = shape, mapping, layer, dev
         # per-adapter factors on the scale (float32 values, also given to the oracle)
@@ -90,6 +90,22 @@ class DeviceCase:
         self.y_view = self.y.view[:, :shape.out_width]
         self.a = [bf16_dev(v, dev) for v in layer.lora_a]
         self.b = [bf16_dev(v, dev) for v in layer.lora_b]
+        # paged weights: every adapter's A_s[l] / B_s[l] in its own allocation
+        # (allocated in reverse adapter order), found through address tables
+        self.paged = paged
+        if paged:
+            torch = torch_mod()
+            L_ = shape.max_loras
+            self.a_pages = [[None] * L_ for _ in layer.lora_a]
+            self.b_pages = [[None] * L_ for _ in layer.lora_b]
+            for l in reversed(range(L_)):
+                for s_ in range(shape.num_slices):
+                    self.a_pages[s_][l] = bf16_dev(layer.lora_a[s_][l], dev)
+                    self.b_pages[s_][l] = bf16_dev(layer.lora_b[s_][l], dev)
+            self.a_tables = [torch.tensor([t.data_ptr() for t in pages], dtype=torch.int64,
+                                          device=dev) for pages in self.a_pages]
+            self.b_tables = [torch.tensor([t.data_ptr() for t in pages], dtype=torch.int64,
+                                          device=dev) for pages in self.b_pages]
         self.u = Guarded((shape.num_slices, T, shape.rank), torch.float32, dev,
                          fill_bits=U_SENTINEL_BITS)
         self.sorted = Guarded((T,), torch.int32, dev, fill_bits=0x11111111)
@@ -108,14 +124,31 @@ class DeviceCase:
                                       self.ws.view, stream)
 
     def shrink(self, stream=None):
+        if self.paged:
+            binding.lora_shrink_paged(self.x, self.a_tables, self.shape.rank, self.shape.scale,
+                                      self.u.view, self.sorted.view, self.starts.view,
+                                      self.ws.view, stream, self.lora_scales)
+            return
         binding.lora_shrink(self.x, self.a, self.shape.scale, self.u.view, self.sorted.view,
                             self.starts.view, self.ws.view, stream, self.lora_scales)
 
     def expand(self, stream=None, u=None):
+        if self.paged:
+            binding.lora_expand_paged(self.u.view if u is None else u, self.b_tables,
+                                      self.shape.slice_widths, self.y_view, self.sorted.view,
+                                      self.starts.view, self.ws.view, stream)
+            return
         binding.lora_expand(self.u.view if u is None else u, self.b, self.y_view,
                             self.sorted.view, self.starts.view, self.ws.view, stream)
 
     def shrink_expand(self, stream=None):
+        if self.paged:
+            binding.lora_shrink_expand_paged(self.x, self.a_tables, self.b_tables,
+                                             self.shape.slice_widths, self.shape.scale,
+                                             self.u.view, self.y_view, self.sorted.view,
+                                             self.starts.view, self.ws.view, stream,
+                                             self.lora_scales)
+            return
         binding.lora_shrink_expand(self.x, self.a, self.b, self.shape.scale, self.u.view,
                                    self.y_view, self.sorted.view, self.starts.view, self.ws.view,
                                    stream, self.lora_scales)

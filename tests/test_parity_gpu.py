@@ -541,3 +541,56 @@ def test_per_adapter_scales_of_one_equal_no_scales(dev):
     b.run()
     assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
     assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
+
+
+# ------------------------------------------------------------ paged adapter weights
+
+PAGED_SHAPES = [
+    # (spec, split_workspace, one_call)
+    ("decode_like_two_calls", (256, 240, 1032, (512, 264, 136), 4, 8), False, False),
+    ("decode_like_split_k", (256, 240, 8200, (1024, 1024, 1024), 4, 8), True, True),
+    ("prefill_like_cluster", (2048, 2000, 1024, (1024,), 8, 16), False, True),
+    ("rank128", (512, 500, 512, (256,), 6, 128), False, False),
+    ("tiny_one_call", (64, 64, 512, (512,), 4, 8), False, True),
+]
+
+
+def _paged_case(spec, dev, split_workspace=False, seed=41, paged=True):
+    T, n, H, widths, L, R = spec
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, neg_prob=0.15)
+    rng = np.random.default_rng(seed)
+    return DeviceCase(shape, W.make_mapping(shape, rng), W.make_layer(shape, rng), dev,
+                      split_workspace=split_workspace, paged=paged)
+
+
+@pytest.mark.parametrize("name,spec,split_ws,one_call", PAGED_SHAPES)
+def test_paged_weights_match_the_oracle(name, spec, split_ws, one_call, dev):
+    case = _paged_case(spec, dev, split_workspace=split_ws)
+    check_case(case, fused=one_call, sample_rows=300)
+    assert case.ws.view[:4].view(torch.int32).item() & binding.LORA_STATUS_BAD_WEIGHT == 0
+
+
+@pytest.mark.parametrize("name,spec,split_ws,one_call", PAGED_SHAPES[:3])
+def test_paged_weights_equal_stacked_weights_bit_for_bit(name, spec, split_ws, one_call, dev):
+    a = _paged_case(spec, dev, split_workspace=split_ws, paged=True)
+    b = _paged_case(spec, dev, split_workspace=split_ws, paged=False)
+    a.run(fused=one_call)
+    b.run(fused=one_call)
+    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
+    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
+
+
+def test_paged_zero_and_misaligned_entries_read_as_zero_adapters(dev):
+    spec = (256, 256, 1024, (512, 512), 4, 16)
+    case = _paged_case(spec, dev)
+    # adapter 1: no pages (0); adapter 2: misaligned addresses
+    for tab in case.a_tables + case.b_tables:
+        tab[1] = 0
+        tab[2] = tab[2] + 2
+    lay = case.layer
+    for s in range(case.shape.num_slices):
+        lay.lora_a[s][1:3] = 0
+        lay.lora_b[s][1:3] = 0
+    check_case(case, sample_rows=300)
+    assert case.ws.view[:4].view(torch.int32).item() & binding.LORA_STATUS_BAD_WEIGHT
