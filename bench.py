@@ -316,24 +316,48 @@ def run_ours(args, world, rank, local):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     stream = torch.cuda.Stream(dev)
-    # the larger workspace lets lora_shrink_expand take its split-K path
-    ws_bytes = binding.lora_shrink_expand_workspace_size(T, L, shape.hidden, shape.slice_widths,
-                                                         shape.rank)
+    # the larger workspace lets lora_shrink_expand take its split-K path (stacked
+    # weights only: the split-K halves have no paged form, so paged runs time
+    # the cluster-path kernels their one call runs)
+    ws_bytes = (None if args.paged else
+                binding.lora_shrink_expand_workspace_size(T, L, shape.hidden, shape.slice_widths,
+                                                          shape.rank))
     meta = binding.LoraMetadata(T, L, dev, workspace_bytes=ws_bytes)
     mapping = torch.from_numpy(wl.mapping).to(dev)
     n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
     xs = [bf16(l.x) for l in wl.layers]
     ys = [bf16(l.y) for l in wl.layers]
-    As = [[bf16(a) for a in l.lora_a] for l in wl.layers]
-    Bs = [[bf16(b) for b in l.lora_b] for l in wl.layers]
+    if args.paged:
+        # every adapter's A_s[l] / B_s[l] in its own allocation, found through
+        # one address table per layer and slice
+        pages = []
+        A_tab, B_tab = [], []
+        for l in wl.layers:
+            ta, tb = [], []
+            for s_ in range(shape.num_slices):
+                pa = [bf16(l.lora_a[s_][a]) for a in range(L)]
+                pb = [bf16(l.lora_b[s_][a]) for a in range(L)]
+                pages += pa + pb
+                ta.append(torch.tensor([t.data_ptr() for t in pa], dtype=torch.int64, device=dev))
+                tb.append(torch.tensor([t.data_ptr() for t in pb], dtype=torch.int64, device=dev))
+            A_tab.append(ta)
+            B_tab.append(tb)
+    else:
+        As = [[bf16(a) for a in l.lora_a] for l in wl.layers]
+        Bs = [[bf16(b) for b in l.lora_b] for l in wl.layers]
+    scales = None
+    if args.lora_scales:
+        scales = torch.from_numpy(np.random.default_rng(seed + 1).uniform(0.5, 1.5, L)
+                                  .astype(np.float32)).to(dev)
     us = [torch.zeros(shape.num_slices, T, shape.rank, dtype=torch.float32, device=dev)
           for _ in wl.layers]
     torch.cuda.synchronize()
 
     # per layer, one lora_shrink_expand call: one fused kernel when the batch
     # fits on chip, else the shrink and expand kernels back to back
-    per_layer_kernels = binding.lora_shrink_expand_kernels(T, L, shape.hidden,
-                                                           shape.slice_widths, shape.rank)
+    per_layer_kernels = (2 if args.paged else
+                         binding.lora_shrink_expand_kernels(T, L, shape.hidden,
+                                                            shape.slice_widths, shape.rank))
 
     # which kernels lora_shrink_expand runs here: the split-K path leaves its
     # partial tiles behind the metadata part of the (zero-initialised) workspace
@@ -344,16 +368,27 @@ def run_ours(args, world, rank, local):
             meta.prepare(mapping, n_dev, stream)
         for k in range(layers):
             if which in ("all", "one_call", "profile"):
-                meta.shrink_expand(xs[k], As[k], Bs[k], shape.scale, us[k], ys[k], stream)
+                if args.paged:
+                    meta.shrink_expand_paged(xs[k], A_tab[k], B_tab[k], shape.slice_widths,
+                                             shape.scale, us[k], ys[k], stream, scales)
+                else:
+                    meta.shrink_expand(xs[k], As[k], Bs[k], shape.scale, us[k], ys[k], stream,
+                                       scales)
             # the kernels of the one call, timed one launch at a time
             if which == "shrink":
-                if split_k:
+                if args.paged:
+                    meta.shrink_paged(xs[k], A_tab[k], shape.rank, shape.scale, us[k], stream,
+                                      scales)
+                elif split_k:
                     meta.shrink_partials(xs[k], As[k], stream)
                 else:
-                    meta.shrink(xs[k], As[k], shape.scale, us[k], stream)
+                    meta.shrink(xs[k], As[k], shape.scale, us[k], stream, scales)
             if which == "expand":
-                if split_k:
-                    meta.expand_partials(shape.hidden, Bs[k], shape.scale, us[k], ys[k], stream)
+                if args.paged:
+                    meta.expand_paged(us[k], B_tab[k], shape.slice_widths, ys[k], stream)
+                elif split_k:
+                    meta.expand_partials(shape.hidden, Bs[k], shape.scale, us[k], ys[k], stream,
+                                         scales)
                 else:
                     meta.expand(us[k], Bs[k], ys[k], stream)
 
@@ -362,7 +397,8 @@ def run_ours(args, world, rank, local):
         step()  # first call per device sets kernel attributes outside capture
     stream.synchronize()
     ws_base = binding.lora_workspace_size(T, L)
-    split_k = per_layer_kernels == 2 and bool(meta.workspace[ws_base:].any().item())
+    split_k = (per_layer_kernels == 2 and meta.workspace.numel() > ws_base and
+               bool(meta.workspace[ws_base:].any().item()))
     if args.mode == "profile":
         for _ in range(args.steps):
             with torch.cuda.stream(stream):
@@ -461,7 +497,8 @@ def run_ours(args, world, rank, local):
     else:
         # the kernel that takes the larger share of the layer's device time
         dominant = "expand" if ms_expand >= ms_shrink else "shrink"
-        kernel_name = f"lora_{dominant}_kernel" + (" (split-K)" if split_k else "")
+        kernel_name = (f"lora_{dominant}_kernel" + (" (split-K)" if split_k else "")
+                       + (" (paged weights)" if args.paged else ""))
         dom_bytes = alg[dominant]
         t_dom = ms_expand if dominant == "expand" else ms_shrink
     achieved = dom_bytes / (t_dom * 1e-3) / 1e9
@@ -483,13 +520,16 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs larger than L2: {layers} distinct layers, "
                              f"{layers * per_layer / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
                        "graph": "one CUDA graph per step: grouping, then one lora_shrink_expand call per layer",
-                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+                       "parallelism": f"replicas x{world} (independent batches, no collective)",
+                       "weights": "paged" if args.paged else "stacked",
+                       "lora_scales": bool(args.lora_scales)},
             "roofline": {"bound": "hbm", "kernel": kernel_name,
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "frac_of_nominal_8tbs": achieved / 8000.0,
                          "algorithmic_bytes_per_launch": dom_bytes,
-                         "traffic": recorded_traffic(dominant + ("-split" if split_k else ""),
+                         "traffic": recorded_traffic(dominant + ("-split" if split_k else "")
+                                                     + ("-paged" if args.paged else ""),
                                                      shape.name)},
             "kernels_per_layer": per_layer_kernels,
             "one_call_path": "fused" if per_layer_kernels == 1 else ("split-K" if split_k else "cluster"),
@@ -523,6 +563,9 @@ def main(argv=None):
     ap.add_argument("--config", choices=list(W.CONFIGS), default="decode_qkv")
     ap.add_argument("--layers", type=int, default=0, help="layers per step (0: >= 2x L2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--paged", action="store_true",
+                    help="adapter weights as per-adapter pages found through address tables")
+    ap.add_argument("--lora-scales", action="store_true", help="per-adapter scale factors")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: only run --steps eager steps (for ncu launch lists)")
     args = ap.parse_args(argv)

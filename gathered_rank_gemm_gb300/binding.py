@@ -393,5 +393,19 @@ class LoraMetadata:
         lora_expand_partials(hidden, lora_b, scale, u, y, self.sorted_token_ids,
                              self.lora_token_start_loc, self.workspace, stream, lora_scales)
 
+    def shrink_paged(self, x, a_tables, rank, scale, u, stream=None, lora_scales=None):
+        lora_shrink_paged(x, a_tables, rank, scale, u, self.sorted_token_ids,
+                          self.lora_token_start_loc, self.workspace, stream, lora_scales)
+
+    def expand_paged(self, u, b_tables, slice_widths, y, stream=None):
+        lora_expand_paged(u, b_tables, slice_widths, y, self.sorted_token_ids,
+                          self.lora_token_start_loc, self.workspace, stream)
+
+    def shrink_expand_paged(self, x, a_tables, b_tables, slice_widths, scale, u, y, stream=None,
+                            lora_scales=None):
+        lora_shrink_expand_paged(x, a_tables, b_tables, slice_widths, scale, u, y,
+                                 self.sorted_token_ids, self.lora_token_start_loc,
+                                 self.workspace, stream, lora_scales)
+
     def read_status(self, stream=None) -> int:
         return lora_read_status(self.workspace, stream)
