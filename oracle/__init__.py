@@ -67,10 +67,12 @@ def _load():
         lib.oracle_prepare_metadata.argtypes = [p, i64, i64, i64, p, p, p]
         lib.oracle_shrink.restype = None
         lib.oracle_shrink.argtypes = [p, i64, i64, p, i64, i64, ctypes.c_double, p, p, i64, i64,
-                                      p, i64, ctypes.c_int]
+                                      p, i64, ctypes.c_int, ctypes.c_int]
         lib.oracle_expand.restype = None
         lib.oracle_expand.argtypes = [p, p, p, i64, i64, p, i64, p, i64, i64, p, i64,
-                                      ctypes.c_int]
+                                      ctypes.c_int, ctypes.c_int]
+        lib.oracle_decode_bits.restype = None
+        lib.oracle_decode_bits.argtypes = [p, i64, ctypes.c_int, p]
         lib.oracle_max_threads.restype = ctypes.c_int
         lib.oracle_max_threads.argtypes = []
         _lib = lib
@@ -112,13 +114,14 @@ def prepare_metadata(token_lora_mapping: np.ndarray, num_tokens: int, max_loras:
 
 def shrink(x_bits: np.ndarray, lora_a_bits, scale: float, token_lora_mapping: np.ndarray,
            num_tokens: int, max_loras: int, u_init: np.ndarray | None = None,
-           num_threads: int = 0, lora_scales=None) -> np.ndarray:
+           num_threads: int = 0, lora_scales=None, f16: bool = False) -> np.ndarray:
     """u[s][t][r] = c(m[t]) * sum_h x[t][h] A_s[m[t]][r][h] in fp64, with
     c(l) = scale, or scale * lora_scales[l] when per-adapter factors are given.
 
-    ``x_bits``: uint16 bf16 bits ``[T_max, H]``; ``lora_a_bits``: list of S
-    uint16 arrays ``[L, R, H]``.  Rows of tokens without an adapter (and
-    rows t >= n) keep ``u_init`` (NaN when not given).
+    ``x_bits``: uint16 bf16 bits ``[T_max, H]`` (fp16 bits when ``f16``);
+    ``lora_a_bits``: list of S uint16 arrays ``[L, R, H]`` of the same type.
+    Rows of tokens without an adapter (and rows t >= n) keep ``u_init`` (NaN
+    when not given).
     """
     x = _c(x_bits, np.uint16)
     t_max, hidden = x.shape
@@ -143,18 +146,20 @@ def shrink(x_bits: np.ndarray, lora_a_bits, scale: float, token_lora_mapping: np
             raise ValueError("lora_scales must have max_loras entries")
     _load().oracle_shrink(_ptr(x), hidden, hidden, ctypes.addressof(ptrs), num_slices, rank,
                           float(scale), None if ls is None else _ptr(ls), _ptr(m),
-                          int(num_tokens), int(max_loras), _ptr(u), t_max,
+                          int(num_tokens), int(max_loras), _ptr(u), t_max, int(bool(f16)),
                           int(num_threads) or max_threads())
     return u
 
 
 def expand(u: np.ndarray, lora_b_bits, y_bits: np.ndarray, token_lora_mapping: np.ndarray,
-           num_tokens: int, max_loras: int, num_threads: int = 0) -> np.ndarray:
+           num_tokens: int, max_loras: int, num_threads: int = 0,
+           f16: bool = False) -> np.ndarray:
     """y[t][off_s + j] + sum_r u[s][t][r] B_s[m[t]][r][j], returned in fp64.
 
     ``u``: float array ``[S, T_max, R]`` (converted to fp64); ``lora_b_bits``:
     list of S uint16 arrays ``[L, R, N_s]``; ``y_bits``: uint16 ``[T_max, W]``
-    with ``W >= sum N_s``.  Every element of the result is written.
+    with ``W >= sum N_s``; B and y hold bf16 bits, or fp16 bits when ``f16``.
+    Every element of the result is written.
     """
     uu = np.ascontiguousarray(u, dtype=np.float64)
     b_list = [_c(b, np.uint16) for b in lora_b_bits]
@@ -175,7 +180,16 @@ def expand(u: np.ndarray, lora_b_bits, y_bits: np.ndarray, token_lora_mapping: n
     ptrs = (ctypes.c_void_p * num_slices)(*[_ptr(b) for b in b_list])
     _load().oracle_expand(_ptr(uu), ctypes.addressof(ptrs), _ptr(widths), num_slices, rank,
                           _ptr(y), row, _ptr(m), int(num_tokens), int(max_loras), _ptr(out),
-                          t_max, int(num_threads) or max_threads())
+                          t_max, int(bool(f16)), int(num_threads) or max_threads())
+    return out
+
+
+def decode_bits(bits: np.ndarray, f16: bool = False) -> np.ndarray:
+    """The oracle's own decoding of 16-bit input words (bf16, or fp16 when
+    ``f16``) to float64, as its shrink and expand read them."""
+    b = _c(np.asarray(bits, dtype=np.uint16), np.uint16)
+    out = np.empty(b.shape, np.float64)
+    _load().oracle_decode_bits(_ptr(b), b.size, int(bool(f16)), _ptr(out))
     return out
 
 

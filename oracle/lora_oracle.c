@@ -24,13 +24,17 @@
  *              (times lora_scales[m[t]] when a per-adapter factor is given)
  *   expand:    y[t][off_s + j] += sum_r u[s][t][r] * B_s[m[t]][r][j]
  *
- * for t < n with 0 <= m[t] < L only.  Everything is plain loops in the
+ * for t < n with 0 <= m[t] < L only.  Inputs (x, A, B, y) are 16-bit words:
+ * bf16 by default, IEEE binary16 (fp16) when the f16 flag is set; the pages
+ * fix no input precision, and both types are decoded exactly to double.
+ * Everything is plain loops in the
  * order the definition states, accumulated in double.  Tokens are
  * independent, so the token loop may run on several host threads (OpenMP)
  * without changing any result.
  */
 #include <stdint.h>
 #include <stdlib.h>
+#include <math.h>
 #include <string.h>
 
 /* status bits reported by the metadata oracle */
@@ -44,6 +48,28 @@ static double bf16_bits_to_double(uint16_t bits)
     float f;
     memcpy(&f, &w, sizeof f);
     return (double)f;
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction
+ * bits; exponent 0 holds zeros and subnormals (fraction * 2^-24), exponent
+ * 31 infinities (fraction 0) and NaNs. */
+static double f16_bits_to_double(uint16_t bits)
+{
+    const int sign = (bits >> 15) & 1, exp = (bits >> 10) & 31, frac = bits & 1023;
+    double v;
+    if (exp == 0)
+        v = ldexp((double)frac, -24);
+    else if (exp == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp(1024.0 + (double)frac, exp - 25);
+    return sign ? -v : v;
+}
+
+/* A 16-bit input word as a double: fp16 when f16 is set, else bf16. */
+static double bits_to_double(uint16_t bits, int f16)
+{
+    return f16 ? f16_bits_to_double(bits) : bf16_bits_to_double(bits);
 }
 
 /* Bin of one token: its LoRA id, or L when it has no (valid) adapter. */
@@ -109,7 +135,7 @@ void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                    const uint16_t *const *lora_a, int64_t num_slices, int64_t rank,
                    double scale, const double *lora_scales, const int32_t *token_lora_mapping,
                    int64_t num_tokens, int64_t num_loras, double *u, int64_t max_num_tokens,
-                   int num_threads)
+                   int f16, int num_threads)
 {
     int64_t t;
 #pragma omp parallel for schedule(dynamic, 4) num_threads(num_threads)
@@ -123,7 +149,7 @@ void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
             for (int64_t r = 0; r < rank; ++r) {
                 double acc = 0.0;
                 for (int64_t h = 0; h < hidden; ++h)
-                    acc += bf16_bits_to_double(xrow[h]) * bf16_bits_to_double(a[r * hidden + h]);
+                    acc += bits_to_double(xrow[h], f16) * bits_to_double(a[r * hidden + h], f16);
                 u[(s * max_num_tokens + t) * rank + r] = c * acc;
             }
         }
@@ -142,13 +168,13 @@ void oracle_shrink(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
 void oracle_expand(const double *u, const uint16_t *const *lora_b, const int64_t *slice_width,
                    int64_t num_slices, int64_t rank, const uint16_t *y_in, int64_t y_row_stride,
                    const int32_t *token_lora_mapping, int64_t num_tokens, int64_t num_loras,
-                   double *y_out, int64_t max_num_tokens, int num_threads)
+                   double *y_out, int64_t max_num_tokens, int f16, int num_threads)
 {
     int64_t t;
 #pragma omp parallel for schedule(dynamic, 4) num_threads(num_threads)
     for (t = 0; t < max_num_tokens; ++t) {
         for (int64_t c = 0; c < y_row_stride; ++c)
-            y_out[t * y_row_stride + c] = bf16_bits_to_double(y_in[t * y_row_stride + c]);
+            y_out[t * y_row_stride + c] = bits_to_double(y_in[t * y_row_stride + c], f16);
         if (t >= num_tokens) continue;
         int32_t id = token_lora_mapping[t];
         if (id < 0 || (int64_t)id >= num_loras) continue;
@@ -159,7 +185,7 @@ void oracle_expand(const double *u, const uint16_t *const *lora_b, const int64_t
                 double acc = 0.0;
                 for (int64_t r = 0; r < rank; ++r)
                     acc += u[(s * max_num_tokens + t) * rank + r] *
-                           bf16_bits_to_double(b[r * slice_width[s] + j]);
+                           bits_to_double(b[r * slice_width[s] + j], f16);
                 y_out[t * y_row_stride + offset + j] += acc;
             }
             offset += slice_width[s];
@@ -176,4 +202,12 @@ int oracle_max_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* Decodes n 16-bit input words (fp16 when f16 is set, else bf16) to doubles;
+ * lets the tests pin the two decoders against an independent float16. */
+void oracle_decode_bits(const uint16_t *bits, int64_t n, int f16, double *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = bits_to_double(bits[i], f16);
 }

@@ -346,3 +346,59 @@ def test_exact_small_integer_case_matches_integer_arithmetic():
 
 def test_oracle_builds_with_threads():
     assert oracle.max_threads() >= 1
+
+
+# ---------------------------------------------------------------- fp16 inputs
+
+def test_decoders_match_numpy_on_every_bit_pattern():
+    """Both 16-bit decoders against independent float conversions over all
+    65536 patterns: fp16 against numpy's float16, bf16 against the top half
+    of a float32 word; NaN patterns must decode to NaN."""
+    every = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):   # widening signalling NaNs
+        refs = ((True, every.view(np.float16).astype(np.float64)),
+                (False, (every.astype(np.uint32) << 16).view(np.float32).astype(np.float64)))
+    for f16, ref in refs:
+        got = oracle.decode_bits(every, f16=f16)
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], ref[~nan])
+    # a few fp16 values written out by hand: smallest subnormal, largest
+    # subnormal, smallest normal, one, largest finite, negative two
+    hand = {0x0001: 2.0 ** -24, 0x03FF: 1023 * 2.0 ** -24, 0x0400: 2.0 ** -14,
+            0x3C00: 1.0, 0x7BFF: 65504.0, 0xC000: -2.0}
+    got = oracle.decode_bits(np.array(list(hand), np.uint16), f16=True)
+    assert got.tolist() == list(hand.values())
+
+
+def _f16_bits(a):
+    return np.asarray(a, np.float16).view(np.uint16)
+
+
+def test_fp16_shrink_and_expand_equal_dense_numpy_matmuls():
+    """fp16 inputs: one-adapter rows of a mixed batch equal numpy's dense
+    products on the same float16 values (a transposed operand or a bf16
+    decoding of fp16 words fails this)."""
+    rng = np.random.default_rng(21)
+    T, H, widths, L, R = 30, 80, (24, 40), 3, 8
+    x16 = rng.standard_normal((T, H)).astype(np.float16)
+    a16 = [(0.5 * rng.standard_normal((L, R, H))).astype(np.float16) for _ in widths]
+    b16 = [(0.5 * rng.standard_normal((L, R, w))).astype(np.float16) for w in widths]
+    y16 = rng.standard_normal((T, sum(widths))).astype(np.float16)
+    m = rng.integers(-1, L, size=T).astype(np.int32)
+    u = oracle.shrink(_f16_bits(x16), [_f16_bits(v) for v in a16], 0.5, m, T, L, f16=True)
+    y = oracle.expand(np.nan_to_num(u), [_f16_bits(v) for v in b16], _f16_bits(y16), m, T, L,
+                      f16=True)
+    x64, y64 = x16.astype(np.float64), y16.astype(np.float64)
+    for t in range(T):
+        off = 0
+        for s, w in enumerate(widths):
+            if m[t] < 0:
+                assert np.all(np.isnan(u[s, t]))
+                assert np.array_equal(y[t, off:off + w], y64[t, off:off + w])
+            else:
+                us = 0.5 * (a16[s][m[t]].astype(np.float64) @ x64[t])
+                np.testing.assert_allclose(u[s, t], us, rtol=1e-12, atol=1e-12)
+                ys = y64[t, off:off + w] + us @ b16[s][m[t]].astype(np.float64)
+                np.testing.assert_allclose(y[t, off:off + w], ys, rtol=1e-12, atol=1e-12)
+            off += w
