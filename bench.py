@@ -189,9 +189,10 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 
 # ---------------------------------------------------------------- oracle timing
 
-def oracle_sample_step(wl: W.Workload, max_tokens: int, threads: int):
+def oracle_sample_step(wl: W.Workload, max_tokens: int, threads: int, f16: bool = False):
     """One oracle pass (grouping + shrink + expand) over the first max_tokens
-    adapter tokens of layer 0; returns (tokens processed, seconds)."""
+    adapter tokens of layer 0 (fp16 input words when f16); returns (tokens
+    processed, seconds)."""
     import oracle
     sh, lay = wl.shape, wl.layers[0]
     n, L = sh.num_tokens, sh.max_loras
@@ -206,15 +207,15 @@ def oracle_sample_step(wl: W.Workload, max_tokens: int, threads: int):
     oracle.prepare_metadata(m, n, L)
     u = oracle.shrink(lay.x, lay.lora_a, sh.scale, m_sample, n, L,
                       u_init=np.zeros((sh.num_slices, sh.max_num_tokens, sh.rank)),
-                      num_threads=threads)
-    oracle.expand(u, lay.lora_b, lay.y, m_sample, n, L, num_threads=threads)
+                      num_threads=threads, f16=f16)
+    oracle.expand(u, lay.lora_b, lay.y, m_sample, n, L, num_threads=threads, f16=f16)
     return cut, time.perf_counter() - t0
 
 
-def oracle_sample_size(wl: W.Workload, budget_s: float, threads: int):
+def oracle_sample_size(wl: W.Workload, budget_s: float, threads: int, f16: bool = False):
     n = wl.shape.num_tokens
     k = min(n, 32)
-    _, dt = oracle_sample_step(wl, k, threads)
+    _, dt = oracle_sample_step(wl, k, threads, f16)
     per_tok = dt / max(k, 1)
     return max(1, min(n, int(budget_s / max(per_tok, 1e-9))))
 
@@ -231,21 +232,21 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def cpu_baseline(wl: W.Workload, seconds: float = 10.0):
+def cpu_baseline(wl: W.Workload, seconds: float = 10.0, f16: bool = False):
     import oracle
     threads = oracle.max_threads()
-    k = oracle_sample_size(wl, 2.0, threads)
+    k = oracle_sample_size(wl, 2.0, threads, f16)
     tok, el, reps = 0, 0.0, 0
     while el < seconds and reps < 1000:
-        t, dt = oracle_sample_step(wl, k, threads)
+        t, dt = oracle_sample_step(wl, k, threads, f16)
         tok += t
         el += dt
         reps += 1
     # one thread, for about a quarter of the time (its own sample size)
-    k1 = oracle_sample_size(wl, min(2.0, seconds / 4), 1)
+    k1 = oracle_sample_size(wl, min(2.0, seconds / 4), 1, f16)
     tok1, el1 = 0, 0.0
     while el1 < seconds / 4 or tok1 == 0:
-        t, dt = oracle_sample_step(wl, k1, 1)
+        t, dt = oracle_sample_step(wl, k1, 1, f16)
         tok1 += t
         el1 += dt
     return {"value": tok / el, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -260,13 +261,16 @@ def run_reference(args, world, rank):
     import oracle
     shape = W.CONFIGS[args.config]
     wl = W.make_workload(shape, num_layers=1, seed=1000 + shape.index + 7919 * rank)
+    f16 = args.dtype == "f16"
+    if f16:
+        wl.layers = [W.layer_as_f16(l) for l in wl.layers]
     threads = oracle.max_threads()
-    k = oracle_sample_size(wl, 1.0, threads)
+    k = oracle_sample_size(wl, 1.0, threads, f16)
     for _ in range(args.warmup):
-        oracle_sample_step(wl, k, threads)
+        oracle_sample_step(wl, k, threads, f16)
     tok, el = 0, 0.0
     for _ in range(args.steps):
-        t, dt = oracle_sample_step(wl, k, threads)
+        t, dt = oracle_sample_step(wl, k, threads, f16)
         tok += t
         el += dt
     value = tok / el
@@ -277,7 +281,7 @@ def run_reference(args, world, rank):
             "config": {"workload": shape.name, "max_num_tokens": shape.max_num_tokens,
                        "num_tokens": shape.num_tokens, "hidden": shape.hidden,
                        "slice_widths": list(shape.slice_widths), "max_loras": shape.max_loras,
-                       "rank": shape.rank},
+                       "rank": shape.rank, "inputs": args.dtype},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"first {k} of {shape.num_tokens} tokens per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -311,9 +315,17 @@ def run_ours(args, world, rank, local):
     seed = 1000 + shape.index + 7919 * rank
     wl = W.make_workload(shape, num_layers=layers, seed=seed)
     T, L, n = shape.max_num_tokens, shape.max_loras, shape.num_tokens
+    f16 = args.dtype == "f16"
+    if f16:
+        if args.paged:
+            print(json.dumps({"error": "paged weights are bf16 only"}))
+            return 1
+        # the same draws rounded to fp16; the *_f16 entry points run them
+        wl.layers = [W.layer_as_f16(l) for l in wl.layers]
+    dt16 = torch.float16 if f16 else torch.bfloat16
 
     def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt16)
 
     stream = torch.cuda.Stream(dev)
     # the larger workspace lets lora_shrink_expand take its split-K path (stacked
@@ -508,11 +520,11 @@ def run_ours(args, world, rank, local):
 
     result = None
     if rank == 0:
-        cpu = cpu_baseline(wl, seconds=args.cpu_seconds) if world == 1 else None
+        cpu = cpu_baseline(wl, seconds=args.cpu_seconds, f16=f16) if world == 1 else None
         result = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
             "data": "synthetic",
             "config": {"workload": shape.name, "max_num_tokens": T, "num_tokens": n,
                        "hidden": shape.hidden, "slice_widths": list(shape.slice_widths),
@@ -566,6 +578,8 @@ def main(argv=None):
     ap.add_argument("--paged", action="store_true",
                     help="adapter weights as per-adapter pages found through address tables")
     ap.add_argument("--lora-scales", action="store_true", help="per-adapter scale factors")
+    ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
+                    help="type of x, A, B and y (fp32 accumulation either way)")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: only run --steps eager steps (for ncu launch lists)")
     args = ap.parse_args(argv)

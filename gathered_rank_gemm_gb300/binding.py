@@ -5,8 +5,11 @@ of ``libgathered_rank_gemm.so``.  There is no CPU fallback: when the library
 is missing or a tensor is not on a CUDA device, the call raises.
 
 PyTorch provides device memory and streams.  Tensors are passed as raw
-pointers; bf16 tensors must be ``torch.bfloat16``, the work is enqueued on
-``stream`` (default: the current torch stream of the tensors' device).
+pointers; the 16-bit operands (x, A, B, y) are all ``torch.bfloat16`` or, with
+stacked weights, all ``torch.float16`` (which selects the ``*_f16`` entry
+points); the work is
+enqueued on ``stream`` (default: the current torch stream of the tensors'
+device).
 """
 from __future__ import annotations
 
@@ -30,7 +33,9 @@ EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora
             "lora_read_status", "lora_error_string", "lora_apply_noalloc",
             "lora_shrink_expand", "lora_shrink_expand_kernels",
             "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials",
-            "lora_shrink_paged", "lora_expand_paged", "lora_shrink_expand_paged")
+            "lora_shrink_paged", "lora_expand_paged", "lora_shrink_expand_paged",
+            "lora_shrink_f16", "lora_expand_f16", "lora_shrink_expand_f16",
+            "lora_shrink_partials_f16", "lora_expand_partials_f16")
 
 _lib = None
 
@@ -86,6 +91,11 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lora_shrink_expand_paged.restype = i32
     lib.lora_shrink_expand_paged.argtypes = [p, i64, i64, p, p, p, i32, i32, ctypes.c_float, p,
                                              p, p, i64, p, p, i64, i64, p, sz, p]
+    for name in ("lora_shrink", "lora_expand", "lora_shrink_expand", "lora_shrink_partials",
+                 "lora_expand_partials"):
+        f16 = getattr(lib, name + "_f16")
+        f16.restype = i32
+        f16.argtypes = getattr(lib, name).argtypes
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, p, i64, p, p, p, p, p]
@@ -123,6 +133,18 @@ def _scales(lora_scales, num_loras):
     return _dev(lora_scales, "lora_scales")
 
 
+def _is_f16(tensors, fp16_ok=True) -> bool:
+    """True for an all-fp16 operand set, False for all-bf16; raises otherwise."""
+    import torch
+    kinds = {t.dtype for t in tensors}
+    if kinds == {torch.bfloat16}:
+        return False
+    if kinds == {torch.float16} and fp16_ok:
+        return True
+    allowed = "all bfloat16 or all float16" if fp16_ok else "bfloat16"
+    raise ValueError(f"16-bit operands must be {allowed}, got {sorted(map(str, kinds))}")
+
+
 def _ptr_array(tensors, name):
     arr = (ctypes.c_void_p * len(tensors))(*[_dev(t, f"{name}[{i}]") for i, t in enumerate(tensors)])
     return arr
@@ -153,7 +175,8 @@ def lora_shrink(x, lora_a, scale: float, u, sorted_token_ids, lora_token_start_l
     lora_a = list(lora_a)
     arr = _ptr_array(lora_a, "lora_a")
     num_loras, rank, hidden = lora_a[0].shape
-    rc = load().lora_shrink(
+    fn = load().lora_shrink_f16 if _is_f16([x] + lora_a) else load().lora_shrink
+    rc = fn(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(lora_a), rank,
         float(scale), _scales(lora_scales, num_loras), _dev(u, "u"), _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
@@ -168,7 +191,8 @@ def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace,
     arr = _ptr_array(lora_b, "lora_b")
     widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
     num_loras, rank = lora_b[0].shape[:2]
-    rc = load().lora_expand(
+    fn = load().lora_expand_f16 if _is_f16([y] + lora_b) else load().lora_expand
+    rc = fn(
         _dev(u, "u"), ctypes.addressof(arr), ctypes.addressof(widths), len(lora_b), rank,
         _dev(y, "y"), y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), y.shape[0], num_loras,
@@ -185,7 +209,9 @@ def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
     arr_b = _ptr_array(lora_b, "lora_b")
     widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
     num_loras, rank, hidden = lora_a[0].shape
-    rc = load().lora_shrink_expand(
+    f16 = _is_f16([x, y] + lora_a + lora_b)
+    fn = load().lora_shrink_expand_f16 if f16 else load().lora_shrink_expand
+    rc = fn(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr_a), ctypes.addressof(arr_b),
         ctypes.addressof(widths), len(lora_a), rank, float(scale),
         _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"),
@@ -202,7 +228,8 @@ def lora_shrink_partials(x, lora_a, sorted_token_ids, lora_token_start_loc, work
     lora_a = list(lora_a)
     arr = _ptr_array(lora_a, "lora_a")
     num_loras, rank, hidden = lora_a[0].shape
-    rc = load().lora_shrink_partials(
+    fn = load().lora_shrink_partials_f16 if _is_f16([x] + lora_a) else load().lora_shrink_partials
+    rc = fn(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(lora_a), rank,
         _dev(sorted_token_ids, "sorted_token_ids"),
         _dev(lora_token_start_loc, "lora_token_start_loc"), x.shape[0], num_loras,
@@ -218,7 +245,8 @@ def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_i
     arr = _ptr_array(lora_b, "lora_b")
     widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
     num_loras, rank = lora_b[0].shape[:2]
-    rc = load().lora_expand_partials(
+    fn = load().lora_expand_partials_f16 if _is_f16([y] + lora_b) else load().lora_expand_partials
+    rc = fn(
         int(hidden), ctypes.addressof(arr), ctypes.addressof(widths), len(lora_b), rank,
         float(scale), _scales(lora_scales, num_loras), _dev(u, "u"), _dev(y, "y"), y.stride(0),
         _dev(sorted_token_ids, "sorted_token_ids"),
@@ -244,6 +272,7 @@ def lora_shrink_paged(x, a_tables, rank: int, scale: float, u, sorted_token_ids,
     a_tables = list(a_tables)
     arr = _table_array(a_tables, "a_tables")
     num_loras, hidden = a_tables[0].numel(), x.shape[1]
+    _is_f16([x], fp16_ok=False)
     rc = load().lora_shrink_paged(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr), len(a_tables), int(rank),
         float(scale), _scales(lora_scales, num_loras), _dev(u, "u"),
@@ -261,6 +290,7 @@ def lora_expand_paged(u, b_tables, slice_widths, y, sorted_token_ids, lora_token
     arr = _table_array(b_tables, "b_tables")
     widths = (ctypes.c_int64 * len(b_tables))(*[int(w) for w in slice_widths])
     num_loras, rank = b_tables[0].numel(), u.shape[2]
+    _is_f16([y], fp16_ok=False)
     rc = load().lora_expand_paged(
         _dev(u, "u"), ctypes.addressof(arr), ctypes.addressof(widths), len(b_tables), rank,
         _dev(y, "y"), y.stride(0), _dev(sorted_token_ids, "sorted_token_ids"),
@@ -279,6 +309,7 @@ def lora_shrink_expand_paged(x, a_tables, b_tables, slice_widths, scale: float, 
     arr_b = _table_array(b_tables, "b_tables")
     widths = (ctypes.c_int64 * len(b_tables))(*[int(w) for w in slice_widths])
     num_loras, hidden, rank = a_tables[0].numel(), x.shape[1], u.shape[2]
+    _is_f16([x, y], fp16_ok=False)
     rc = load().lora_shrink_expand_paged(
         _dev(x, "x"), x.stride(0), hidden, ctypes.addressof(arr_a), ctypes.addressof(arr_b),
         ctypes.addressof(widths), len(a_tables), rank, float(scale),
@@ -335,6 +366,7 @@ def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale:
     arr_b = _ptr_array(lora_b, "lora_b")
     widths = (ctypes.c_int64 * len(lora_b))(*[b.shape[2] for b in lora_b])
     num_loras, rank, hidden = lora_a[0].shape
+    _is_f16([x, y] + lora_a + lora_b, fp16_ok=False)
     rc = load().lora_apply_noalloc(
         _dev(token_lora_mapping, "token_lora_mapping"), _dev(num_tokens, "num_tokens"),
         token_lora_mapping.shape[0], num_loras, _dev(x, "x"), x.stride(0), hidden,

@@ -168,11 +168,12 @@ int split_of(int64_t max_num_tokens, int64_t max_loras, int64_t hidden, int num_
 }
 }  // namespace
 
-int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
-                         const uint16_t* const* lora_a, int num_slices, int rank,
-                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
-                         int64_t max_num_tokens, int64_t max_loras, void* workspace,
-                         size_t workspace_bytes, void* stream) {
+namespace {
+int shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                    const uint16_t* const* lora_a, int num_slices, int rank,
+                    const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                    int64_t max_num_tokens, int64_t max_loras, void* workspace,
+                    size_t workspace_bytes, void* stream, bool f16) {
   grg::ShrinkArgs sa;
   const int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, 1.0f,
                              nullptr, nullptr, sorted_token_ids, lora_token_start_loc,
@@ -183,7 +184,29 @@ int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden
   if (workspace_bytes < base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank))
     return LORA_ERR_WORKSPACE;
   sa.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + base);
+  sa.f16 = f16;
   return grg::launch_shrink(sa, static_cast<cudaStream_t>(stream));
+}
+}  // namespace
+
+int lora_shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                         const uint16_t* const* lora_a, int num_slices, int rank,
+                         const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                         int64_t max_num_tokens, int64_t max_loras, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  return shrink_partials(x, x_row_stride, hidden, lora_a, num_slices, rank, sorted_token_ids,
+                         lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                         workspace_bytes, stream, false);
+}
+
+int lora_shrink_partials_f16(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                             const uint16_t* const* lora_a, int num_slices, int rank,
+                             const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                             int64_t max_num_tokens, int64_t max_loras, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  return shrink_partials(x, x_row_stride, hidden, lora_a, num_slices, rank, sorted_token_ids,
+                         lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                         workspace_bytes, stream, true);
 }
 
 namespace {
@@ -193,7 +216,7 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
                     int64_t y_row_stride, const int32_t* sorted_token_ids,
                     const int32_t* lora_token_start_loc, int64_t max_num_tokens,
                     int64_t max_loras, const void* workspace, size_t workspace_bytes,
-                    void* stream, bool y_early) {
+                    void* stream, bool y_early, bool f16) {
   grg::ExpandArgs ea;
   const int rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
                              sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
@@ -211,6 +234,7 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
   ea.scale = scale;
   ea.lora_scales = lora_scales;
   ea.y_early = y_early;
+  ea.f16 = f16;
   return grg::launch_expand(ea, static_cast<cudaStream_t>(stream));
 }
 }  // namespace
@@ -224,7 +248,19 @@ int lora_expand_partials(int64_t hidden, const uint16_t* const* lora_b,
   // the caller may run anything between the halves: y only after the wait
   return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, lora_scales, u, y,
                          y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
-                         max_loras, workspace, workspace_bytes, stream, false);
+                         max_loras, workspace, workspace_bytes, stream, false, false);
+}
+
+int lora_expand_partials_f16(int64_t hidden, const uint16_t* const* lora_b,
+                             const int64_t* slice_width, int num_slices, int rank, float scale,
+                             const float* lora_scales, float* u, uint16_t* y,
+                             int64_t y_row_stride, const int32_t* sorted_token_ids,
+                             const int32_t* lora_token_start_loc, int64_t max_num_tokens,
+                             int64_t max_loras, const void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return expand_partials(hidden, lora_b, slice_width, num_slices, rank, scale, lora_scales, u, y,
+                         y_row_stride, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                         max_loras, workspace, workspace_bytes, stream, false, true);
 }
 
 int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
@@ -379,6 +415,58 @@ int lora_shrink_expand_paged(const uint16_t* x, int64_t x_row_stride, int64_t hi
                    sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras, workspace,
                    workspace_bytes, &ea);
   if (rc != LORA_OK) return rc;
+  return shrink_expand(sa, ea, hidden, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink_f16(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                    const uint16_t* const* lora_a, int num_slices, int rank, float scale,
+                    const float* lora_scales, float* u, const int32_t* sorted_token_ids,
+                    const int32_t* lora_token_start_loc, int64_t max_num_tokens,
+                    int64_t max_loras, const void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  grg::ShrinkArgs a;
+  const int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, scale,
+                             lora_scales, u, sorted_token_ids, lora_token_start_loc,
+                             max_num_tokens, max_loras, workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
+  a.f16 = true;
+  return grg::launch_shrink(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_expand_f16(const float* u, const uint16_t* const* lora_b, const int64_t* slice_width,
+                    int num_slices, int rank, uint16_t* y, int64_t y_row_stride,
+                    const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                    int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  grg::ExpandArgs a;
+  const int rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
+                             sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                             workspace, workspace_bytes, &a);
+  if (rc != LORA_OK) return rc;
+  a.f16 = true;
+  return grg::launch_expand(a, static_cast<cudaStream_t>(stream));
+}
+
+int lora_shrink_expand_f16(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
+                           const uint16_t* const* lora_a, const uint16_t* const* lora_b,
+                           const int64_t* slice_width, int num_slices, int rank, float scale,
+                           const float* lora_scales, float* u, uint16_t* y, int64_t y_row_stride,
+                           const int32_t* sorted_token_ids, const int32_t* lora_token_start_loc,
+                           int64_t max_num_tokens, int64_t max_loras, const void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  grg::ShrinkArgs sa;
+  grg::ExpandArgs ea;
+  int rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, scale,
+                       lora_scales, u, sorted_token_ids, lora_token_start_loc, max_num_tokens,
+                       max_loras, workspace, workspace_bytes, &sa);
+  if (rc != LORA_OK) return rc;
+  rc = expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
+                   sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                   workspace_bytes, &ea);
+  if (rc != LORA_OK) return rc;
+  sa.f16 = true;
+  ea.f16 = true;
   return shrink_expand(sa, ea, hidden, workspace, workspace_bytes,
                        static_cast<cudaStream_t>(stream));
 }

@@ -48,6 +48,7 @@ struct ExpandParams {
   // ([R][N_s] bf16), loaded by cp.async; null for stacked weights (tensor maps)
   const uint64_t* b_tab[3];
   int paged;
+  int f16;  // fp16 y and B (u is split into fp16 terms), else bf16
   int max_num_tokens;
   int w0, w1, w2;        // slice widths
   int off0, off1, off2;  // slice column offsets in y
@@ -86,7 +87,7 @@ constexpr int expand_stages() {
   return RANK <= 32 ? 2 : 1;
 }
 
-template <int BM, int RANK, int NS, bool PARTIAL, bool PAGED>
+template <int BM, int RANK, int NS, bool PARTIAL, bool PAGED, bool F16>
 __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     lora_expand_kernel(const __grid_constant__ ExpandParams p) {
   using Lay = ExpandLayout<BM, RANK, NS, PARTIAL>;
@@ -353,14 +354,14 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
         const float2 v0 = *reinterpret_cast<const float2*>(u0 + 2 * q);
         const float2 v1 = *reinterpret_cast<const float2*>(u1 + 2 * q);
         uint32_t a[4];
-        split_bf16x2(v0.x, v0.y, a[0], a[2]);
-        split_bf16x2(v1.x, v1.y, a[1], a[3]);
+        split_t<F16>(v0.x, v0.y, a[0], a[2]);
+        split_t<F16>(v1.x, v1.y, a[1], a[3]);
 #pragma unroll
         for (int nt = 0; nt < 8; nt += 4) {
           uint32_t bfr[4];
           ldsm_x4_trans(bfr, bw + swz128(lane & 7, nt + (lane >> 3)));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) mma_bf16(acc[nt + j], a, bfr[j], bfr[j]);
+          for (int j = 0; j < 4; ++j) mma_t<F16>(acc[nt + j], a, bfr[j], bfr[j]);
         }
       } else {
 #pragma unroll
@@ -371,20 +372,20 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
           const float2 v01 = *reinterpret_cast<const float2*>(u0 + kc + 8);
           const float2 v11 = *reinterpret_cast<const float2*>(u1 + kc + 8);
           uint32_t ah[4], al[4];
-          split_bf16x2(v00.x, v00.y, ah[0], al[0]);
-          split_bf16x2(v10.x, v10.y, ah[1], al[1]);
-          split_bf16x2(v01.x, v01.y, ah[2], al[2]);
-          split_bf16x2(v11.x, v11.y, ah[3], al[3]);
+          split_t<F16>(v00.x, v00.y, ah[0], al[0]);
+          split_t<F16>(v10.x, v10.y, ah[1], al[1]);
+          split_t<F16>(v01.x, v01.y, ah[2], al[2]);
+          split_t<F16>(v11.x, v11.y, ah[3], al[3]);
 #pragma unroll
           for (int nt = 0; nt < 8; nt += 2) {
             uint32_t bfr[4];
             const int mat = lane >> 3;
             ldsm_x4_trans(bfr, bw + swz128(kk * 16 + ((mat & 1) << 3) + (lane & 7),
                                            nt + (mat >> 1)));
-            mma_bf16(acc[nt], ah, bfr[0], bfr[1]);
-            mma_bf16(acc[nt], al, bfr[0], bfr[1]);
-            mma_bf16(acc[nt + 1], ah, bfr[2], bfr[3]);
-            mma_bf16(acc[nt + 1], al, bfr[2], bfr[3]);
+            mma_t<F16>(acc[nt], ah, bfr[0], bfr[1]);
+            mma_t<F16>(acc[nt], al, bfr[0], bfr[1]);
+            mma_t<F16>(acc[nt + 1], ah, bfr[2], bfr[3]);
+            mma_t<F16>(acc[nt + 1], al, bfr[2], bfr[3]);
           }
         }
       }
@@ -397,10 +398,10 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
             reinterpret_cast<uint32_t*>(stp + Lay::kY + (mi * 16 + g) * kYPitch + cbyte);
         uint32_t* y1 =
             reinterpret_cast<uint32_t*>(stp + Lay::kY + (mi * 16 + g + 8) * kYPitch + cbyte);
-        const float2 f0 = unpack_bf16x2(*y0);
-        const float2 f1 = unpack_bf16x2(*y1);
-        *y0 = pack_bf16x2(f0.x + acc[nt][0], f0.y + acc[nt][1]);
-        *y1 = pack_bf16x2(f1.x + acc[nt][2], f1.y + acc[nt][3]);
+        const float2 f0 = unpack_t<F16>(*y0);
+        const float2 f1 = unpack_t<F16>(*y1);
+        *y0 = pack_t<F16>(f0.x + acc[nt][0], f0.y + acc[nt][1]);
+        *y1 = pack_t<F16>(f1.x + acc[nt][2], f1.y + acc[nt][3]);
       }
     }
     __syncthreads();  // the updated stage is complete
@@ -434,9 +435,14 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
 template <int BM, int RANK, bool PARTIAL>
 static int run_expand(const ExpandParams& prm, cudaStream_t stream, long long max_items) {
   constexpr int NS = expand_stages<RANK>();
+  // fp16 inputs come with stacked weights only
+  if (prm.paged && prm.f16) return -3;
   const void* fn =
-      prm.paged ? reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, true>)
-                : reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, false>);
+      prm.paged
+          ? reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, true, false>)
+      : prm.f16
+          ? reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, false, true>)
+          : reinterpret_cast<const void*>(lora_expand_kernel<BM, RANK, NS, PARTIAL, false, false>);
   const size_t smem = ExpandLayout<BM, RANK, NS, PARTIAL>::kSmem;
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
@@ -456,6 +462,7 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   ExpandParams p;
   memset(&p, 0, sizeof(p));
   p.paged = a.b_tables[0] != nullptr;
+  p.f16 = a.f16 ? 1 : 0;
   for (int s = 0; s < 3; ++s) p.b_tab[s] = s < a.num_slices ? a.b_tables[s] : a.b_tables[0];
   p.u = a.u;
   p.partials = a.partials;

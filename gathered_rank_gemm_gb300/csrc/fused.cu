@@ -66,7 +66,7 @@ struct FusedParams {
   int off_a, off_x, off_b, off_y, off_u, off_red, off_rec, off_bar;
 };
 
-template <int NTW>
+template <int NTW, bool F16>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     lora_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -220,8 +220,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
               bf[2] = 0u;
               bf[3] = 0u;
             }
-            mma_bf16(acc[j], af, bf[0], bf[1]);
-            if (j + 1 < NTW && j + 1 < nt_cnt) mma_bf16(acc[j + 1], af, bf[2], bf[3]);
+            mma_t<F16>(acc[j], af, bf[0], bf[1]);
+            if (j + 1 < NTW && j + 1 < nt_cnt) mma_t<F16>(acc[j + 1], af, bf[2], bf[3]);
           }
         }
       }
@@ -303,14 +303,14 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const float2 v0 = *reinterpret_cast<const float2*>(u0 + 2 * q);
         const float2 v1 = *reinterpret_cast<const float2*>(u1 + 2 * q);
         uint32_t a[4];
-        split_bf16x2(v0.x, v0.y, a[0], a[2]);
-        split_bf16x2(v1.x, v1.y, a[1], a[3]);
+        split_t<F16>(v0.x, v0.y, a[0], a[2]);
+        split_t<F16>(v1.x, v1.y, a[1], a[3]);
 #pragma unroll
         for (int nt = 0; nt < 8; nt += 4) {
           uint32_t bfr[4];
           ldsm_x4_trans(bfr, bw + swz128(lane & 7, nt + (lane >> 3)));
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) mma_bf16(eacc[nt + jj], a, bfr[jj], bfr[jj]);
+          for (int jj = 0; jj < 4; ++jj) mma_t<F16>(eacc[nt + jj], a, bfr[jj], bfr[jj]);
         }
       } else {
         for (int kk = 0; kk < R / 16; ++kk) {
@@ -320,19 +320,19 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           const float2 v01 = *reinterpret_cast<const float2*>(u0 + kc + 8);
           const float2 v11 = *reinterpret_cast<const float2*>(u1 + kc + 8);
           uint32_t ah[4], al[4];
-          split_bf16x2(v00.x, v00.y, ah[0], al[0]);
-          split_bf16x2(v10.x, v10.y, ah[1], al[1]);
-          split_bf16x2(v01.x, v01.y, ah[2], al[2]);
-          split_bf16x2(v11.x, v11.y, ah[3], al[3]);
+          split_t<F16>(v00.x, v00.y, ah[0], al[0]);
+          split_t<F16>(v10.x, v10.y, ah[1], al[1]);
+          split_t<F16>(v01.x, v01.y, ah[2], al[2]);
+          split_t<F16>(v11.x, v11.y, ah[3], al[3]);
 #pragma unroll
           for (int nt = 0; nt < 8; nt += 2) {
             uint32_t bfr[4];
             const int mat = lane >> 3;
             ldsm_x4_trans(bfr, bw + swz128(kk * 16 + ((mat & 1) << 3) + (lane & 7), nt + (mat >> 1)));
-            mma_bf16(eacc[nt], ah, bfr[0], bfr[1]);
-            mma_bf16(eacc[nt], al, bfr[0], bfr[1]);
-            mma_bf16(eacc[nt + 1], ah, bfr[2], bfr[3]);
-            mma_bf16(eacc[nt + 1], al, bfr[2], bfr[3]);
+            mma_t<F16>(eacc[nt], ah, bfr[0], bfr[1]);
+            mma_t<F16>(eacc[nt], al, bfr[0], bfr[1]);
+            mma_t<F16>(eacc[nt + 1], ah, bfr[2], bfr[3]);
+            mma_t<F16>(eacc[nt + 1], al, bfr[2], bfr[3]);
           }
         }
       }
@@ -342,10 +342,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         uint32_t* y0 = reinterpret_cast<uint32_t*>(smem + p.off_y + j * 2048 + swz128(g, nt) + 4 * q);
         uint32_t* y1 =
             reinterpret_cast<uint32_t*>(smem + p.off_y + j * 2048 + swz128(g + 8, nt) + 4 * q);
-        const float2 f0 = unpack_bf16x2(*y0);
-        const float2 f1 = unpack_bf16x2(*y1);
-        *y0 = pack_bf16x2(f0.x + eacc[nt][0], f0.y + eacc[nt][1]);
-        *y1 = pack_bf16x2(f1.x + eacc[nt][2], f1.y + eacc[nt][3]);
+        const float2 f0 = unpack_t<F16>(*y0);
+        const float2 f1 = unpack_t<F16>(*y1);
+        *y0 = pack_t<F16>(f0.x + eacc[nt][0], f0.y + eacc[nt][1]);
+        *y1 = pack_t<F16>(f1.x + eacc[nt][2], f1.y + eacc[nt][3]);
       }
     }
     __syncthreads();
@@ -454,16 +454,19 @@ static int fused_active_clusters(const void* fn, int cluster, size_t smem) {
   return n;
 }
 
-static const void* fused_fn(int ntw) {
-  return ntw <= 4 ? reinterpret_cast<const void*>(lora_fused_kernel<4>)
-                  : reinterpret_cast<const void*>(lora_fused_kernel<8>);
+static const void* fused_fn(int ntw, bool f16) {
+  if (f16)
+    return ntw <= 4 ? reinterpret_cast<const void*>(lora_fused_kernel<4, true>)
+                    : reinterpret_cast<const void*>(lora_fused_kernel<8, true>);
+  return ntw <= 4 ? reinterpret_cast<const void*>(lora_fused_kernel<4, false>)
+                  : reinterpret_cast<const void*>(lora_fused_kernel<8, false>);
 }
 
 // The fused kernel pays off only when every tile's cluster runs in one wave:
 // a cluster holds one tile's whole problem, so a second wave doubles the time.
 static bool fused_one_wave(const FusedPlan& f) {
   if (!f.ok) return false;
-  const void* fn = fused_fn(f.ntw);
+  const void* fn = fused_fn(f.ntw, false);
   if (ensure_smem_attr(fn, f.smem) != 0) return false;
   return static_cast<long long>(fused_active_clusters(fn, f.cluster, f.smem)) >= f.max_tiles;
 }
@@ -542,7 +545,7 @@ int launch_fused(const ShrinkArgs& sa, const ExpandArgs& ea, cudaStream_t stream
   p.off_rec = f.off_rec;
   p.off_bar = f.off_bar;
 
-  const void* fn = fused_fn(f.ntw);
+  const void* fn = fused_fn(f.ntw, sa.f16);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   int per_sm = occupancy_blocks(fn, kFusedThreads, smem);
   if (per_sm < 1) per_sm = 1;

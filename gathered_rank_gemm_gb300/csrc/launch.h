@@ -60,6 +60,7 @@ struct ShrinkArgs {
   // paged weights: per slice a device table of max_loras addresses of A_s[l]
   // ([rank][hidden] bf16); all null for stacked weights (lora_a)
   const uint64_t* a_tables[3] = {nullptr, nullptr, nullptr};
+  bool f16 = false;  // fp16 x and A (else bf16)
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
 // CTAs sharing one tile's hidden dimension for this shape on the current
@@ -92,6 +93,7 @@ struct ExpandArgs {
   // paged weights: per slice a device table of max_loras addresses of B_s[l]
   // ([rank][slice_width] bf16); all null for stacked weights (lora_b)
   const uint64_t* b_tables[3] = {nullptr, nullptr, nullptr};
+  bool f16 = false;  // fp16 y and B (else bf16)
   // y may be read before the dependency wait: only when the expand directly
   // follows this library's shrink on the stream (the one-call path)
   bool y_early = false;

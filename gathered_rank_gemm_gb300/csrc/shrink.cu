@@ -65,9 +65,10 @@ struct ShrinkParams {
   // A_s[l] ([R][hidden] bf16); null for stacked weights (tensor maps)
   const uint64_t* a_tab[3];
   int paged;
+  int f16;  // fp16 x and A (else bf16)
 };
 
-template <int BM, int NTW, int NST, bool PAGED>
+template <int BM, int NTW, int NST, bool PAGED, bool F16>
 __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW > 8) ? 3 : 4)
     lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -293,8 +294,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
               }
 #pragma unroll
               for (int mi = 0; mi < BM / 16; ++mi) {
-                mma_bf16(acc[mi][j], af[mi], bf[0], bf[1]);
-                if (j + 1 < NTW && j + 1 < nt_cnt) mma_bf16(acc[mi][j + 1], af[mi], bf[2], bf[3]);
+                mma_t<F16>(acc[mi][j], af[mi], bf[0], bf[1]);
+                if (j + 1 < NTW && j + 1 < nt_cnt) mma_t<F16>(acc[mi][j + 1], af[mi], bf[2], bf[3]);
               }
             }
           }
@@ -398,8 +399,12 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
 template <int BM, int NTW, int NST>
 static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStream_t stream,
                       long long max_tiles) {
-  const void* fn = prm.paged ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, true>)
-                             : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false>);
+  // fp16 inputs come with stacked weights only
+  if (prm.paged && prm.f16) return -3;
+  const void* fn =
+      prm.paged  ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, true, false>)
+      : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false, true>)
+                : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false, false>);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -464,6 +469,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   ShrinkParams p;
   memset(&p, 0, sizeof(p));
   p.paged = a.a_tables[0] != nullptr;
+  p.f16 = a.f16 ? 1 : 0;
   for (int s = 0; s < 3; ++s) {
     p.a_tab[s] = s < a.num_slices ? a.a_tables[s] : a.a_tables[0];
     if (p.paged) continue;

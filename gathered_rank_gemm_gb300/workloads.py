@@ -178,3 +178,19 @@ def custom_shape(name: str = "custom", *, max_num_tokens: int, num_tokens: int |
     """A LayerShape for tests (same recipes as the named workloads)."""
     return LayerShape(name, max_num_tokens, max_num_tokens if num_tokens is None else num_tokens,
                       hidden, tuple(slice_widths), max_loras, rank, scale, mapping, neg_prob, 0)
+
+
+def to_f16_bits(bits: np.ndarray) -> np.ndarray:
+    """The values of bf16 bit patterns rounded to IEEE fp16 (numpy's float16
+    cast: nearest, ties to even; out-of-range values become infinities)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        f = (b.astype(np.uint32) << 16).view(np.float32).astype(np.float16)
+    return f.view(np.uint16)
+
+
+def layer_as_f16(layer: Layer) -> Layer:
+    """The same layer drawn in fp16: every input array's values as fp16 bits
+    (the pad-row NaN / huge garbage stays NaN / becomes infinity)."""
+    return Layer(x=to_f16_bits(layer.x), lora_a=[to_f16_bits(a) for a in layer.lora_a],
+                 lora_b=[to_f16_bits(b) for b in layer.lora_b], y=to_f16_bits(layer.y))

@@ -199,6 +199,47 @@ size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_lor
                                          int num_slices, int rank);
 
 /*
+ * fp16 variants (the pages fix no input precision; models served in fp16
+ * need them): the same arguments, results and rules as lora_shrink,
+ * lora_expand, lora_shrink_expand, lora_shrink_partials and
+ * lora_expand_partials (stacked weights), with x, A_s, B_s and y holding IEEE
+ * fp16 words instead of bf16.  Accumulation stays fp32; u enters the
+ * expand's tensor cores as an fp16 high part plus an fp16 residual, so |u|
+ * must stay below the fp16 range (65504); y is rounded once to fp16 (round
+ * to nearest even).  Paged weights and lora_apply_noalloc are bf16 only.
+ */
+int lora_shrink_f16(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                    const uint16_t *const *lora_a, int num_slices, int rank, float scale,
+                    const float *lora_scales, float *u, const int32_t *sorted_token_ids,
+                    const int32_t *lora_token_start_loc, int64_t max_num_tokens,
+                    int64_t max_loras, const void *workspace, size_t workspace_bytes,
+                    void *stream);
+int lora_expand_f16(const float *u, const uint16_t *const *lora_b, const int64_t *slice_width,
+                    int num_slices, int rank, uint16_t *y, int64_t y_row_stride,
+                    const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                    int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                    size_t workspace_bytes, void *stream);
+int lora_shrink_expand_f16(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                           const uint16_t *const *lora_a, const uint16_t *const *lora_b,
+                           const int64_t *slice_width, int num_slices, int rank, float scale,
+                           const float *lora_scales, float *u, uint16_t *y, int64_t y_row_stride,
+                           const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                           int64_t max_num_tokens, int64_t max_loras, const void *workspace,
+                           size_t workspace_bytes, void *stream);
+int lora_shrink_partials_f16(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
+                             const uint16_t *const *lora_a, int num_slices, int rank,
+                             const int32_t *sorted_token_ids, const int32_t *lora_token_start_loc,
+                             int64_t max_num_tokens, int64_t max_loras, void *workspace,
+                             size_t workspace_bytes, void *stream);
+int lora_expand_partials_f16(int64_t hidden, const uint16_t *const *lora_b,
+                             const int64_t *slice_width, int num_slices, int rank, float scale,
+                             const float *lora_scales, float *u, uint16_t *y,
+                             int64_t y_row_stride, const int32_t *sorted_token_ids,
+                             const int32_t *lora_token_start_loc, int64_t max_num_tokens,
+                             int64_t max_loras, const void *workspace, size_t workspace_bytes,
+                             void *stream);
+
+/*
  * Paged adapter weights (the S-LoRA idea of the pages' "[Tracking] Multi-LoRA
  * Serving" overview: adapters live in separately allocated pages rather than
  * one stacked tensor).  Same arguments, results and rules as lora_shrink,

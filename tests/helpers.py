@@ -24,6 +24,11 @@ def bf16_dev(a: np.ndarray, dev):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
 
+def f16_dev(a: np.ndarray, dev):
+    torch = torch_mod()
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.float16)
+
+
 def bits_of(t) -> np.ndarray:
     torch = torch_mod()
     return t.detach().view(torch.int16).cpu().numpy().view(np.uint16)
@@ -65,8 +70,15 @@ class DeviceCase:
 
     def __init__(self, shape: W.LayerShape, mapping: np.ndarray, layer: W.Layer, dev,
                  x_pad: int = 0, y_pad: int = 0, split_workspace: bool = False,
-                 lora_scales=None, paged: bool = False):
+                 lora_scales=None, paged: bool = False, f16: bool = False):
         torch = torch_mod()
+        # fp16 inputs: the same draws rounded to fp16, through the *_f16 entry points
+        self.f16 = f16
+        if f16:
+            assert not paged, "paged weights are bf16 only"
+            layer = W.layer_as_f16(layer)
+        dev16 = f16_dev if f16 else bf16_dev
+        dt16 = torch.float16 if f16 else torch.bfloat16
         self.shape, self.mapping_np, self.layer, self.dev = shape, mapping, layer, dev
         # per-adapter factors on the scale (float32 values, also given to the oracle)
         self.lora_scales_np = None if lora_scales is None else np.asarray(lora_scales, np.float32)
@@ -79,17 +91,17 @@ class DeviceCase:
         xs[:, :shape.hidden] = layer.x
         if x_pad:
             xs[:, shape.hidden:] = W.BF16_QNAN_PAYLOAD   # never read
-        self.x_full = bf16_dev(xs, dev)
+        self.x_full = dev16(xs, dev)
         self.x = self.x_full[:, :shape.hidden]
         ys = np.zeros((T, shape.out_width + y_pad), np.uint16)
         ys[:, :shape.out_width] = layer.y
         if y_pad:
             ys[:, shape.out_width:] = W.BF16_Y_SENTINEL
         self.y_in_bits = ys
-        self.y = Guarded((T, shape.out_width + y_pad), torch.bfloat16, dev, init=bf16_dev(ys, dev))
+        self.y = Guarded((T, shape.out_width + y_pad), dt16, dev, init=dev16(ys, dev))
         self.y_view = self.y.view[:, :shape.out_width]
-        self.a = [bf16_dev(v, dev) for v in layer.lora_a]
-        self.b = [bf16_dev(v, dev) for v in layer.lora_b]
+        self.a = [dev16(v, dev) for v in layer.lora_a]
+        self.b = [dev16(v, dev) for v in layer.lora_b]
         # paged weights: every adapter's A_s[l] / B_s[l] in its own allocation
         # (allocated in reverse adapter order), found through address tables
         self.paged = paged
@@ -210,12 +222,12 @@ def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None,
     u_ref = oracle.shrink(lay.x, lay.lora_a, sh.scale, m_sel, n, L,
                           u_init=np.zeros((sh.num_slices, T, sh.rank)),
                           lora_scales=None if case.lora_scales_np is None
-                          else case.lora_scales_np.astype(np.float64))
+                          else case.lora_scales_np.astype(np.float64), f16=case.f16)
     ok_u, r_u = within_tol(u_gpu[:, rows].astype(np.float64), u_ref[:, rows])
     assert ok_u, f"u differs from the oracle (worst err/bound {r_u:.3f})"
 
     y_gpu_bits = bits_of(case.y.view)
-    y_gpu = oracle.bf16_bits_to_f64(y_gpu_bits)
+    y_gpu = oracle.decode_bits(y_gpu_bits, f16=case.f16)
     y_in = case.y_in_bits
     untouched = ~keep
     assert np.array_equal(y_gpu_bits[untouched], y_in[untouched]), "y rows without adapter changed"
@@ -224,15 +236,17 @@ def check_case(case: DeviceCase, *, full_oracle: bool = True, sample_rows=None,
             "y columns past the slices changed"
     y_in_used = np.ascontiguousarray(y_in[:, :sh.out_width])
     # (i) end to end: oracle u in fp64
-    y_ref = oracle.expand(u_ref, lay.lora_b, y_in_used, m_sel, n, L)
+    y_ref = oracle.expand(u_ref, lay.lora_b, y_in_used, m_sel, n, L, f16=case.f16)
     ok_y, r_y = within_tol(y_gpu[rows, :sh.out_width], y_ref[rows])
     assert ok_y, f"y differs from the oracle end to end (worst err/bound {r_y:.3f})"
     # (ii) expand alone: the GPU's own u fed to the oracle, zero base output
     zero_y = np.zeros_like(y_in_used)
-    d_ref = oracle.expand(np.nan_to_num(u_gpu.astype(np.float64)), lay.lora_b, zero_y, m_sel, n, L)
-    d_gpu = y_gpu[rows, :sh.out_width] - oracle.bf16_bits_to_f64(y_in_used[rows])
-    # the GPU delta carries the final bf16 rounding of y: bound it by half an ulp of y
-    ulp = np.abs(y_gpu[rows, :sh.out_width]) * 2.0 ** -8
+    d_ref = oracle.expand(np.nan_to_num(u_gpu.astype(np.float64)), lay.lora_b, zero_y, m_sel, n, L,
+                          f16=case.f16)
+    d_gpu = y_gpu[rows, :sh.out_width] - oracle.decode_bits(y_in_used[rows], f16=case.f16)
+    # the GPU delta carries the final 16-bit rounding of y: bound it by an ulp
+    # of y (8 significand bits for bf16, 11 for fp16)
+    ulp = np.abs(y_gpu[rows, :sh.out_width]) * 2.0 ** (-10 if case.f16 else -8)
     err = np.abs(d_gpu - d_ref[rows])
     assert np.all(err <= ATOL + RTOL * np.abs(d_ref[rows]) + ulp), \
         "expand delta differs from the oracle's expand of the GPU u"

@@ -23,7 +23,7 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(lora_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -201,3 +201,16 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(4, 8, dtype=torch.int32)
     with pytest.raises(ValueError, match="CUDA tensor"):
         binding.lora_prepare_metadata(x[0], x[0, :1], 4, x[0], x[0], x[0], x[0])
+
+
+def test_binding_selects_the_input_type_and_rejects_mixtures():
+    torch = pytest.importorskip("torch")
+    bf, hf = torch.zeros(2, dtype=torch.bfloat16), torch.zeros(2, dtype=torch.float16)
+    assert binding._is_f16([bf, bf]) is False
+    assert binding._is_f16([hf, hf]) is True
+    with pytest.raises(ValueError):
+        binding._is_f16([bf, hf])
+    with pytest.raises(ValueError):
+        binding._is_f16([torch.zeros(2)])
+    with pytest.raises(ValueError):   # entry points without an fp16 variant
+        binding._is_f16([hf], fp16_ok=False)

@@ -35,7 +35,8 @@ def _worker(rank, world, port, out_q):
     try:
         bench.barrier(world)
         mx = bench.max_over_ranks(10.0 + rank, world)
-        args = bench.argparse.Namespace(steps=2, warmup=1, config="tiny", impl="reference")
+        args = bench.argparse.Namespace(steps=2, warmup=1, config="tiny", impl="reference",
+                                         dtype="bf16")
         buf = io.StringIO()
         with redirect_stdout(buf):
             rc = bench.run_reference(args, world, rank)

@@ -594,3 +594,75 @@ def test_paged_zero_and_misaligned_entries_read_as_zero_adapters(dev):
         lay.lora_b[s][1:3] = 0
     check_case(case, sample_rows=300)
     assert case.ws.view[:4].view(torch.int32).item() & binding.LORA_STATUS_BAD_WEIGHT
+
+
+# ------------------------------------------------------------ fp16 inputs
+
+F16_SHAPES = [
+    # (name, spec or workload, split_workspace, one_call)
+    ("decode_qkv_two_calls", None, False, False),
+    ("decode_qkv_split_k", None, True, True),
+    ("tiny_fused", (64, 64, 512, (512,), 4, 8), False, True),
+    ("ragged_cluster", (300, 211, 1032, (264, 72, 136), 6, 16), False, True),
+    ("prefill_like", (4096, 4000, 1024, (1024,), 8, 16), False, False),
+    ("rank64_two_slices", (1024, 1000, 1024, (1032, 520), 8, 64), False, True),
+    ("rank128", (512, 500, 2048, (256,), 6, 128), False, False),
+    ("split_k_rank32", (1000, 977, 8264, (1032, 520, 264), 5, 32), True, True),
+]
+
+
+def _f16_case(spec, dev, split_workspace=False, seed=51, lora_scales=None):
+    if spec is None:
+        wl = W.make_workload("decode_qkv")
+        return DeviceCase(wl.shape, wl.mapping, wl.layers[0], dev,
+                          split_workspace=split_workspace, f16=True, lora_scales=lora_scales)
+    T, n, H, widths, L, R = spec
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, scale=0.5, neg_prob=0.15)
+    rng = np.random.default_rng(seed)
+    return DeviceCase(shape, W.make_mapping(shape, rng), W.make_layer(shape, rng), dev,
+                      split_workspace=split_workspace, f16=True, lora_scales=lora_scales)
+
+
+@pytest.mark.parametrize("name,spec,split_ws,one_call", F16_SHAPES)
+def test_fp16_inputs_match_the_oracle(name, spec, split_ws, one_call, dev):
+    case = _f16_case(spec, dev, split_workspace=split_ws)
+    assert case.x.dtype == torch.float16 and case.y_view.dtype == torch.float16
+    check_case(case, fused=one_call, sample_rows=300)
+    if split_ws:
+        assert torch.any(case.ws.view[case.ws_base:] != 0)
+
+
+def test_fp16_inputs_with_per_adapter_scales(dev):
+    spec = (256, 240, 8200, (1024, 512), 4, 8)
+    factors = np.array([0.0, 1.5, -0.75, 2.0], np.float32)
+    case = _f16_case(spec, dev, split_workspace=True, lora_scales=factors)
+    check_case(case, fused=True, sample_rows=200)
+
+
+@pytest.mark.parametrize("one_call", [False, True])
+def test_fp16_and_bf16_paths_agree_exactly_on_small_integers(one_call, dev):
+    """Small integers are exact in both formats and every product and sum
+    stays exact in fp32, so the two input types give the same values."""
+    T, H = 64, 4096
+    case_b, _ = _int_case(dev, T, H, 16, seed=H)
+    case_h = DeviceCase(case_b.shape, case_b.mapping_np, case_b.layer, dev, f16=True)
+    case_b.run(fused=one_call)
+    case_h.run(fused=one_call)
+    assert torch.equal(case_b.u.view.view(torch.int32), case_h.u.view.view(torch.int32))
+    rows = lora_rows(case_b.mapping_np, T, 3)
+    assert torch.equal(case_b.y.view[rows].float(), case_h.y.view[rows].float())
+
+
+def test_fp16_split_k_halves_equal_the_one_call(dev):
+    a = _f16_case(None, dev, split_workspace=True)
+    b = _f16_case(None, dev, split_workspace=True)
+    a.run(fused=True)
+    b.prepare()
+    binding.lora_shrink_partials(b.x, b.a, b.sorted.view, b.starts.view, b.ws.view)
+    binding.lora_expand_partials(b.shape.hidden, b.b, b.shape.scale, b.u.view, b.y_view,
+                                 b.sorted.view, b.starts.view, b.ws.view)
+    torch.cuda.synchronize()
+    assert b.guards_intact()
+    assert torch.equal(a.y.view.view(torch.int16), b.y.view.view(torch.int16))
+    assert torch.equal(a.u.view.view(torch.int32), b.u.view.view(torch.int32))
