@@ -112,6 +112,21 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool 
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(bytes)
                : "memory");
 }
+// An L2 policy that marks the lines a load brings in as the first to evict
+// (for data this kernel reads once and nothing after it reads again).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// cp_async_16 with an L2 cache policy.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, bool pred,
+                                                 uint64_t pol) {
+  const int bytes = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "l"(pol)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }

@@ -14,8 +14,8 @@
 //  - a producer warp fills a stage with the adapter's R x 64 block of every
 //    slice (one TMA tile load each: tensor map, 128-byte swizzle) and the BM
 //    gathered x rows (16-byte cp.async, zero-filled past the tile's tokens and
-//    past H); TMA bytes and the lanes' cp.async arrivals complete the stage's
-//    "full" mbarrier;
+//    past H, under an L2 evict-first policy: x is read once); TMA bytes and
+//    the lanes' cp.async arrivals complete the stage's "full" mbarrier;
 //  - four consumer warps wait on "full", run the tensor-core MMAs (mma.sync
 //    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
 //    mbarrier; no block-wide barrier inside the k-loop.
@@ -89,6 +89,12 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
 
+  // the gathered x rows are read once (by this kernel's CTAs only): their L2
+  // lines go first, which leaves the L2 to the adapter blocks every tile of
+  // a LoRA re-reads and to the lines the expand works on (prefill layer
+  // 52 -> 48 us)
+  const uint64_t x_pol = l2_evict_first_policy();
+
   uint32_t cl_size;
   asm volatile("mov.u32 %0, %%cluster_nctarank;\n" : "=r"(cl_size));
   const bool split_k = p.partials != nullptr;
@@ -137,8 +143,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
       const int kcol = kb * kBK + ch * 8;
       const bool ok = t >= 0 && kcol < p.hidden;
-      cp_async_16(sbase + st * p.stage_bytes + swz128(row, ch),
-                  ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
+      cp_async_16_hint(sbase + st * p.stage_bytes + swz128(row, ch),
+                       ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok, x_pol);
     };
     // paged weights: this adapter's A_s (a null or misaligned table entry
     // reads as an all-zero adapter and sets LORA_STATUS_BAD_WEIGHT)
@@ -250,7 +256,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
 #pragma unroll
         for (int j = 0; j < XJ; ++j) {
           const bool ok = xrow[j] != nullptr && kin;
-          cp_async_16(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
+          cp_async_16_hint(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok,
+                           x_pol);
         }
         cp_async_mbar_arrive(full_bar + 8 * st);
       }
