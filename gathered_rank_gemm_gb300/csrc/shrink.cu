@@ -465,10 +465,14 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int kb_per = (kblocks + cluster - 1) / cluster;
   // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
   // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
-  // for the next kernel's CTAs to start under programmatic launch)
+  // for the next kernel's CTAs to start under programmatic launch).  Up to 4
+  // blocks, 4 stages hold the whole range and leave the room to the expand
+  // CTAs that start under this kernel (decode layer 8.72 -> 8.49 us)
   const int stage = (BM + SR) * 128;  // a multiple of 1024: BM and S*R are multiples of 8
   int nst;
-  if (kb_per <= 8)
+  if (kb_per <= 4 && ntw <= 8)
+    nst = 4;
+  else if (kb_per <= 8)
     nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
   else
     nst = ((SR >= 128 && kb_per > 32) || 4 * stage > 96 * 1024) ? 2 : 4;
