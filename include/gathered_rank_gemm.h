@@ -331,7 +331,7 @@ int lora_read_status(void *workspace, uint32_t *status, void *stream);
 
 /*
  * One layer - grouping, shrink and expand - without allocating anything.
- * The paper has no counterpart to this call: it exists for callers that
+ * The pages describe no counterpart to this call: it exists for callers that
  * cannot call cudaMalloc (a memory manager that owns the whole device, a
  * plugin host that hands out no device memory, code that must not allocate)
  * and so cannot provide the workspace the three calls above take.
