@@ -1,22 +1,36 @@
 #!/usr/bin/env python3
 """Benchmark: multi-LoRA shrink + expand throughput (tokens/s per LoRA layer).
 
-One step is one pass of the whole hot path over one batch: the device
-grouping of the batch's tokens by LoRA id (once per batch), then shrink and
-expand for each of ``--layers`` independent LoRA layers (distinct x, A, B, u,
-y per layer, so the step's inputs are larger than the 129 MB L2 and every
-byte comes from HBM).  The step is captured once in a CUDA graph and
-replayed, as a serving engine does.
+A step is one pass of the whole hot path over one batch: the device grouping
+of the batch's tokens by LoRA id (once per batch), then one
+``lora_shrink_expand`` call (shrink + expand) for each of ``layers`` LoRA
+layers held in distinct device buffers (so the step's inputs are larger than
+twice the L2 and every byte comes from HBM).  Grouping and layers are
+captured once as CUDA graphs and replayed, as a serving engine does.
 
-value   = n * layers / step time * ranks  (tokens/s per LoRA layer, whole job)
-e2e     = the same metric with the per-step inputs (mapping, n, x, y of every
-          layer) copied from pinned host memory and y copied back each step
+With no ``--config`` every one of the five workloads is measured and the
+JSON line's headline is ``down_proj_graph``, the largest one; the others are
+in ``per_workload``.  For each workload:
+
+value   = n * layers / t_layers  (tokens/s per LoRA layer, whole job): t_layers
+          is the device time of the shrink + expand calls of a step, read with
+          CUDA events around them; the grouping's time is reported on its own
+          (``us.metadata_in_step``) and ``value_with_metadata`` counts it in
+ms_per_step = grouping + layers, device time of one step
+e2e     = the same metric through the C ABI with each step's inputs (mapping,
+          n, every layer's x and y) copied from pinned host memory and every
+          layer's y copied back, host clock around the steps
 roofline: the algorithmic bytes of the kernel with the largest share of the
-          layer's device time / its measured launch time
-          against the measured HBM copy bandwidth
+          layer's device time / its launch time, against the measured HBM copy
+          bandwidth; ``shrink_expand_frac`` is the same for the whole layer
+
+The timed region is exactly --steps steps, bracketed by a barrier and a
+device synchronisation; it is repeated until a workload has been timed for at
+least --min-timed-ms, and ms_per_step is the median over the repetitions.
+GPU clocks are sampled with nvidia-smi throughout.
 
 ``--impl reference`` times the fp64 CPU oracle instead (the only reference
-this method has here), on the host cores, one bounded sample per step.
+this method has), on the host cores, one bounded sample per step.
 """
 from __future__ import annotations
 
@@ -26,9 +40,10 @@ import json
 import math
 import os
 import shutil
+import socket
 import subprocess
 import sys
-import tempfile
+import threading
 import time
 
 import numpy as np
@@ -40,6 +55,8 @@ from gathered_rank_gemm_gb300 import workloads as W  # noqa: E402
 
 METRIC = "LoRA shrink+expand tokens/s per layer; achieved HBM GB/s vs GB300 peak"
 UNIT = "tokens/s"
+HEADLINE = "down_proj_graph"
+ORDER = ("tiny", "decode_qkv", "chunked_prefill", "mlp_gate_up", "down_proj_graph")
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {"expand": "gathered_rank_gemm_gb300/csrc/expand.cu",
                   "shrink": "gathered_rank_gemm_gb300/csrc/shrink.cu",
@@ -65,6 +82,47 @@ def algorithmic_bytes(shape: W.LayerShape, mapping: np.ndarray):
     flops = {"shrink": 2 * n_l * S * R * H, "expand": 2 * n_l * R * N}
     return dict(n_lora_tokens=n_l, active_loras=l_act, shrink=shrink, expand=expand,
                 metadata=meta, flops=flops)
+
+
+def layer_bytes(shape: W.LayerShape) -> int:
+    """Device bytes of one layer's buffers (x, y, u, A, B)."""
+    return (shape.max_num_tokens * (shape.hidden + shape.out_width) * 2
+            + sum(shape.max_loras * shape.rank * (shape.hidden + w) * 2 for w in shape.slice_widths)
+            + 4 * shape.num_slices * shape.max_num_tokens * shape.rank)
+
+
+def layers_per_step(shape: W.LayerShape, l2_bytes: int) -> int:
+    """Distinct layer buffers per step: together more than twice the L2, and
+    at least four, so a layer's inputs were evicted before it comes round."""
+    return max(4, math.ceil(2 * l2_bytes / layer_bytes(shape)))
+
+
+def config_of(shape: W.LayerShape, args, l2_bytes: int, world: int) -> dict:
+    """The workload and how it is run (the same for both arms)."""
+    layers = args.layers or layers_per_step(shape, l2_bytes)
+    return {"workload": shape.name, "max_num_tokens": shape.max_num_tokens,
+            "num_tokens": shape.num_tokens, "hidden": shape.hidden,
+            "slice_widths": list(shape.slice_widths), "max_loras": shape.max_loras,
+            "rank": shape.rank, "inputs": args.dtype,
+            "weights": "paged" if args.paged else "stacked",
+            "lora_scales": bool(args.lora_scales), "layers_per_step": layers,
+            "l2": f"inputs larger than L2: {layers} distinct layer buffers, "
+                  f"{layers * layer_bytes(shape) / 1e6:.0f} MB per step vs "
+                  f"{l2_bytes / 1e6:.0f} MB L2",
+            "graph": "per step: one CUDA graph of the grouping, one of the "
+                     "lora_shrink_expand calls of every layer",
+            "parallelism": f"replicas x{world} (independent batches, no collective)"}
+
+
+def device_l2_bytes() -> int:
+    """L2 size of the GPU (GB300: about 130 MB when none is visible)."""
+    try:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.get_device_properties(0).L2_cache_size)
+    except Exception:
+        pass
+    return 132_120_576
 
 
 def load_peaks():
@@ -101,53 +159,63 @@ def recorded_traffic(kernel: str, workload: str):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi clock / throttle samples, each stamped with the host clock."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, local_rank: int):
         self.proc = None
         vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
         self.gpu = vis[local_rank] if local_rank < len(vis) and vis[local_rank].isdigit() \
-            else local_rank
-        self.tmp = None
+            else str(local_rank)
+        self.rows = []
+        self.reader = None
 
     def start(self):
         exe = shutil.which("nvidia-smi")
         if not exe:
             return
-        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.proc = subprocess.Popen([exe, f"--query-gpu={self.FIELDS}",
-                                      "--format=csv,noheader,nounits", "-lms", "100"],
-                                     stdout=self.tmp, stderr=subprocess.DEVNULL)
+                                      "--format=csv,noheader,nounits", "-lms", "50"],
+                                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+        def read():
+            for line in self.proc.stdout:
+                if line.strip():
+                    self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+        self.reader = threading.Thread(target=read, daemon=True)
+        self.reader.start()
         time.sleep(0.3)
 
     def stop(self):
         if self.proc is None:
-            return None
-        time.sleep(0.2)
+            return
+        time.sleep(0.1)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        self.tmp.flush()
-        self.tmp.seek(0)
-        rows = [r.split(",") for r in self.tmp.read().splitlines() if r.strip()]
-        self.tmp.close()
-        os.unlink(self.tmp.name)
+        self.reader.join(timeout=5)
+
+    def summary(self, windows=None):
+        """Median SM clock, max clock and active throttle reasons over the
+        samples inside the host-time windows (all samples when None)."""
+        ids = {r[0] for _, r in self.rows if r}
+        target = self.gpu if self.gpu in ids else (sorted(ids)[0] if ids else "0")
         sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        ids = {r[0].strip() for r in rows if r}
-        target = str(self.gpu) if str(self.gpu) in ids else (sorted(ids)[0] if ids else "0")
-        for r in rows:
+        for ts, r in self.rows:
+            if windows is not None and not any(a <= ts <= b for a, b in windows):
+                continue
             try:
-                if r[0].strip() != target:
+                if r[0] != target:
                     continue
                 sm.append(float(r[1]))
                 mx.append(float(r[2]))
-                for name, val in zip(names, r[5:9]):
-                    if val.strip().lower() == "active":
+                for name, val in zip(self.REASONS, r[5:9]):
+                    if val.lower() == "active":
                         reasons.add(name)
             except (ValueError, IndexError):
                 continue
@@ -191,18 +259,15 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
 
 def oracle_sample_step(wl: W.Workload, max_tokens: int, threads: int, f16: bool = False):
     """One oracle pass (grouping + shrink + expand) over the first max_tokens
-    adapter tokens of layer 0 (fp16 input words when f16); returns (tokens
-    processed, seconds)."""
+    tokens of layer 0 (fp16 input words when f16); returns (tokens processed,
+    seconds)."""
     import oracle
     sh, lay = wl.shape, wl.layers[0]
     n, L = sh.num_tokens, sh.max_loras
     m = wl.mapping.copy()
-    if max_tokens < n:
-        cut = n if max_tokens >= n else max_tokens
-        m_sample = m.copy()
-        m_sample[cut:n] = -1
-    else:
-        cut, m_sample = n, m
+    cut = min(max_tokens, n)
+    m_sample = m.copy()
+    m_sample[cut:n] = -1
     t0 = time.perf_counter()
     oracle.prepare_metadata(m, n, L)
     u = oracle.shrink(lay.x, lay.lora_a, sh.scale, m_sample, n, L,
@@ -233,17 +298,17 @@ def cpu_model() -> str:
 
 
 def cpu_baseline(wl: W.Workload, seconds: float = 10.0, f16: bool = False):
+    """The oracle on all host cores (and, for a quarter of the time, on one)."""
     import oracle
     threads = oracle.max_threads()
-    k = oracle_sample_size(wl, 2.0, threads, f16)
+    k = oracle_sample_size(wl, min(2.0, seconds / 2), threads, f16)
     tok, el, reps = 0, 0.0, 0
     while el < seconds and reps < 1000:
         t, dt = oracle_sample_step(wl, k, threads, f16)
         tok += t
         el += dt
         reps += 1
-    # one thread, for about a quarter of the time (its own sample size)
-    k1 = oracle_sample_size(wl, min(2.0, seconds / 4), 1, f16)
+    k1 = oracle_sample_size(wl, min(1.0, seconds / 8), 1, f16)
     tok1, el1 = 0, 0.0
     while el1 < seconds / 4 or tok1 == 0:
         t, dt = oracle_sample_step(wl, k1, 1, f16)
@@ -256,11 +321,12 @@ def cpu_baseline(wl: W.Workload, seconds: float = 10.0, f16: bool = False):
 
 
 def run_reference(args, world, rank):
+    """The oracle as the reference arm: rank 0 alone runs and prints."""
     if rank != 0:
         return 0
     import oracle
-    shape = W.CONFIGS[args.config]
-    wl = W.make_workload(shape, num_layers=1, seed=1000 + shape.index + 7919 * rank)
+    shape = W.CONFIGS[args.config if args.config != "all" else HEADLINE]
+    wl = W.make_workload(shape, num_layers=1, seed=1000 + shape.index)
     f16 = args.dtype == "f16"
     if f16:
         wl.layers = [W.layer_as_f16(l) for l in wl.layers]
@@ -278,10 +344,7 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": shape.name, "max_num_tokens": shape.max_num_tokens,
-                       "num_tokens": shape.num_tokens, "hidden": shape.hidden,
-                       "slice_widths": list(shape.slice_widths), "max_loras": shape.max_loras,
-                       "rank": shape.rank, "inputs": args.dtype},
+            "config": config_of(shape, args, device_l2_bytes(), world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "sample": f"first {k} of {shape.num_tokens} tokens per step"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -292,6 +355,283 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
+class WorkloadRun:
+    """One workload on the device: buffers, graphs and timings."""
+
+    def __init__(self, args, shape, dev, stream, rank, l2):
+        import torch
+
+        from gathered_rank_gemm_gb300 import binding
+        self.torch, self.binding = torch, binding
+        self.args, self.shape, self.dev, self.stream = args, shape, dev, stream
+        self.l2 = l2
+        self.layers = args.layers or layers_per_step(shape, l2)
+        self.seed = 1000 + shape.index + 7919 * rank
+        # one layer's values drawn on the host, held in `layers` distinct
+        # device buffers (distinct addresses are what the L2 sees)
+        wl = W.make_workload(shape, num_layers=1, seed=self.seed)
+        self.f16 = args.dtype == "f16"
+        if self.f16:
+            wl.layers = [W.layer_as_f16(l) for l in wl.layers]
+        self.wl = wl
+        T, L, n = shape.max_num_tokens, shape.max_loras, shape.num_tokens
+        dt16 = torch.float16 if self.f16 else torch.bfloat16
+        lay = wl.layers[0]
+
+        def dev16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt16)
+
+        # the larger workspace lets lora_shrink_expand take its split-K path
+        # (stacked weights only: the split-K halves have no paged form)
+        ws_bytes = (None if args.paged else
+                    binding.lora_shrink_expand_workspace_size(T, L, shape.hidden,
+                                                              shape.slice_widths, shape.rank))
+        self.meta = binding.LoraMetadata(T, L, dev, workspace_bytes=ws_bytes)
+        self.mapping = torch.from_numpy(wl.mapping).to(dev)
+        self.n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
+        x0, y0 = dev16(lay.x), dev16(lay.y)
+        self.xs = [x0] + [x0.clone() for _ in range(self.layers - 1)]
+        self.ys = [y0] + [y0.clone() for _ in range(self.layers - 1)]
+        a0 = [dev16(a) for a in lay.lora_a]
+        b0 = [dev16(b) for b in lay.lora_b]
+        self.As = [a0] + [[a.clone() for a in a0] for _ in range(self.layers - 1)]
+        self.Bs = [b0] + [[b.clone() for b in b0] for _ in range(self.layers - 1)]
+        if args.paged:
+            # every adapter's A_s[l] / B_s[l] viewed as its own page, found
+            # through one address table per layer and slice
+            self.A_tab = [[torch.tensor([a[l].data_ptr() for l in range(L)], dtype=torch.int64,
+                                        device=dev) for a in As] for As in self.As]
+            self.B_tab = [[torch.tensor([b[l].data_ptr() for l in range(L)], dtype=torch.int64,
+                                        device=dev) for b in Bs] for Bs in self.Bs]
+        self.scales = None
+        if args.lora_scales:
+            self.scales = torch.from_numpy(np.random.default_rng(self.seed + 1).uniform(0.5, 1.5, L)
+                                           .astype(np.float32)).to(dev)
+        self.us = [torch.zeros(shape.num_slices, T, shape.rank, dtype=torch.float32, device=dev)
+                   for _ in range(self.layers)]
+        torch.cuda.synchronize()
+        self.per_layer_kernels = (2 if args.paged else
+                                  binding.lora_shrink_expand_kernels(T, L, shape.hidden,
+                                                                     shape.slice_widths,
+                                                                     shape.rank))
+        self.split_k = False
+        self.graphs = {}
+
+    def launch(self, which):
+        """Enqueue one step's part: metadata, layers (one call each), or the
+        one-call path's shrink / expand kernels alone (one launch per layer)."""
+        m, sh, s = self.meta, self.shape, self.stream
+        if which == "metadata":
+            m.prepare(self.mapping, self.n_dev, s)
+            return
+        for k in range(self.layers):
+            if which == "layers":
+                if self.args.paged:
+                    m.shrink_expand_paged(self.xs[k], self.A_tab[k], self.B_tab[k],
+                                          sh.slice_widths, sh.scale, self.us[k], self.ys[k], s,
+                                          self.scales)
+                else:
+                    m.shrink_expand(self.xs[k], self.As[k], self.Bs[k], sh.scale, self.us[k],
+                                    self.ys[k], s, self.scales)
+            elif which == "shrink":
+                if self.args.paged:
+                    m.shrink_paged(self.xs[k], self.A_tab[k], sh.rank, sh.scale, self.us[k], s,
+                                   self.scales)
+                elif self.split_k:
+                    m.shrink_partials(self.xs[k], self.As[k], s)
+                else:
+                    m.shrink(self.xs[k], self.As[k], sh.scale, self.us[k], s, self.scales)
+            elif which == "expand":
+                if self.args.paged:
+                    m.expand_paged(self.us[k], self.B_tab[k], sh.slice_widths, self.ys[k], s)
+                elif self.split_k:
+                    m.expand_partials(sh.hidden, self.Bs[k], sh.scale, self.us[k], self.ys[k], s,
+                                      self.scales)
+                else:
+                    m.expand(self.us[k], self.Bs[k], self.ys[k], s)
+
+    def capture(self):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            self.launch("metadata")   # first calls per device set kernel attributes
+            self.launch("layers")     # outside any capture
+        self.stream.synchronize()
+        base = self.binding.lora_workspace_size(self.shape.max_num_tokens, self.shape.max_loras)
+        ws = self.meta.workspace
+        # the split-K path leaves its partial tiles behind the metadata part of
+        # the (zero-initialised) workspace
+        self.split_k = (self.per_layer_kernels == 2 and ws.numel() > base
+                        and bool(ws[base:].any().item()))
+        for which in ("metadata", "layers", "shrink", "expand"):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=self.stream):
+                self.launch(which)
+            self.graphs[which] = g
+
+    def time_graph(self, which, min_ms=50.0):
+        """Device ms per replay of one graph (CUDA events on the stream)."""
+        torch, g = self.torch, self.graphs[which]
+        with torch.cuda.stream(self.stream):
+            for _ in range(3):
+                g.replay()
+        self.stream.synchronize()
+        reps, total = 0, 0.0
+        while total < min_ms or reps < 10:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(self.stream)
+            with torch.cuda.stream(self.stream):
+                for _ in range(10):
+                    g.replay()
+            e1.record(self.stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+            reps += 10
+        return total / reps
+
+    def timed_steps(self, steps, world):
+        """Exactly `steps` steps, barrier + synchronize on both sides; returns
+        (ms per step, ms of the layers per step, ms of the grouping per step,
+        host window)."""
+        torch = self.torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        barrier(world)
+        torch.cuda.synchronize()
+        h0 = time.time()
+        with torch.cuda.stream(self.stream):
+            for e in ev:
+                e[0].record(self.stream)
+                self.graphs["metadata"].replay()
+                e[1].record(self.stream)
+                self.graphs["layers"].replay()
+                e[2].record(self.stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        h1 = time.time()
+        meta = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+        lay = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+        step = sum(e[0].elapsed_time(e[2]) for e in ev) / steps
+        return step, lay, meta, (h0, h1)
+
+    def measure(self, steps, warmup, min_ms, world):
+        torch = self.torch
+        with torch.cuda.stream(self.stream):
+            for _ in range(max(warmup, 3)):
+                self.graphs["metadata"].replay()
+                self.graphs["layers"].replay()
+        self.stream.synchronize()
+        reps, windows = [], []
+        spent = 0.0
+        while spent < min_ms or not reps:
+            step, lay, meta, win = self.timed_steps(steps, world)
+            reps.append((step, lay, meta))
+            windows.append(win)
+            spent += step * steps
+        self.windows = windows
+        self.reps = reps
+        med = sorted(reps, key=lambda r: r[0])[len(reps) // 2]
+        self.ms_step, self.ms_layers, self.ms_meta = med
+        self.timed_ms = spent
+        # each kernel of the layer on its own (graphs of `layers` launches)
+        self.ms_one = self.time_graph("layers") / self.layers
+        self.ms_shrink = self.time_graph("shrink") / self.layers
+        self.ms_expand = self.time_graph("expand") / self.layers
+        self.ms_meta_alone = self.time_graph("metadata")
+
+    def e2e(self, steps, world):
+        """Steps through the public API with host buffers: the step's inputs
+        copied from pinned host memory and every layer's y copied back."""
+        torch = self.torch
+        lay = self.wl.layers[0]
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        h_map = pin(self.wl.mapping)
+        h_n = pin(np.array([self.shape.num_tokens], np.int32))
+        h_x = pin(lay.x.view(np.int16))
+        h_y = pin(lay.y.view(np.int16))
+        h_out = [torch.empty_like(h_y).pin_memory() for _ in range(self.layers)]
+        h2d = h_map.numel() * 4 + 4 + self.layers * (h_x.numel() * 2 + h_y.numel() * 2)
+        d2h = self.layers * h_y.numel() * 2
+
+        def one():
+            with torch.cuda.stream(self.stream):
+                self.mapping.copy_(h_map, non_blocking=True)
+                self.n_dev.copy_(h_n, non_blocking=True)
+                for k in range(self.layers):
+                    self.xs[k].view(torch.int16).copy_(h_x, non_blocking=True)
+                    self.ys[k].view(torch.int16).copy_(h_y, non_blocking=True)
+                self.graphs["metadata"].replay()
+                self.graphs["layers"].replay()
+                for k in range(self.layers):
+                    h_out[k].copy_(self.ys[k].view(torch.int16), non_blocking=True)
+
+        for _ in range(2):
+            one()
+        self.stream.synchronize()
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        self.stream.synchronize()
+        ms = 1e3 * (time.perf_counter() - t0) / steps
+        barrier(world)
+        return ms, h2d, d2h
+
+    def record(self, peak, peak_kind, world, ms_layers_max, ms_step_max):
+        sh = self.shape
+        n, T, L = sh.num_tokens, sh.max_num_tokens, sh.max_loras
+        alg = algorithmic_bytes(sh, self.wl.mapping)
+        both = alg["shrink"] + alg["expand"]
+        if self.per_layer_kernels == 1:
+            dominant, kernel_name = "shrink_expand", "lora_fused_kernel"
+            dom_bytes, t_dom = both, self.ms_one
+        else:
+            dominant = "expand" if self.ms_expand >= self.ms_shrink else "shrink"
+            kernel_name = (f"lora_{dominant}_kernel" + (" (split-K)" if self.split_k else "")
+                           + (" (paged weights)" if self.args.paged else ""))
+            dom_bytes = alg[dominant]
+            t_dom = self.ms_expand if dominant == "expand" else self.ms_shrink
+        gbs = lambda b, ms: b / (ms * 1e-3) / 1e9
+        achieved = gbs(dom_bytes, t_dom)
+        ms_layer = ms_layers_max / self.layers
+        key = dominant + ("-split" if self.split_k else "") + ("-paged" if self.args.paged else "")
+        return {
+            "config": config_of(sh, self.args, self.l2, world),
+            "layers_per_step": self.layers,
+            "one_call_path": ("fused" if self.per_layer_kernels == 1
+                              else ("split-K" if self.split_k else "cluster")),
+            "kernels_per_layer": self.per_layer_kernels,
+            "tokens_per_s": n * self.layers * world / (ms_layers_max * 1e-3),
+            "tokens_per_s_with_metadata": n * self.layers * world / (ms_step_max * 1e-3),
+            "lora_tokens_per_s": alg["n_lora_tokens"] * self.layers * world / (ms_layers_max * 1e-3),
+            "lora_tokens": alg["n_lora_tokens"], "active_loras": alg["active_loras"],
+            "us": {"layer_in_step": 1e3 * ms_layer, "metadata_in_step": 1e3 * self.ms_meta,
+                   "metadata_alone": 1e3 * self.ms_meta_alone,
+                   "one_call": 1e3 * self.ms_one, "shrink": 1e3 * self.ms_shrink,
+                   "expand": 1e3 * self.ms_expand},
+            "algorithmic_bytes": {"shrink": alg["shrink"], "expand": alg["expand"]},
+            "hbm": {"peak_gbs": peak, "peak_source": peak_kind,
+                    "shrink_expand_gbs": gbs(both, ms_layer),
+                    "shrink_expand_frac": gbs(both, ms_layer) / peak,
+                    "one_call_frac": gbs(both, self.ms_one) / peak,
+                    "shrink_frac": gbs(alg["shrink"], self.ms_shrink) / peak,
+                    "expand_frac": gbs(alg["expand"], self.ms_expand) / peak},
+            "tflops": {"shrink": alg["flops"]["shrink"] / (self.ms_shrink * 1e-3) / 1e12,
+                       "expand": alg["flops"]["expand"] / (self.ms_expand * 1e-3) / 1e12},
+            "roofline": {"bound": "hbm", "kernel": kernel_name, "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": peak_kind, "frac_of_nominal_8tbs": achieved / 8000.0,
+                         "algorithmic_bytes_per_launch": dom_bytes,
+                         "traffic": recorded_traffic(key, sh.name)},
+            "timed": {"steps_per_repeat": self.args.steps,
+                      "repeats": len(self.reps), "ms": self.timed_ms,
+                      "ms_per_step_repeats": [r[0] for r in self.reps]},
+        }
+
+    def free(self):
+        self.graphs.clear()
+        for name in ("xs", "ys", "As", "Bs", "us", "meta", "mapping", "n_dev"):
+            setattr(self, name, None)
+
+
 def run_ours(args, world, rank, local):
     import torch
 
@@ -299,292 +639,146 @@ def run_ours(args, world, rank, local):
     from gathered_rank_gemm_gb300 import build as B
 
     if not torch.cuda.is_available():
-        print(json.dumps({"error": "no CUDA device"}))
+        print(json.dumps({"error": "no CUDA device: the library has no CPU path"}))
+        return 1
+    if args.paged and args.dtype == "f16":
+        print(json.dumps({"error": "paged weights are bf16 only"}))
         return 1
     B.build()
     binding.load()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    shape = W.CONFIGS[args.config]
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_layer = (shape.max_num_tokens * (shape.hidden + shape.out_width) * 2
-                 + sum(shape.max_loras * shape.rank * (shape.hidden + w) * 2
-                       for w in shape.slice_widths)
-                 + 4 * shape.num_slices * shape.max_num_tokens * shape.rank)
-    layers = args.layers or max(1, math.ceil(2 * l2 / per_layer))
-    seed = 1000 + shape.index + 7919 * rank
-    wl = W.make_workload(shape, num_layers=layers, seed=seed)
-    T, L, n = shape.max_num_tokens, shape.max_loras, shape.num_tokens
-    f16 = args.dtype == "f16"
-    if f16:
-        if args.paged:
-            print(json.dumps({"error": "paged weights are bf16 only"}))
-            return 1
-        # the same draws rounded to fp16; the *_f16 entry points run them
-        wl.layers = [W.layer_as_f16(l) for l in wl.layers]
-    dt16 = torch.float16 if f16 else torch.bfloat16
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(dt16)
-
+    names = ORDER if args.config == "all" else (args.config,)
+    headline = HEADLINE if args.config == "all" else args.config
+    peak, peak_kind = load_peaks()
     stream = torch.cuda.Stream(dev)
-    # the larger workspace lets lora_shrink_expand take its split-K path (stacked
-    # weights only: the split-K halves have no paged form, so paged runs time
-    # the cluster-path kernels their one call runs)
-    ws_bytes = (None if args.paged else
-                binding.lora_shrink_expand_workspace_size(T, L, shape.hidden, shape.slice_widths,
-                                                          shape.rank))
-    meta = binding.LoraMetadata(T, L, dev, workspace_bytes=ws_bytes)
-    mapping = torch.from_numpy(wl.mapping).to(dev)
-    n_dev = torch.tensor([n], dtype=torch.int32, device=dev)
-    xs = [bf16(l.x) for l in wl.layers]
-    ys = [bf16(l.y) for l in wl.layers]
-    if args.paged:
-        # every adapter's A_s[l] / B_s[l] in its own allocation, found through
-        # one address table per layer and slice
-        pages = []
-        A_tab, B_tab = [], []
-        for l in wl.layers:
-            ta, tb = [], []
-            for s_ in range(shape.num_slices):
-                pa = [bf16(l.lora_a[s_][a]) for a in range(L)]
-                pb = [bf16(l.lora_b[s_][a]) for a in range(L)]
-                pages += pa + pb
-                ta.append(torch.tensor([t.data_ptr() for t in pa], dtype=torch.int64, device=dev))
-                tb.append(torch.tensor([t.data_ptr() for t in pb], dtype=torch.int64, device=dev))
-            A_tab.append(ta)
-            B_tab.append(tb)
-    else:
-        As = [[bf16(a) for a in l.lora_a] for l in wl.layers]
-        Bs = [[bf16(b) for b in l.lora_b] for l in wl.layers]
-    scales = None
-    if args.lora_scales:
-        scales = torch.from_numpy(np.random.default_rng(seed + 1).uniform(0.5, 1.5, L)
-                                  .astype(np.float32)).to(dev)
-    us = [torch.zeros(shape.num_slices, T, shape.rank, dtype=torch.float32, device=dev)
-          for _ in wl.layers]
-    torch.cuda.synchronize()
-
-    # per layer, one lora_shrink_expand call: one fused kernel when the batch
-    # fits on chip, else the shrink and expand kernels back to back
-    per_layer_kernels = (2 if args.paged else
-                         binding.lora_shrink_expand_kernels(T, L, shape.hidden,
-                                                            shape.slice_widths, shape.rank))
-
-    # which kernels lora_shrink_expand runs here: the split-K path leaves its
-    # partial tiles behind the metadata part of the (zero-initialised) workspace
-    split_k = False
-
-    def step(which="all"):
-        if which in ("all", "metadata", "profile"):
-            meta.prepare(mapping, n_dev, stream)
-        for k in range(layers):
-            if which in ("all", "one_call", "profile"):
-                if args.paged:
-                    meta.shrink_expand_paged(xs[k], A_tab[k], B_tab[k], shape.slice_widths,
-                                             shape.scale, us[k], ys[k], stream, scales)
-                else:
-                    meta.shrink_expand(xs[k], As[k], Bs[k], shape.scale, us[k], ys[k], stream,
-                                       scales)
-            # the kernels of the one call, timed one launch at a time
-            if which == "shrink":
-                if args.paged:
-                    meta.shrink_paged(xs[k], A_tab[k], shape.rank, shape.scale, us[k], stream,
-                                      scales)
-                elif split_k:
-                    meta.shrink_partials(xs[k], As[k], stream)
-                else:
-                    meta.shrink(xs[k], As[k], shape.scale, us[k], stream, scales)
-            if which == "expand":
-                if args.paged:
-                    meta.expand_paged(us[k], B_tab[k], shape.slice_widths, ys[k], stream)
-                elif split_k:
-                    meta.expand_partials(shape.hidden, Bs[k], shape.scale, us[k], ys[k], stream,
-                                         scales)
-                else:
-                    meta.expand(us[k], Bs[k], ys[k], stream)
-
-    graphs = {}
-    with torch.cuda.stream(stream):
-        step()  # first call per device sets kernel attributes outside capture
-    stream.synchronize()
-    ws_base = binding.lora_workspace_size(T, L)
-    split_k = (per_layer_kernels == 2 and meta.workspace.numel() > ws_base and
-               bool(meta.workspace[ws_base:].any().item()))
-    if args.mode == "profile":
-        for _ in range(args.steps):
-            with torch.cuda.stream(stream):
-                step()
-        stream.synchronize()
-        if rank == 0:
-            print(json.dumps({"mode": "profile", "workload": shape.name, "layers": layers,
-                              "steps": args.steps, "launches": (1 + 2 * layers) * (args.steps + 1)}))
-        return 0
-    for which in ("all", "metadata", "one_call", "shrink", "expand"):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            step(which)
-        graphs[which] = g
-
-    def time_graph(g, reps, warm):
-        with torch.cuda.stream(stream):
-            for _ in range(warm):
-                g.replay()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        with torch.cuda.stream(stream):
-            for _ in range(reps):
-                g.replay()
-        e1.record(stream)
-        e1.synchronize()
-        return e0.elapsed_time(e1) / reps  # ms per replay
-
-    # ---- timed region: K steps, barrier + synchronize on both sides
-    for _ in range(max(args.warmup, 3)):
-        with torch.cuda.stream(stream):
-            graphs["all"].replay()
-    stream.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(args.steps):
-            graphs["all"].replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    ms_step = e0.elapsed_time(e1) / args.steps
-    # per-kernel launch times (each graph launches that kernel `layers` times)
-    ms_meta = time_graph(graphs["metadata"], args.steps, 3)
-    ms_one = time_graph(graphs["one_call"], args.steps, 3) / layers
-    ms_shrink = time_graph(graphs["shrink"], args.steps, 3) / layers
-    ms_expand = time_graph(graphs["expand"], args.steps, 3) / layers
-    clk = clocks.stop()
-    ms_step_max = max_over_ranks(ms_step, world, dev)
-
-    # ---- end to end through the public API with host buffers
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_map = pin(wl.mapping)
-    h_n = pin(np.array([n], np.int32))
-    h_x = [pin(l.x.view(np.int16)) for l in wl.layers]
-    h_y = [pin(l.y.view(np.int16)) for l in wl.layers]
-    h_out = [torch.empty_like(h) .pin_memory() for h in h_y]
-    h2d = h_map.numel() * 4 + 4 + sum(h.numel() * 2 for h in h_x) + sum(h.numel() * 2 for h in h_y)
-    d2h = sum(h.numel() * 2 for h in h_y)
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            mapping.copy_(h_map, non_blocking=True)
-            n_dev.copy_(h_n, non_blocking=True)
-            for k in range(layers):
-                xs[k].view(torch.int16).copy_(h_x[k], non_blocking=True)
-                ys[k].view(torch.int16).copy_(h_y[k], non_blocking=True)
-            graphs["all"].replay()
-            for k in range(layers):
-                h_out[k].copy_(ys[k].view(torch.int16), non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    stream.synchronize()
-    barrier(world)
-    e2e_steps = max(3, min(args.steps, 20))
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    stream.synchronize()
-    ms_e2e = 1e3 * (time.perf_counter() - t0) / e2e_steps
-    barrier(world)
-    ms_e2e = max_over_ranks(ms_e2e, world, dev)
-
-    alg = algorithmic_bytes(shape, wl.mapping)
-    peak, peak_kind = load_peaks()
-    if per_layer_kernels == 1:
-        # one fused kernel per layer: it moves the bytes of both steps
-        dominant, kernel_name = "shrink_expand", "lora_fused_kernel"
-        dom_bytes, t_dom = alg["shrink"] + alg["expand"], ms_one
-    else:
-        # the kernel that takes the larger share of the layer's device time
-        dominant = "expand" if ms_expand >= ms_shrink else "shrink"
-        kernel_name = (f"lora_{dominant}_kernel" + (" (split-K)" if split_k else "")
-                       + (" (paged weights)" if args.paged else ""))
-        dom_bytes = alg[dominant]
-        t_dom = ms_expand if dominant == "expand" else ms_shrink
-    achieved = dom_bytes / (t_dom * 1e-3) / 1e9
-    value = n * layers * world / (ms_step_max * 1e-3)
-    e2e_value = n * layers * world / (ms_e2e * 1e-3)
-    launches = (1 + per_layer_kernels * layers) * args.steps
-
-    result = None
-    if rank == 0:
-        cpu = cpu_baseline(wl, seconds=args.cpu_seconds, f16=f16) if world == 1 else None
-        result = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
-            "data": "synthetic",
-            "config": {"workload": shape.name, "max_num_tokens": T, "num_tokens": n,
-                       "hidden": shape.hidden, "slice_widths": list(shape.slice_widths),
-                       "max_loras": L, "rank": shape.rank, "layers_per_step": layers,
-                       "l2": f"inputs larger than L2: {layers} distinct layers, "
-                             f"{layers * per_layer / 1e6:.0f} MB per step vs {l2 / 1e6:.0f} MB L2",
-                       "graph": "one CUDA graph per step: grouping, then one lora_shrink_expand call per layer",
-                       "parallelism": f"replicas x{world} (independent batches, no collective)",
-                       "weights": "paged" if args.paged else "stacked",
-                       "lora_scales": bool(args.lora_scales)},
-            "roofline": {"bound": "hbm", "kernel": kernel_name,
-                         "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "peak_source": peak_kind,
-                         "frac_of_nominal_8tbs": achieved / 8000.0,
-                         "algorithmic_bytes_per_launch": dom_bytes,
-                         "traffic": recorded_traffic(dominant + ("-split" if split_k else "")
-                                                     + ("-paged" if args.paged else ""),
-                                                     shape.name)},
-            "kernels_per_layer": per_layer_kernels,
-            "one_call_path": "fused" if per_layer_kernels == 1 else ("split-K" if split_k else "cluster"),
-            "kernels_us": {"metadata": 1e3 * ms_meta, "shrink_expand_one_call": 1e3 * ms_one,
-                           "shrink": 1e3 * ms_shrink, "expand": 1e3 * ms_expand,
-                           "layer_in_graph": 1e3 * ms_step / layers},
-            "hbm_gbs": {"shrink": alg["shrink"] / (ms_shrink * 1e-3) / 1e9,
-                        "expand": alg["expand"] / (ms_expand * 1e-3) / 1e9,
-                        "shrink_expand_one_call": (alg["shrink"] + alg["expand"]) / (ms_one * 1e-3) / 1e9,
-                        "layer": (alg["shrink"] + alg["expand"]) / (ms_step / layers * 1e-3) / 1e9},
-            "tflops": {"shrink": alg["flops"]["shrink"] / (ms_shrink * 1e-3) / 1e12,
-                       "expand": alg["flops"]["expand"] / (ms_expand * 1e-3) / 1e12},
-            "lora_tokens": alg["n_lora_tokens"], "active_loras": alg["active_loras"],
-            "lora_tokens_per_s": alg["n_lora_tokens"] * layers * world / (ms_step_max * 1e-3),
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
-            "gpu_launches": launches,
-            "clocks": clk,
-        }
-        print(json.dumps(result), flush=True)
+    records, head = {}, None
+    try:
+        for name in names:
+            run = WorkloadRun(args, W.CONFIGS[name], dev, stream, rank, l2)
+            run.capture()
+            # the headline is timed longer, so the clock record has tens of samples
+            min_ms = args.min_timed_ms * (5.0 if name == headline else 1.0)
+            run.measure(args.steps, args.warmup, min_ms, world)
+            ms_layers = max_over_ranks(run.ms_layers, world, dev)
+            ms_step = max_over_ranks(run.ms_step, world, dev)
+            rec = run.record(peak, peak_kind, world, ms_layers, ms_step)
+            rec["clocks"] = clocks.summary(run.windows)
+            if name == headline:
+                ms_e2e, h2d, d2h = run.e2e(max(3, min(args.steps, 10)), world)
+                ms_e2e = max_over_ranks(ms_e2e, world, dev)
+                rec["e2e"] = {"value": run.shape.num_tokens * run.layers * world / (ms_e2e * 1e-3),
+                              "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                              "ms_per_step": ms_e2e}
+                head = (run, ms_layers, ms_step)
+            rec["_wl"] = run.wl
+            records[name] = rec
+            run.free()
+            torch.cuda.empty_cache()
+    finally:
+        clocks.stop()
+    if rank != 0:
+        return 0
+    # the oracle on the host cores, a bounded sample of each workload
+    for name, rec in records.items():
+        wl = rec.pop("_wl")
+        if world == 1:
+            secs = args.cpu_seconds if name == headline else max(1.0, args.cpu_seconds / 4)
+            rec["cpu_baseline"] = cpu_baseline(wl, seconds=secs, f16=args.dtype == "f16")
+        else:
+            rec["cpu_baseline"] = None
+    run, ms_layers, ms_step = head
+    h = records[headline]
+    result = {
+        "metric": METRIC, "value": h["tokens_per_s"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": args.dtype,
+        "data": "synthetic",
+        "config": h["config"],
+        "value_with_metadata": h["tokens_per_s_with_metadata"],
+        "ms_layers_per_step": ms_layers,
+        "roofline": h["roofline"],
+        "shrink_expand_frac": h["hbm"]["shrink_expand_frac"],
+        "cpu_baseline": h["cpu_baseline"],
+        "e2e": h.pop("e2e"),
+        # this library's kernels in the headline's timed region: the grouping
+        # and the kernels of every layer's call, per step
+        "gpu_launches": h["timed"]["repeats"] * args.steps * (1 + h["kernels_per_layer"]
+                                                              * h["layers_per_step"]),
+        "timed": h["timed"],
+        "clocks": h["clocks"],
+        "clocks_all_workloads": clocks.summary(None),
+        "per_workload": records,
+    }
+    print(json.dumps(result), flush=True)
     return 0
 
 
-def main(argv=None):
+def _spawn_ranks(argv, n):
+    """One process per GPU (rank = local rank), launched here when no
+    launcher set WORLD_SIZE; returns the worst exit code."""
+    import torch.multiprocessing as mp
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_rank_main, args=(argv, r, n, port)) for r in range(n)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join()
+    return max(abs(p.exitcode or 0) for p in procs)
+
+
+def _rank_main(argv, rank, world, port):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.exit(main(argv))
+
+
+def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=list(W.CONFIGS), default="decode_qkv")
-    ap.add_argument("--layers", type=int, default=0, help="layers per step (0: >= 2x L2)")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--config", choices=["all"] + list(W.CONFIGS), default="all",
+                    help="one workload, or all five (headline: down_proj_graph)")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="layers per step (0: at least 4 and more than 2x L2)")
+    ap.add_argument("--min-timed-ms", type=float, default=200.0,
+                    help="repeat the timed --steps steps until a workload was timed this long")
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--paged", action="store_true",
                     help="adapter weights as per-adapter pages found through address tables")
     ap.add_argument("--lora-scales", action="store_true", help="per-adapter scale factors")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="type of x, A, B and y (fp32 accumulation either way)")
-    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
-                    help="profile: only run --steps eager steps (for ncu launch lists)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 0)
+    return args
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        if args.impl == "ours":
+            import torch
+            have = torch.cuda.device_count() if torch.cuda.is_available() else 0
+            if have < args.gpus:
+                print(json.dumps({"error": f"--gpus {args.gpus} needs {args.gpus} CUDA devices, "
+                                           f"{have} visible"}), flush=True)
+                return 1
+        return _spawn_ranks(sys.argv[1:] if argv is None else list(argv), args.gpus)
     world, rank, local = dist_setup(args)
+    if args.gpus != world:
+        if rank == 0:
+            print(json.dumps({"error": f"--gpus {args.gpus} but the launcher started {world} "
+                                       "ranks"}), flush=True)
+        return 1
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)

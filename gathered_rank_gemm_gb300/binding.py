@@ -103,6 +103,24 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     return lib
 
 
+def _on_tensor_device(fn):
+    """Runs a C-ABI call with the device of its first CUDA tensor argument
+    current: the library launches on, and looks its per-device state up for,
+    the current device."""
+    import functools
+
+    @functools.wraps(fn)
+    def wrapped(*args, **kwargs):
+        import torch
+        for a in list(args) + list(kwargs.values()):
+            t = a[0] if isinstance(a, (list, tuple)) and a else a
+            if isinstance(t, torch.Tensor) and t.is_cuda:
+                with torch.cuda.device(t.device):
+                    return fn(*args, **kwargs)
+        return fn(*args, **kwargs)
+    return wrapped
+
+
 def _check(name: str, rc: int) -> None:
     if rc != LORA_OK:
         raise LoraError(name, rc, load().lora_error_string(rc).decode())
@@ -156,6 +174,7 @@ def lora_workspace_size(max_num_tokens: int, max_loras: int) -> int:
     return int(load().lora_workspace_size(int(max_num_tokens), int(max_loras)))
 
 
+@_on_tensor_device
 def lora_prepare_metadata(token_lora_mapping, num_tokens, max_loras: int, sorted_token_ids,
                           num_tokens_per_lora, lora_token_start_loc, workspace, stream=None):
     """Stable grouping of the tokens by LoRA id (see the C header)."""
@@ -169,6 +188,7 @@ def lora_prepare_metadata(token_lora_mapping, num_tokens, max_loras: int, sorted
     _check("lora_prepare_metadata", rc)
 
 
+@_on_tensor_device
 def lora_shrink(x, lora_a, scale: float, u, sorted_token_ids, lora_token_start_loc, workspace,
                 stream=None, lora_scales=None):
     """u[s][t][r] = scale (* lora_scales[m[t]]) * x[t] . A_s[m[t]][r] for the adapter tokens."""
@@ -185,6 +205,7 @@ def lora_shrink(x, lora_a, scale: float, u, sorted_token_ids, lora_token_start_l
     _check("lora_shrink", rc)
 
 
+@_on_tensor_device
 def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace, stream=None):
     """y[t][off_s + j] += u[s][t] . B_s[m[t]][:, j] for the adapter tokens (in place)."""
     lora_b = list(lora_b)
@@ -201,6 +222,7 @@ def lora_expand(u, lora_b, y, sorted_token_ids, lora_token_start_loc, workspace,
     _check("lora_expand", rc)
 
 
+@_on_tensor_device
 def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
                        lora_token_start_loc, workspace, stream=None, lora_scales=None):
     """Shrink then expand in one call (one fused kernel for decode-sized batches)."""
@@ -222,6 +244,7 @@ def lora_shrink_expand(x, lora_a, lora_b, scale: float, u, y, sorted_token_ids,
     _check("lora_shrink_expand", rc)
 
 
+@_on_tensor_device
 def lora_shrink_partials(x, lora_a, sorted_token_ids, lora_token_start_loc, workspace,
                          stream=None):
     """Split-K shrink: each CTA's partial tile of u into the workspace (u is not written)."""
@@ -238,6 +261,7 @@ def lora_shrink_partials(x, lora_a, sorted_token_ids, lora_token_start_loc, work
     _check("lora_shrink_partials", rc)
 
 
+@_on_tensor_device
 def lora_expand_partials(hidden: int, lora_b, scale: float, u, y, sorted_token_ids,
                          lora_token_start_loc, workspace, stream=None, lora_scales=None):
     """Sums the split-K partials (scaled) into u, then y += u . B_s (in place)."""
@@ -266,6 +290,7 @@ def _table_array(tables, name):
     return _ptr_array(tables, name)
 
 
+@_on_tensor_device
 def lora_shrink_paged(x, a_tables, rank: int, scale: float, u, sorted_token_ids,
                       lora_token_start_loc, workspace, stream=None, lora_scales=None):
     """lora_shrink with paged adapter weights: a_tables[s][l] = address of A_s[l] ([rank][hidden])."""
@@ -283,6 +308,7 @@ def lora_shrink_paged(x, a_tables, rank: int, scale: float, u, sorted_token_ids,
     _check("lora_shrink_paged", rc)
 
 
+@_on_tensor_device
 def lora_expand_paged(u, b_tables, slice_widths, y, sorted_token_ids, lora_token_start_loc,
                       workspace, stream=None):
     """lora_expand with paged adapter weights: b_tables[s][l] = address of B_s[l] ([rank][N_s])."""
@@ -300,6 +326,7 @@ def lora_expand_paged(u, b_tables, slice_widths, y, sorted_token_ids, lora_token
     _check("lora_expand_paged", rc)
 
 
+@_on_tensor_device
 def lora_shrink_expand_paged(x, a_tables, b_tables, slice_widths, scale: float, u, y,
                              sorted_token_ids, lora_token_start_loc, workspace, stream=None,
                              lora_scales=None):
@@ -341,6 +368,7 @@ def lora_shrink_expand_workspace_size(max_num_tokens: int, max_loras: int, hidde
         len(slice_widths), int(rank)))
 
 
+@_on_tensor_device
 def lora_read_status(workspace, stream=None) -> int:
     """Status bits OR-ed since the last read (synchronises the stream, clears them)."""
     out = ctypes.c_uint32(0)
@@ -350,6 +378,7 @@ def lora_read_status(workspace, stream=None) -> int:
     return int(out.value)
 
 
+@_on_tensor_device
 def lora_apply_noalloc(token_lora_mapping, num_tokens, x, lora_a, lora_b, scale: float, u, y,
                        sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
                        status=None, stream=None, lora_scales=None):

@@ -263,10 +263,14 @@ int lora_expand_partials_f16(int64_t hidden, const uint16_t* const* lora_b,
                          max_loras, workspace, workspace_bytes, stream, false, true);
 }
 
-int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
-                          int64_t max_num_tokens, int64_t max_loras, int32_t* sorted_token_ids,
-                          int32_t* num_tokens_per_lora, int32_t* lora_token_start_loc,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks of lora_prepare_metadata.
+int metadata_args(const int32_t* token_lora_mapping, const int32_t* num_tokens,
+                  int64_t max_num_tokens, int64_t max_loras, const int32_t* sorted_token_ids,
+                  const int32_t* num_tokens_per_lora, const int32_t* lora_token_start_loc,
+                  const void* workspace, size_t workspace_bytes) {
   if (!token_lora_mapping || !num_tokens || !sorted_token_ids || !num_tokens_per_lora ||
       !lora_token_start_loc || !workspace)
     return LORA_ERR_NULL;
@@ -279,6 +283,48 @@ int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_
     return LORA_ERR_ALIGN;
   if (workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
     return LORA_ERR_WORKSPACE;
+  return LORA_OK;
+}
+}  // namespace
+
+namespace grg {
+// Every argument check of lora_prepare_metadata, lora_shrink and lora_expand
+// for one layer, without launching anything.
+__attribute__((visibility("hidden"))) int check_layer_args(
+    const int32_t* token_lora_mapping, const int32_t* num_tokens,
+                     int64_t max_num_tokens, int64_t max_loras, const uint16_t* x,
+                     int64_t x_row_stride, int64_t hidden, const uint16_t* const* lora_a,
+                     const uint16_t* const* lora_b, const int64_t* slice_width, int num_slices,
+                     int rank, float* u, uint16_t* y, int64_t y_row_stride,
+                     const int32_t* sorted_token_ids, const int32_t* num_tokens_per_lora,
+                     const int32_t* lora_token_start_loc, const void* workspace,
+                     size_t workspace_bytes) {
+  int rc = metadata_args(token_lora_mapping, num_tokens, max_num_tokens, max_loras,
+                         sorted_token_ids, num_tokens_per_lora, lora_token_start_loc, workspace,
+                         workspace_bytes);
+  if (rc != LORA_OK) return rc;
+  ShrinkArgs sa;
+  rc = shrink_args(x, x_row_stride, hidden, lora_a, nullptr, num_slices, rank, 1.0f, nullptr, u,
+                   sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras, workspace,
+                   workspace_bytes, &sa);
+  if (rc != LORA_OK) return rc;
+  ExpandArgs ea;
+  return expand_args(u, lora_b, nullptr, slice_width, num_slices, rank, y, y_row_stride,
+                     sorted_token_ids, lora_token_start_loc, max_num_tokens, max_loras,
+                     workspace, workspace_bytes, &ea);
+}
+}  // namespace grg
+
+extern "C" {
+
+int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_tokens,
+                          int64_t max_num_tokens, int64_t max_loras, int32_t* sorted_token_ids,
+                          int32_t* num_tokens_per_lora, int32_t* lora_token_start_loc,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = metadata_args(token_lora_mapping, num_tokens, max_num_tokens, max_loras,
+                               sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
+                               workspace, workspace_bytes);
+  if (rc != LORA_OK) return rc;
   return grg::launch_metadata(token_lora_mapping, num_tokens, static_cast<int>(max_num_tokens),
                               static_cast<int>(max_loras), sorted_token_ids, num_tokens_per_lora,
                               lora_token_start_loc, workspace, static_cast<cudaStream_t>(stream));

@@ -14,9 +14,10 @@
 //  - the gathered 256-column segments of y and the gathered rows of u with
 //    16-byte cp.async (rows padded so the epilogue hits distinct banks).
 // Ranks up to 32 use two stages, so the next item's copies fly while the
-// current one is computed.  Before griddepcontrol.wait only metadata and
-// weights are fetched (the first record and B block) and the first y rows
-// are prefetched into L2; u and y are copied after it.
+// current one is computed.  Before griddepcontrol.wait only the first tile
+// records are copied and the first B block and y rows are prefetched into
+// L2; B, u and y are copied after it - except directly after this library's
+// shrink in the one-call paths, where B and y load before the wait.
 //
 // Compute: four warps, 64 columns each; per 16-token m-tile a warp runs
 // mma.sync m16n8k16 (bf16 operands, fp32 accumulate) of the u rows against B.
@@ -113,7 +114,13 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   const int nloc = static_cast<int>(blockIdx.x) < nitems
                        ? (nitems - 1 - static_cast<int>(blockIdx.x)) / G + 1
                        : 0;
-  if (nloc <= 0) return;  // this CTA writes nothing
+  if (nloc <= 0) {
+    // this CTA writes nothing, but still waits: the grid must not complete
+    // (and so release the next kernel's wait) before the kernel ahead of it has
+    pdl_wait();
+    pdl_launch_dependents();
+    return;
+  }
 
   if (tid == 0) {
     for (int s = 0; s < NS + RS; ++s) mbar_init(stage_bar + 8 * s, 1);
@@ -248,16 +255,17 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     issue_u(k);
   };
 
-  // prologue: the records of the first items and the first B block before the
-  // dependency wait (metadata and weights), the activations after it
+  // prologue: the records of the first items (lora_prepare_metadata's output,
+  // visible before it released its dependents) before the dependency wait
   const int npro = min(nloc, NS);
   if (tid == 0) {
     for (int k = 0; k < min(nloc, RS); ++k) issue_rec(k);
   }
   if (p.y_early) {
-    // y is not written by the preceding shrink, and every kernel before that
-    // one had completed when the shrink triggered this launch: the first
-    // items' y segments load before the dependency wait, u / partials after
+    // Directly after this library's shrink of the same call: that kernel
+    // writes neither B nor y and released this launch only after its own
+    // dependency wait, so every kernel before it has completed.  The first
+    // items' B blocks and y segments load before the wait, u / partials after
     for (int k = 0; k < npro; ++k) {
       wait_rec(k);
       if (tid == 0) issue_b(k);
@@ -267,13 +275,21 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     pdl_launch_dependents();
     for (int k = 0; k < npro; ++k) issue_u(k);
   } else {
+    // The kernel ahead on the stream may still be writing any input: before
+    // the wait only L2 prefetches (L2 is the coherence point, so the copies
+    // after the wait read the final values) of item 0's B block and y rows
     wait_rec(0);
-    if (tid == 0) issue_b(0);
     {
-      // warm L2 (and the TLB) with item 0's y rows while the previous kernel finishes
       const Item it = item_of(0);
       const int32_t* rec = rec_of(0);
       const TileView tv = TileView::of(rec, BM, p.num_loras);
+      if constexpr (!PAGED) {
+        if (tid == 0) {
+          const int boxes = min(4, (it.width - it.c0 + 63) / 64);
+          for (int b = 0; b < boxes; ++b)
+            tma_prefetch_2d(&p.tmap[it.s], it.c0 + 64 * b, tv.lora * RANK);
+        }
+      }
       const int bytes = min(kEN, it.width - it.c0) * 2;
       for (int r = tid; r < tv.count; r += kExpandThreads) {
         const int t = record_token(rec, r, tv.count, p.max_num_tokens);
@@ -283,6 +299,7 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     }
     pdl_wait();
     pdl_launch_dependents();
+    if (tid == 0) issue_b(0);
     issue_uy(0);
     for (int k = 1; k < npro; ++k) {
       wait_rec(k);

@@ -18,8 +18,9 @@
 //    requested together with x, so the whole read traffic of the layer is in
 //    flight at once; u enters the tensor cores as bf16 high + residual terms,
 //    y is added in fp32, rounded once and stored with 16-byte stores.
-// Before griddepcontrol.wait only the record and the weights (A, B) are
-// fetched and the x / y rows are prefetched into L2.
+// Before griddepcontrol.wait a CTA only reads its tile record and prefetches
+// its weight blocks (A, B) and x / y rows into L2; every copy into shared
+// memory comes after the wait.
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -125,26 +126,21 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const TileView tv = TileView::of(rec, kFBM, p.num_loras);
     const int lora = tv.lora, cnt = tv.count;
 
-    // weights (A blocks of this CTA's k-range, B blocks of its units) by TMA
-    if (tid == 0) {
-      for (int i = 0; i < nkb; ++i) {
-        mbar_arrive_expect_tx(bar_a + 8 * i, static_cast<uint32_t>(SR * 128));
-        for (int s = 0; s < p.num_slices; ++s)
-          tma_load_2d(sbase + p.off_a + i * SR * 128 + s * R * 128, &p.amap[s], (kb0 + i) * 64,
-                      lora * R, bar_a + 8 * i);
-      }
-      if (nun > 0) {
-        mbar_arrive_expect_tx(bar_b, static_cast<uint32_t>(nun * R * 128));
+    if (!waited) {
+      // The kernel ahead on the stream may still be writing any input:
+      // before the wait only L2 prefetches (L2 is the coherence point, so the
+      // copies after the wait read the final values) of this CTA's weight
+      // blocks and x / y rows
+      if (tid == 0) {
+        for (int i = 0; i < nkb; ++i)
+          for (int s = 0; s < p.num_slices; ++s)
+            tma_prefetch_2d(&p.amap[s], (kb0 + i) * 64, lora * R);
         for (int j = 0; j < nun; ++j) {
           const int unit = un0 + j;
           const int s = unit_slice(unit);
-          tma_load_2d(sbase + p.off_b + j * R * 128, &p.bmap[s], (unit - p.unit_start[s]) * 64,
-                      lora * R, bar_b);
+          tma_prefetch_2d(&p.bmap[s], (unit - p.unit_start[s]) * 64, lora * R);
         }
       }
-    }
-    if (!waited) {
-      // warm L2 with this CTA's x and y rows while the previous kernel finishes
       for (int r = tid; r < cnt; r += kFusedThreads) {
         const int t = record_token(rec, r, cnt, p.max_num_tokens);
         if (t < 0) continue;
@@ -163,6 +159,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       pdl_wait();
       pdl_launch_dependents();
       waited = true;
+    }
+    // weights (A blocks of this CTA's k-range, B blocks of its units) by TMA
+    if (tid == 0) {
+      for (int i = 0; i < nkb; ++i) {
+        mbar_arrive_expect_tx(bar_a + 8 * i, static_cast<uint32_t>(SR * 128));
+        for (int s = 0; s < p.num_slices; ++s)
+          tma_load_2d(sbase + p.off_a + i * SR * 128 + s * R * 128, &p.amap[s], (kb0 + i) * 64,
+                      lora * R, bar_a + 8 * i);
+      }
+      if (nun > 0) {
+        mbar_arrive_expect_tx(bar_b, static_cast<uint32_t>(nun * R * 128));
+        for (int j = 0; j < nun; ++j) {
+          const int unit = un0 + j;
+          const int s = unit_slice(unit);
+          tma_load_2d(sbase + p.off_b + j * R * 128, &p.bmap[s], (unit - p.unit_start[s]) * 64,
+                      lora * R, bar_b);
+        }
+      }
     }
     // activations: x rows of the k-range (group 1), y segments of the units (group 2)
     for (int c = tid; c < nkb * kFBM * 8; c += kFusedThreads) {
@@ -363,6 +377,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     phase ^= 1u;
     fence_proxy_async();  // generic smem use before the next item's TMA writes
     cluster_sync_all();   // remote reads of red[] are done before it is reused or freed
+  }
+  if (!waited) {
+    // a cluster without a tile still waits: the grid must not complete (and
+    // so release the next kernel's wait) before the kernel ahead of it has
+    pdl_wait();
+    pdl_launch_dependents();
   }
   if (timed_out) atomicOr(p.status, kStatusTimeout);
 }

@@ -108,4 +108,16 @@ int launch_fused(const ShrinkArgs& s, const ExpandArgs& e, cudaStream_t stream);
 int fused_fits(int max_num_tokens, int num_loras, int hidden, const int* widths, int num_slices,
                int rank);
 
+// Every argument check of lora_prepare_metadata, lora_shrink and lora_expand
+// for one layer (bf16, stacked weights), without launching anything: LORA_OK
+// or the LORA_ERR_* code the first failing call would return.
+int check_layer_args(const int32_t* token_lora_mapping, const int32_t* num_tokens,
+                     int64_t max_num_tokens, int64_t max_loras, const uint16_t* x,
+                     int64_t x_row_stride, int64_t hidden, const uint16_t* const* lora_a,
+                     const uint16_t* const* lora_b, const int64_t* slice_width, int num_slices,
+                     int rank, float* u, uint16_t* y, int64_t y_row_stride,
+                     const int32_t* sorted_token_ids, const int32_t* num_tokens_per_lora,
+                     const int32_t* lora_token_start_loc, const void* workspace,
+                     size_t workspace_bytes);
+
 }  // namespace grg

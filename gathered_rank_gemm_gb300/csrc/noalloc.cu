@@ -57,6 +57,13 @@ extern "C" int lora_apply_noalloc(const int32_t* token_lora_mapping, const int32
   void* ws = nullptr;
   const int rc0 = scratch_address(&ws);
   if (rc0 != LORA_OK) return rc0;
+  // every argument is checked before anything is enqueued
+  const int rc1 = grg::check_layer_args(
+      token_lora_mapping, num_tokens, max_num_tokens, max_loras, x, x_row_stride, hidden, lora_a,
+      lora_b, slice_width, num_slices, rank, u, y, y_row_stride, sorted_token_ids,
+      num_tokens_per_lora, lora_token_start_loc, ws, kScratchBytes);
+  if (rc1 != LORA_OK) return rc1;
+  if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return LORA_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // the status word is OR-ed by the grouping kernel: start this call from zero
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t), s) != cudaSuccess) return LORA_ERR_CUDA;

@@ -19,9 +19,9 @@
 //  - four consumer warps wait on "full", run the tensor-core MMAs (mma.sync
 //    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
 //    mbarrier; no block-wide barrier inside the k-loop.
-// The adapter blocks of the first tile are requested before
-// griddepcontrol.wait (weights are never written by the preceding kernel) and
-// the first x rows are prefetched into L2 there.  The C partial tiles are
+// Before griddepcontrol.wait a CTA reads only its first tile record
+// (lora_prepare_metadata's output) and prefetches that tile's first adapter
+// blocks and x rows into L2; every copy into shared memory comes after it.  The C partial tiles are
 // summed in rank order through distributed shared memory (no atomics, no
 // global scratch), scaled once and stored to u.
 #include <cstring>
@@ -146,6 +146,48 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       cp_async_16_hint(sbase + st * p.stage_bytes + swz128(row, ch),
                        ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok, x_pol);
     };
+    // the adapter blocks of k-block kb -> stage st, by TMA (one thread)
+    auto issue_a = [&](int st, int kb) {
+      const uint32_t bar = full_bar + 8 * st;
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(SR * 128));
+      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
+      for (int s = 0; s < p.num_slices; ++s)
+        tma_load_2d(sa + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
+    };
+    auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
+      const int st = g % NST, use = g / NST;
+      if (use > 0 && !mbar_wait(empty_bar + 8 * st, (use - 1) & 1)) timed_out = true;
+    };
+
+    if (!waited) {
+      // Before the dependency wait nothing is copied into shared memory: the
+      // kernel ahead on the stream may still be writing any input (weights
+      // included).  Only L2 prefetches go out - L2 is the GPU's coherence
+      // point, so a line prefetched early still reads the final values - of
+      // the first stages' adapter blocks and of this CTA's first x columns
+      // (cluster mode: the span of the first npro rounds, its rows shared out
+      // between the cluster's CTAs); the copies after the wait then hit L2.
+      if (producer && npro > 0) {
+        if constexpr (!PAGED) {
+          if (lane == 0)
+            for (int i = 0; i < npro; ++i)
+              for (int s = 0; s < p.num_slices; ++s)
+                tma_prefetch_2d(&p.tmap[s], kb_of(i) * kBK, lora * p.rank);
+        }
+        const int kcol = kb_of(0) * kBK;
+        const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
+        const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
+        for (int r = r0; r < cnt; r += rstep) {
+          const int t = record_token(rec, r, cnt, p.max_num_tokens);
+          if (t >= 0)
+            prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + (split_k ? kcol : 0), bytes);
+        }
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      waited = true;
+    }
+
     // paged weights: this adapter's A_s (a null or misaligned table entry
     // reads as an all-zero adapter and sets LORA_STATUS_BAD_WEIGHT)
     const __nv_bfloat16* abase[3] = {nullptr, nullptr, nullptr};
@@ -170,21 +212,10 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
                     ok);
       }
     };
-    // the adapter blocks of k-block kb -> stage st, by TMA (one thread)
-    auto issue_a = [&](int st, int kb) {
-      const uint32_t bar = full_bar + 8 * st;
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(SR * 128));
-      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
-      for (int s = 0; s < p.num_slices; ++s)
-        tma_load_2d(sa + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
-    };
-    auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
-      const int st = g % NST, use = g / NST;
-      if (use > 0 && !mbar_wait(empty_bar + 8 * st, (use - 1) & 1)) timed_out = true;
-    };
 
-    // first stages: the weights before the dependency wait, then every thread
-    // issues its share of the x rows and arrives on the stage's barrier
+    // first stages: the producer's lane 0 requests the adapter blocks, then
+    // every thread issues its share of the x rows and arrives on the stage's
+    // barrier
     if (producer && lane == 0) {
       for (int i = 0; i < npro; ++i) {
         wait_empty(kb_global + i);
@@ -199,25 +230,6 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       // barrier); each thread's adapter chunks complete with its x chunks
       for (int i = 0; i < npro; ++i)
         a_chunks((kb_global + i) % NST, kb_of(i), tid, kShrinkThreads);
-    }
-    if (!waited) {
-      if (producer && npro > 0) {
-        // warm L2 (and the TLB) with this CTA's first x columns while the
-        // previous kernel finishes; the copies below then hit L2.  Cluster
-        // mode: the span of the first npro rounds, its rows shared out
-        // between the cluster's CTAs
-        const int kcol = kb_of(0) * kBK;
-        const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
-        const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
-        for (int r = r0; r < cnt; r += rstep) {
-          const int t = record_token(rec, r, cnt, p.max_num_tokens);
-          if (t >= 0)
-            prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + (split_k ? kcol : 0), bytes);
-        }
-      }
-      pdl_wait();
-      pdl_launch_dependents();
-      waited = true;
     }
     for (int i = 0; i < npro; ++i) {
       const int st = (kb_global + i) % NST;
@@ -399,6 +411,12 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     }
     fence_proxy_async();  // generic use of the ring before the next item's TMA writes
     cluster_sync_all();
+  }
+  if (!waited) {
+    // a CTA without a tile still waits: the grid must not complete (and so
+    // release the next kernel's wait) before the kernel ahead of it has
+    pdl_wait();
+    pdl_launch_dependents();
   }
   if (timed_out) atomicOr(p.status, kStatusTimeout);
 }

@@ -37,8 +37,25 @@
  *    stream) on the current device, so every call can be captured into a CUDA
  *    graph.  The number of valid tokens n lives in device memory, so one
  *    captured graph serves every n <= max_num_tokens.
- *  - Kernels are launched with programmatic dependent launch enabled; each
- *    one waits for the preceding work on the stream before touching memory.
+ *  - Kernels are launched with programmatic dependent launch enabled, so a
+ *    kernel may start while the one ahead of it on the stream is finishing.
+ *    Before its dependency wait (which returns once every earlier kernel on
+ *    the stream has completed and its writes are visible) a kernel of this
+ *    library only
+ *      - reads the tile records in the workspace, which only
+ *        lora_prepare_metadata writes and which it makes visible before it
+ *        lets the next kernel start (so nothing else may write the workspace
+ *        while calls that use it are in flight), and
+ *      - prefetches weights and activation rows into L2, which is the GPU's
+ *        coherence point: a prefetch never yields stale data.
+ *    Every copy into shared memory and every other read comes after the
+ *    wait, with one exception inside lora_shrink_expand (and its fp16 and
+ *    paged forms): its second kernel loads B and its y rows before the wait,
+ *    because the kernel ahead of it is the same call's shrink, which writes
+ *    neither and lets the second kernel start only after its own wait.  So
+ *    any kernel may come right before any call, including one that rewrites
+ *    the weights, x or y.  A kernel whose CTAs have no work still waits
+ *    before it exits, so stream order holds through it.
  *  - Return value: LORA_OK when the work was enqueued, a negative LORA_ERR_*
  *    code when an argument was rejected (nothing is launched) or the launch
  *    failed.  Problems that only the data reveals (a LoRA id outside [-1, L),
@@ -89,8 +106,9 @@ size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras);
  * kernels for V1", "Why do we need a new set of kernels": V1 keeps the batch
  * unsorted, so the grouping is computed on the device from the token -> LoRA
  * map; "[Kernel] LoRA - Enable CUDAGraphs for V1": the map is a static
- * max_num_tokens buffer).  One single-CTA histogram / prefix-sum / stable
- * scatter; the grid does not depend on the data.
+ * max_num_tokens buffer).  One thread-block cluster (one CTA per 1024 tokens
+ * of max_num_tokens, up to 8) runs a histogram / prefix-sum / stable scatter;
+ * the grid depends only on max_num_tokens, not on the data.
  *
  *   token_lora_mapping   int32[max_num_tokens]; entries t >= n are never read
  *   num_tokens           device int32: n
@@ -122,8 +140,7 @@ int lora_prepare_metadata(const int32_t *token_lora_mapping, const int32_t *num_
  *   lora_a           HOST array of num_slices device pointers, each
  *                    bf16[max_loras][rank][hidden] row-major
  *   lora_scales      NULL, or device fp32[max_loras]: a per-adapter factor on
- *                    scale (the pages are silent on per-LoRA scales); read
- *                    after the preceding kernel on the stream has finished
+ *                    scale (the pages are silent on per-LoRA scales)
  *   u                fp32[num_slices][max_num_tokens][rank] out; only rows of
  *                    adapter tokens t < n are written
  *   sorted_token_ids, lora_token_start_loc, workspace: from lora_prepare_metadata
@@ -252,9 +269,8 @@ int lora_expand_partials_f16(int64_t hidden, const uint16_t *const *lora_b,
  * Table pointers must be 8-byte aligned.  An entry must be 16-byte aligned
  * or 0; 0 reads as an all-zero adapter (its tokens get u = 0, y unchanged),
  * and a misaligned entry reads the same way and sets LORA_STATUS_BAD_WEIGHT.
- * The tables and the weights they point to are read before the kernel's
- * dependency wait, like stacked weights: the kernel immediately before on
- * the stream must not write them.  The weights move by 16-byte cp.async
+ * The tables and the weights they point to are read after the kernels'
+ * dependency wait, like stacked weights.  The weights move by 16-byte cp.async
  * instead of TMA tensor maps; the one-call entry point never takes the
  * fused kernel.
  */
@@ -350,9 +366,8 @@ int lora_read_status(void *workspace, uint32_t *status, void *stream);
  * device current): make that first call before any stream capture.  Every
  * call uses the same array and leaves its contents behind; the call clears
  * the status word it needs zeroed itself.  Calls that overlap on the GPU
- * (other streams, other threads) race on the array: serialise them.  An
- * argument error in the shrink or expand step is reported after the earlier
- * steps of the same call were enqueued.
+ * (other streams, other threads) race on the array: serialise them.  Every
+ * argument is checked before anything is enqueued.
  */
 #define LORA_NOALLOC_SCRATCH_BYTES (384 * 1024)
 int lora_apply_noalloc(const int32_t *token_lora_mapping, const int32_t *num_tokens,

@@ -51,13 +51,33 @@ def test_decode_and_prefill_bytes_per_launch():
     assert (b["shrink"], b["expand"]) == (68_681_728, 135_790_592)
 
 
-def test_recorded_traffic_is_current_for_the_reported_kernels():
-    """The DRAM traffic the bench reports comes from committed ncu records whose
-    source hash matches the kernel sources; a stale record reads as null."""
+def test_recorded_traffic_is_returned_only_for_unchanged_kernels():
+    """The DRAM traffic the bench reports comes from committed ncu records:
+    a record whose source hash matches the kernel sources is returned, a
+    stale one reads as null."""
     with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
         rec = json.load(f)
-    for key in ("expand-split/decode_qkv", "expand/chunked_prefill"):
+    assert rec
+    for key, r in rec.items():
         kernel, workload = key.split("/")
-        assert bench.recorded_traffic(kernel, workload) == rec[key]["bytes_per_launch"]
-        assert rec[key]["bytes_per_launch"] == rec[key]["read"] + rec[key]["write"]
+        assert r["bytes_per_launch"] == r["read"] + r["write"]
+        current = r["source_hash"] == bench.kernel_source_hash(kernel)
+        expect = r["bytes_per_launch"] if current else None
+        assert bench.recorded_traffic(kernel, workload) == expect
     assert bench.recorded_traffic("expand", "no_such_workload") is None
+
+
+def test_layers_per_step_exceed_twice_the_l2():
+    l2 = 132_120_576
+    for name, shape in W.CONFIGS.items():
+        k = bench.layers_per_step(shape, l2)
+        assert k >= 4 and k * bench.layer_bytes(shape) > 2 * l2, name
+
+
+def test_both_arms_describe_the_same_config():
+    args = bench.parse_args([])
+    assert args.config == "all" and args.steps == 20
+    shape = W.CONFIGS[bench.HEADLINE]
+    a = bench.config_of(shape, args, 132_120_576, 1)
+    assert a["workload"] == "down_proj_graph" and "inputs larger than L2" in a["l2"]
+    assert a == bench.config_of(shape, bench.parse_args(["--impl", "reference"]), 132_120_576, 1)

@@ -35,8 +35,8 @@ def _worker(rank, world, port, out_q):
     try:
         bench.barrier(world)
         mx = bench.max_over_ranks(10.0 + rank, world)
-        args = bench.argparse.Namespace(steps=2, warmup=1, config="tiny", impl="reference",
-                                         dtype="bf16")
+        args = bench.parse_args(["--steps", "2", "--warmup", "1", "--config", "tiny",
+                                 "--impl", "reference", "--gpus", "2"])
         buf = io.StringIO()
         with redirect_stdout(buf):
             rc = bench.run_reference(args, world, rank)
@@ -64,3 +64,32 @@ def test_two_ranks_take_the_max_and_only_rank0_prints():
     line = json.loads(res[0][2].strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
     assert res[1][2].strip() == ""
+
+
+def test_bench_spawns_its_own_ranks_when_no_launcher_did():
+    """`bench.py --gpus 2` without torchrun starts two ranks itself; on CPU
+    the reference arm runs (gloo): rank 0 prints one line for 2 GPUs."""
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--config", "tiny", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2
+    assert line["config"]["workload"] == "tiny"
+
+
+def test_bench_refuses_more_gpus_than_visible():
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k != "WORLD_SIZE"}
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--config", "tiny"], capture_output=True, text=True, timeout=300,
+                       env=env, cwd=ROOT)
+    assert r.returncode == 1
+    assert "needs 2 CUDA devices" in r.stdout

@@ -35,7 +35,7 @@ def _regular(shape, mapping, layer, dev):
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name", ["decode_qkv", "ragged"])
+@pytest.mark.parametrize("name", ["decode_qkv", "ragged", "down_proj_graph"])
 def test_noalloc_matches_the_regular_path_twice(name):
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
