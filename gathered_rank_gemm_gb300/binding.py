@@ -35,7 +35,14 @@ EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora
             "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials",
             "lora_shrink_paged", "lora_expand_paged", "lora_shrink_expand_paged",
             "lora_shrink_f16", "lora_expand_f16", "lora_shrink_expand_f16",
-            "lora_shrink_partials_f16", "lora_expand_partials_f16")
+            "lora_shrink_partials_f16", "lora_expand_partials_f16", "lora_shrink_expand_path")
+
+LORA_PATH_FUSED = 1
+LORA_PATH_SPLIT_FUSED = 2
+LORA_PATH_SPLIT_PAIR = 3
+LORA_PATH_PAIR = 4
+PATH_NAMES = {LORA_PATH_FUSED: "fused", LORA_PATH_SPLIT_FUSED: "split-K one kernel",
+              LORA_PATH_SPLIT_PAIR: "split-K pair", LORA_PATH_PAIR: "cluster pair"}
 
 _lib = None
 
@@ -96,6 +103,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         f16 = getattr(lib, name + "_f16")
         f16.restype = i32
         f16.argtypes = getattr(lib, name).argtypes
+    lib.lora_shrink_expand_path.restype = i32
+    lib.lora_shrink_expand_path.argtypes = [i64, i64, i64, p, i32, i32, sz, i32, i32]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, p, i64, p, p, p, p, p]
@@ -356,6 +365,20 @@ def lora_shrink_expand_kernels(max_num_tokens: int, max_loras: int, hidden: int,
                                            ctypes.addressof(w), len(slice_widths), int(rank))
     if rc < 0:
         _check("lora_shrink_expand_kernels", rc)
+    return int(rc)
+
+
+def lora_shrink_expand_path(max_num_tokens: int, max_loras: int, hidden: int, slice_widths,
+                            rank: int, workspace_bytes: int, fp16: bool = False,
+                            paged: bool = False) -> int:
+    """Which path one lora_shrink_expand call takes (LORA_PATH_*) for a shape
+    and workspace size on the current device."""
+    w = (ctypes.c_int64 * len(slice_widths))(*[int(v) for v in slice_widths])
+    rc = load().lora_shrink_expand_path(int(max_num_tokens), int(max_loras), int(hidden),
+                                        ctypes.addressof(w), len(slice_widths), int(rank),
+                                        int(workspace_bytes), int(bool(fp16)), int(bool(paged)))
+    if rc < 0:
+        _check("lora_shrink_expand_path", rc)
     return int(rc)
 
 

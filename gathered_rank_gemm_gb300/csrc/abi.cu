@@ -135,9 +135,26 @@ constexpr int kSplitMaxRank = 32;
 bool split_shape(int64_t max_num_tokens, int rank) {
   return max_num_tokens <= kSplitMaxTokens && rank <= kSplitMaxRank;
 }
+// Behind the metadata part: one arrival counter per 16-token tile (the
+// one-kernel split path's hand-off; zeroed by lora_prepare_metadata), then the
+// partial tiles.
+size_t split_arrival_bytes(int64_t max_num_tokens, int64_t max_loras) {
+  return (static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) * 4 + 255) /
+         256 * 256;
+}
 size_t split_scratch_bytes(int64_t max_num_tokens, int64_t max_loras, int num_slices, int rank) {
-  return static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) *
-         grg::split_k_max(rank) * 16 * num_slices * rank * 4;
+  return split_arrival_bytes(max_num_tokens, max_loras) +
+         static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) *
+             grg::split_k_max(rank) * 16 * num_slices * rank * 4;
+}
+float* split_partials(const void* workspace, int64_t max_num_tokens, int64_t max_loras) {
+  return reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) +
+                                  grg::workspace_bytes_needed(max_num_tokens, max_loras) +
+                                  split_arrival_bytes(max_num_tokens, max_loras));
+}
+unsigned int* split_arrivals(const void* workspace, int64_t max_num_tokens, int64_t max_loras) {
+  return reinterpret_cast<unsigned int*>(static_cast<char*>(const_cast<void*>(workspace)) +
+                                         grg::workspace_bytes_needed(max_num_tokens, max_loras));
 }
 }  // namespace
 
@@ -183,7 +200,7 @@ int shrink_partials(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
   const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
   if (workspace_bytes < base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank))
     return LORA_ERR_WORKSPACE;
-  sa.partials = reinterpret_cast<float*>(static_cast<char*>(workspace) + base);
+  sa.partials = split_partials(workspace, max_num_tokens, max_loras);
   sa.f16 = f16;
   return grg::launch_shrink(sa, static_cast<cudaStream_t>(stream));
 }
@@ -228,8 +245,7 @@ int expand_partials(int64_t hidden, const uint16_t* const* lora_b, const int64_t
   const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
   if (workspace_bytes < base + split_scratch_bytes(max_num_tokens, max_loras, num_slices, rank))
     return LORA_ERR_WORKSPACE;
-  ea.partials =
-      reinterpret_cast<const float*>(static_cast<const char*>(workspace) + base);
+  ea.partials = split_partials(workspace, max_num_tokens, max_loras);
   ea.split = split_of(max_num_tokens, max_loras, hidden, num_slices, rank);
   ea.scale = scale;
   ea.lora_scales = lora_scales;
@@ -325,9 +341,15 @@ int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_
                                sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
                                workspace, workspace_bytes);
   if (rc != LORA_OK) return rc;
+  // a workspace with room for the split path's arrival counters gets them zeroed
+  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
+  const bool counters = workspace_bytes >= base + split_arrival_bytes(max_num_tokens, max_loras);
   return grg::launch_metadata(token_lora_mapping, num_tokens, static_cast<int>(max_num_tokens),
                               static_cast<int>(max_loras), sorted_token_ids, num_tokens_per_lora,
-                              lora_token_start_loc, workspace, static_cast<cudaStream_t>(stream));
+                              lora_token_start_loc, workspace,
+                              counters ? split_arrivals(workspace, max_num_tokens, max_loras)
+                                       : nullptr,
+                              static_cast<cudaStream_t>(stream));
 }
 
 int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
@@ -388,6 +410,16 @@ int lora_expand_paged(const float* u, const uint64_t* const* lora_b_tables,
 }
 
 namespace {
+// The split-K one-call path applies: a decode-sized shape, a workspace with
+// room for the arrival counters and partial tiles, and a split of at least 2.
+bool split_path_ok(const grg::ShrinkArgs& sa, size_t workspace_bytes) {
+  const int64_t T = sa.max_num_tokens, L = sa.num_loras;
+  return split_shape(T, sa.rank) &&
+         workspace_bytes >= grg::workspace_bytes_needed(T, L) +
+                                split_scratch_bytes(T, L, sa.num_slices, sa.rank) &&
+         grg::shrink_split(sa, true) >= 2;
+}
+
 // One layer in one call, for validated arguments (stacked or paged weights):
 // the fused kernel when the batch fits it, else the split-K pair when the
 // workspace has room for the partial tiles, else the two kernels.
@@ -401,12 +433,14 @@ int shrink_expand(grg::ShrinkArgs& sa, grg::ExpandArgs& ea, int64_t hidden,
   // split-K: with the larger workspace, the shrink's CTAs write partial tiles
   // and the expand sums them in rank order (no cluster-wide steps)
   const int64_t T = sa.max_num_tokens, L = sa.num_loras;
-  const size_t base = grg::workspace_bytes_needed(T, L);
-  if (split_shape(T, sa.rank) &&
-      workspace_bytes >= base + split_scratch_bytes(T, L, sa.num_slices, sa.rank) &&
-      grg::shrink_split(sa, true) >= 2) {
-    char* ws = static_cast<char*>(const_cast<void*>(workspace));
-    sa.partials = reinterpret_cast<float*>(ws + base);
+  if (split_path_ok(sa, workspace_bytes)) {
+    float* partials = split_partials(workspace, T, L);
+    // one kernel when its grid fits the device at once, else two
+    rc = grg::launch_split_fused(sa, ea, grg::shrink_split(sa, true), partials,
+                                 split_arrivals(workspace, T, L), s);
+    if (rc < 0) return rc;
+    if (rc == 1) return LORA_OK;
+    sa.partials = partials;
     rc = grg::launch_shrink(sa, s);
     if (rc != LORA_OK) return rc;
     ea.partials = sa.partials;
@@ -533,6 +567,40 @@ int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_
                          static_cast<int>(hidden), w, num_slices, rank)
              ? 1
              : 2;
+}
+
+int lora_shrink_expand_path(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,
+                            const int64_t* slice_width, int num_slices, int rank,
+                            size_t workspace_bytes, int fp16, int paged) {
+  if (!slice_width) return LORA_ERR_NULL;
+  if (num_slices < 1 || num_slices > LORA_MAX_SLICES || !sizes_ok(max_num_tokens, max_loras) ||
+      !rank_ok(rank) || hidden < 8 || hidden > kMaxHidden || (hidden % 8) != 0)
+    return LORA_ERR_SHAPE;
+  if ((fp16 && paged) ||
+      workspace_bytes < grg::workspace_bytes_needed(max_num_tokens, max_loras))
+    return LORA_ERR_SHAPE;
+  int w[3] = {0, 0, 0};
+  for (int s = 0; s < num_slices; ++s) {
+    if (slice_width[s] < 8 || slice_width[s] > kMaxWidth || (slice_width[s] % 8) != 0)
+      return LORA_ERR_SHAPE;
+    w[s] = static_cast<int>(slice_width[s]);
+  }
+  const int T = static_cast<int>(max_num_tokens), L = static_cast<int>(max_loras);
+  const int H = static_cast<int>(hidden);
+  if (!paged && grg::fused_fits(T, L, H, w, num_slices, rank)) return LORA_PATH_FUSED;
+  grg::ShrinkArgs sa;
+  sa.hidden = H;
+  sa.num_slices = num_slices;
+  sa.rank = rank;
+  sa.max_num_tokens = T;
+  sa.num_loras = L;
+  if (split_path_ok(sa, workspace_bytes)) {
+    if (!paged && grg::split_fused_fits(T, L, H, w, num_slices, rank,
+                                        grg::shrink_split(sa, true), fp16 != 0))
+      return LORA_PATH_SPLIT_FUSED;
+    return LORA_PATH_SPLIT_PAIR;
+  }
+  return LORA_PATH_PAIR;
 }
 
 int lora_read_status(void* workspace, uint32_t* status, void* stream) {

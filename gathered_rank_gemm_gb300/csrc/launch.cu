@@ -111,6 +111,11 @@ int launch_raw(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_
 
 int make_weight_tmap(CUtensorMap* map, const void* base, long long cols, long long rows,
                      int box_rows) {
+  return make_tmap_2d(map, base, cols, rows, cols * 2, box_rows);
+}
+
+int make_tmap_2d(CUtensorMap* map, const void* base, long long cols, long long rows,
+                 long long row_stride_bytes, int box_rows) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -123,7 +128,7 @@ int make_weight_tmap(CUtensorMap* map, const void* base, long long cols, long lo
   });
   if (!encode) return -6;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_stride_bytes)};
   const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,

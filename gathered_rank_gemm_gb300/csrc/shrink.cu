@@ -37,6 +37,7 @@ constexpr int kBK = 64;  // bf16 columns per k-block: one 128-byte (swizzled) ro
 
 struct ShrinkParams {
   CUtensorMap tmap[3];  // A_s viewed as [L * R][hidden], boxes of R x 64
+  CUtensorMap xmap;     // x viewed as [max_num_tokens][hidden], boxes of BM x 64
   const __nv_bfloat16* x;
   long long x_stride;
   int hidden;
@@ -136,6 +137,15 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     const int lora = tv.lora, cnt = tv.count;
     const int npro = min(nkb, NST);
+    // A full tile whose tokens are consecutive (a request's run of prompt
+    // tokens, the usual case in prefill: the grouping keeps each adapter's
+    // tokens in ascending order, so first + BM - 1 == last means a run) has
+    // its x rows at one place: one TMA box per k-block moves them, in the
+    // same swizzled layout the per-row copies give.
+    const int t_first = rec[kRecordHeaderInts];
+    const bool xbox = cnt == BM && t_first >= 0 &&
+                      rec[kRecordHeaderInts + BM - 1] - t_first == BM - 1 &&
+                      t_first <= p.max_num_tokens - BM;
 
     // x chunk (row, 16-byte chunk) c of k-block kb -> stage st
     auto x_chunk = [&](int st, int kb, int c) {
@@ -146,13 +156,23 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       cp_async_16_hint(sbase + st * p.stage_bytes + swz128(row, ch),
                        ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok, x_pol);
     };
-    // the adapter blocks of k-block kb -> stage st, by TMA (one thread)
+    // the TMA part of k-block kb -> stage st (one thread): the adapter blocks
+    // (stacked weights) and the x box (a run tile); with neither, a plain
+    // arrival stands in for the transaction count
     auto issue_a = [&](int st, int kb) {
       const uint32_t bar = full_bar + 8 * st;
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(SR * 128));
-      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
-      for (int s = 0; s < p.num_slices; ++s)
-        tma_load_2d(sa + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
+      const uint32_t bytes = (PAGED ? 0u : static_cast<uint32_t>(SR * 128)) +
+                             (xbox ? static_cast<uint32_t>(BM * 128) : 0u);
+      if (bytes == 0) {
+        mbar_arrive(bar);
+        return;
+      }
+      mbar_arrive_expect_tx(bar, bytes);
+      const uint32_t sx = sbase + st * p.stage_bytes;
+      if constexpr (!PAGED)
+        for (int s = 0; s < p.num_slices; ++s)
+          tma_load_2d(sx + BM * 128 + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
+      if (xbox) tma_load_2d_hint(sx, &p.xmap, kb * kBK, t_first, bar, x_pol);
     };
     auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
       const int st = g % NST, use = g / NST;
@@ -174,13 +194,19 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
               for (int s = 0; s < p.num_slices; ++s)
                 tma_prefetch_2d(&p.tmap[s], kb_of(i) * kBK, lora * p.rank);
         }
-        const int kcol = kb_of(0) * kBK;
-        const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
-        const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
-        for (int r = r0; r < cnt; r += rstep) {
-          const int t = record_token(rec, r, cnt, p.max_num_tokens);
-          if (t >= 0)
-            prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + (split_k ? kcol : 0), bytes);
+        if (xbox) {
+          if (lane == 0)
+            for (int i = 0; i < npro; ++i) tma_prefetch_2d(&p.xmap, kb_of(i) * kBK, t_first);
+        } else {
+          const int kcol = kb_of(0) * kBK;
+          const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
+          const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
+          for (int r = r0; r < cnt; r += rstep) {
+            const int t = record_token(rec, r, cnt, p.max_num_tokens);
+            if (t >= 0)
+              prefetch_l2(p.x + static_cast<long long>(t) * p.x_stride + (split_k ? kcol : 0),
+                          bytes);
+          }
         }
       }
       pdl_wait();
@@ -213,16 +239,13 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       }
     };
 
-    // first stages: the producer's lane 0 requests the adapter blocks, then
-    // every thread issues its share of the x rows and arrives on the stage's
-    // barrier
+    // first stages: the producer's lane 0 issues the TMA part, then every
+    // thread issues its share of the x rows (per-row tiles) and arrives on the
+    // stage's barrier once its copies have landed
     if (producer && lane == 0) {
       for (int i = 0; i < npro; ++i) {
         wait_empty(kb_global + i);
-        if constexpr (PAGED)
-          mbar_arrive(full_bar + 8 * ((kb_global + i) % NST));  // no transaction bytes
-        else
-          issue_a((kb_global + i) % NST, kb_of(i));
+        issue_a((kb_global + i) % NST, kb_of(i));
       }
     }
     if constexpr (PAGED) {
@@ -233,7 +256,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     }
     for (int i = 0; i < npro; ++i) {
       const int st = (kb_global + i) % NST;
-      for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb_of(i), c);
+      if (!xbox)
+        for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb_of(i), c);
       cp_async_mbar_arrive(full_bar + 8 * st);
     }
 
@@ -255,21 +279,20 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         wait_empty(g);  // every lane: the consumers released the stage
         __syncwarp();
         if (lane == 0) {
-          if constexpr (PAGED)
-            mbar_arrive(full_bar + 8 * st);
-          else
-            issue_a(st, kb_of(i));
+          issue_a(st, kb_of(i));
           mbar_arrive_count(full_bar + 8 * st, kShrinkThreads - 32);
         }
         if constexpr (PAGED) a_chunks(st, kb_of(i), lane, 32);
-        const uint32_t sx = sbase + st * p.stage_bytes;
-        const int kb = kb_of(i);
-        const bool kin = kb * kBK + xch * 8 < p.hidden;
+        if (!xbox) {
+          const uint32_t sx = sbase + st * p.stage_bytes;
+          const int kb = kb_of(i);
+          const bool kin = kb * kBK + xch * 8 < p.hidden;
 #pragma unroll
-        for (int j = 0; j < XJ; ++j) {
-          const bool ok = xrow[j] != nullptr && kin;
-          cp_async_16_hint(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok,
-                           x_pol);
+          for (int j = 0; j < XJ; ++j) {
+            const bool ok = xrow[j] != nullptr && kin;
+            cp_async_16_hint(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x,
+                             ok, x_pol);
+          }
         }
         cp_async_mbar_arrive(full_bar + 8 * st);
       }
@@ -510,6 +533,10 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
       p.tmap[s] = p.tmap[0];
     }
   }
+  // x as a [max_num_tokens][hidden] matrix of row stride x_row_stride, in
+  // boxes of BM rows x 64 columns (run tiles)
+  if (make_tmap_2d(&p.xmap, a.x, a.hidden, a.max_num_tokens, a.x_row_stride * 2, BM) != 0)
+    return -6;
   p.x = static_cast<const __nv_bfloat16*>(a.x);
   p.x_stride = a.x_row_stride;
   p.hidden = a.hidden;

@@ -187,13 +187,22 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
  * problem on chip (decode-sized batches: up to 16 k-blocks of 64 columns and
  * 48 output units of 64 columns per CTA) and every tile's cluster fits in one
  * wave, one fused kernel does both steps and the expand reads u from shared
- * memory.  Otherwise two kernels run back to back: with a workspace of at
- * least lora_shrink_expand_workspace_size bytes and a batch of up to 1024
- * tokens with rank <= 32, the shrink's CTAs (up to 16 per tile, no cluster)
- * write partial tiles of u into the workspace and the expand adds them up in
- * CTA order (u and y then match the two separate calls up to the order of
- * the fp32 partial sums); else the kernels of lora_shrink and lora_expand run
- * unchanged.  Either way the work stays on the GPU.
+ * memory.  Otherwise, with a workspace of at least
+ * lora_shrink_expand_workspace_size bytes and a batch of up to 1024 tokens
+ * with rank <= 32, the split-K path runs: the shrink's CTAs (up to 16 per
+ * tile, no cluster) write partial tiles of u into the workspace and the
+ * expand adds them up in CTA order (u and y then match the two separate calls
+ * up to the order of the fp32 partial sums).  With stacked weights, when
+ * every CTA of its grid fits on the device at once, both halves run in ONE
+ * kernel whose CTAs hand each tile's partials over through arrival counters
+ * in the workspace (release / acquire, bounded waits), bit for bit the
+ * results of the two halves; else the two halves run as two kernels.  Else
+ * the kernels of lora_shrink and lora_expand run unchanged.  Either way the
+ * work stays on the GPU; lora_shrink_expand_path tells which path a shape
+ * takes.  The split paths keep state in the workspace (partial tiles, arrival
+ * counters that lora_prepare_metadata zeroes when its workspace_bytes covers
+ * them): pass the same workspace size to lora_prepare_metadata, and order
+ * calls that share a workspace on one stream.
  */
 int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t *const *lora_a, const uint16_t *const *lora_b,
@@ -205,11 +214,13 @@ int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
 
 /*
  * Workspace bytes that let lora_shrink_expand take its split-K path for this
- * shape: lora_workspace_size plus P * 16 * num_slices * rank * 4 bytes per
- * 16-token tile of the batch (P = 16 for rank <= 16, 8 for rank 32: the
- * largest split) when max_num_tokens <= 1024 and rank <= 32 (else just
- * lora_workspace_size); 0 for sizes the calls reject.  A smaller workspace
- * (at least lora_workspace_size) is still valid for every call.
+ * shape: lora_workspace_size, then one 4-byte arrival counter per 16-token
+ * tile of the batch (rounded up to 256 bytes), then P * 16 * num_slices *
+ * rank * 4 bytes of partial tiles per 16-token tile (P = 16 for rank <= 16,
+ * 8 for rank 32: the largest split) when max_num_tokens <= 1024 and
+ * rank <= 32 (else just lora_workspace_size); 0 for sizes the calls reject.
+ * A smaller workspace (at least lora_workspace_size) is still valid for
+ * every call.
  */
 size_t lora_shrink_expand_workspace_size(int64_t max_num_tokens, int64_t max_loras,
                                          int64_t hidden, const int64_t *slice_width,
@@ -305,8 +316,9 @@ int lora_shrink_expand_paged(const uint16_t *x, int64_t x_row_stride, int64_t hi
  *   - lora_shrink_partials splits each 16-token tile's hidden dimension over
  *     up to P CTAs (as for the workspace size above; no cluster) and writes
  *     each CTA's fp32 partial tile (its warps summed) into the workspace
- *     behind the metadata: [tile][split][16][num_slices * rank].  It does not
- *     scale and does not write u.
+ *     behind the metadata and the arrival counters:
+ *     [tile][split][16][num_slices * rank].  It does not scale and does not
+ *     write u.
  *   - lora_expand_partials takes `hidden` (it fixes the split), `scale` and
  *     `lora_scales`, sums each tile's partials in CTA order, multiplies by
  *     c(lora) as lora_shrink does, writes the result to u (rows of tokens
@@ -331,12 +343,36 @@ int lora_expand_partials(int64_t hidden, const uint16_t *const *lora_b,
                          size_t workspace_bytes, void *stream);
 
 /*
- * Kernels one lora_shrink_expand call launches for this shape on the current
- * device: 1 (the fused kernel) or 2 (shrink, then expand); a negative
- * LORA_ERR_* code for sizes the calls reject.  Host-only, no GPU work.
+ * Whether one lora_shrink_expand call for this shape on the current device
+ * runs the fused kernel: 1 (it does) or 2 (it does not: the split-K or the
+ * two-kernel path, see lora_shrink_expand_path); a negative LORA_ERR_* code
+ * for sizes the calls reject.  Host-only, no GPU work.
  */
 int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,
                                const int64_t *slice_width, int num_slices, int rank);
+
+/*
+ * Which kernels one lora_shrink_expand call (fp16 != 0: lora_shrink_expand_f16;
+ * paged != 0: lora_shrink_expand_paged) runs for this shape, workspace size
+ * and the current device; host-only, no GPU work:
+ *   LORA_PATH_FUSED        one kernel holding a tile's whole problem on chip
+ *                          (tiny batches; never with paged weights)
+ *   LORA_PATH_SPLIT_FUSED  one kernel: the split-K shrink, a hand-off through
+ *                          per-tile arrival counters in the workspace, then
+ *                          the expand (decode-sized batches whose grid fits
+ *                          the device at once; stacked weights)
+ *   LORA_PATH_SPLIT_PAIR   the split-K shrink, then the partial-sum expand
+ *   LORA_PATH_PAIR         the kernels of lora_shrink, then of lora_expand
+ * The split paths need a workspace of lora_shrink_expand_workspace_size bytes.
+ * A negative LORA_ERR_* code for sizes the calls reject.
+ */
+#define LORA_PATH_FUSED 1
+#define LORA_PATH_SPLIT_FUSED 2
+#define LORA_PATH_SPLIT_PAIR 3
+#define LORA_PATH_PAIR 4
+int lora_shrink_expand_path(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,
+                            const int64_t *slice_width, int num_slices, int rank,
+                            size_t workspace_bytes, int fp16, int paged);
 
 /*
  * Copies the workspace's status word (LORA_STATUS_* bits OR-ed by every
