@@ -410,11 +410,13 @@ class WorkloadRun:
         self.us = [torch.zeros(shape.num_slices, T, shape.rank, dtype=torch.float32, device=dev)
                    for _ in range(self.layers)]
         torch.cuda.synchronize()
-        self.per_layer_kernels = (2 if args.paged else
-                                  binding.lora_shrink_expand_kernels(T, L, shape.hidden,
-                                                                     shape.slice_widths,
-                                                                     shape.rank))
-        self.split_k = False
+        # the path one lora_shrink_expand call takes here (fused kernel, split-K
+        # pair or cluster pair)
+        self.path = binding.lora_shrink_expand_path(T, L, shape.hidden, shape.slice_widths,
+                                                    shape.rank, self.meta.workspace.numel(),
+                                                    fp16=self.f16, paged=args.paged)
+        self.per_layer_kernels = 1 if self.path == binding.LORA_PATH_FUSED else 2
+        self.split_k = self.path == binding.LORA_PATH_SPLIT_PAIR
         self.graphs = {}
 
     def launch(self, which):
@@ -457,11 +459,10 @@ class WorkloadRun:
             self.launch("layers")     # outside any capture
         self.stream.synchronize()
         base = self.binding.lora_workspace_size(self.shape.max_num_tokens, self.shape.max_loras)
-        ws = self.meta.workspace
-        # the split-K path leaves its partial tiles behind the metadata part of
-        # the (zero-initialised) workspace
-        self.split_k = (self.per_layer_kernels == 2 and ws.numel() > base
-                        and bool(ws[base:].any().item()))
+        if self.split_k:
+            # the split paths leave partial tiles behind the metadata part of
+            # the (zero-initialised) workspace: check that this one ran
+            assert bool(self.meta.workspace[base:].any().item()), "split-K path did not run"
         for which in ("metadata", "layers", "shrink", "expand"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
@@ -581,6 +582,7 @@ class WorkloadRun:
         alg = algorithmic_bytes(sh, self.wl.mapping)
         both = alg["shrink"] + alg["expand"]
         if self.per_layer_kernels == 1:
+            # one fused kernel per layer: it moves the bytes of both steps
             dominant, kernel_name = "shrink_expand", "lora_fused_kernel"
             dom_bytes, t_dom = both, self.ms_one
         else:
@@ -596,8 +598,7 @@ class WorkloadRun:
         return {
             "config": config_of(sh, self.args, self.l2, world),
             "layers_per_step": self.layers,
-            "one_call_path": ("fused" if self.per_layer_kernels == 1
-                              else ("split-K" if self.split_k else "cluster")),
+            "one_call_path": self.binding.PATH_NAMES[self.path],
             "kernels_per_layer": self.per_layer_kernels,
             "tokens_per_s": n * self.layers * world / (ms_layers_max * 1e-3),
             "tokens_per_s_with_metadata": n * self.layers * world / (ms_step_max * 1e-3),

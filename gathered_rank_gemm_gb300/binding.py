@@ -38,11 +38,10 @@ EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora
             "lora_shrink_partials_f16", "lora_expand_partials_f16", "lora_shrink_expand_path")
 
 LORA_PATH_FUSED = 1
-LORA_PATH_SPLIT_FUSED = 2
 LORA_PATH_SPLIT_PAIR = 3
 LORA_PATH_PAIR = 4
-PATH_NAMES = {LORA_PATH_FUSED: "fused", LORA_PATH_SPLIT_FUSED: "split-K one kernel",
-              LORA_PATH_SPLIT_PAIR: "split-K pair", LORA_PATH_PAIR: "cluster pair"}
+PATH_NAMES = {LORA_PATH_FUSED: "fused", LORA_PATH_SPLIT_PAIR: "split-K",
+              LORA_PATH_PAIR: "cluster"}
 
 _lib = None
 

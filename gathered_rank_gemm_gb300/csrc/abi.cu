@@ -135,26 +135,14 @@ constexpr int kSplitMaxRank = 32;
 bool split_shape(int64_t max_num_tokens, int rank) {
   return max_num_tokens <= kSplitMaxTokens && rank <= kSplitMaxRank;
 }
-// Behind the metadata part: one arrival counter per 16-token tile (the
-// one-kernel split path's hand-off; zeroed by lora_prepare_metadata), then the
-// partial tiles.
-size_t split_arrival_bytes(int64_t max_num_tokens, int64_t max_loras) {
-  return (static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) * 4 + 255) /
-         256 * 256;
-}
+// The partial tiles, behind the metadata part of the workspace.
 size_t split_scratch_bytes(int64_t max_num_tokens, int64_t max_loras, int num_slices, int rank) {
-  return split_arrival_bytes(max_num_tokens, max_loras) +
-         static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) *
-             grg::split_k_max(rank) * 16 * num_slices * rank * 4;
+  return static_cast<size_t>(grg::tile_list_capacity(max_num_tokens, max_loras, 0)) *
+         grg::split_k_max(rank) * 16 * num_slices * rank * 4;
 }
 float* split_partials(const void* workspace, int64_t max_num_tokens, int64_t max_loras) {
   return reinterpret_cast<float*>(static_cast<char*>(const_cast<void*>(workspace)) +
-                                  grg::workspace_bytes_needed(max_num_tokens, max_loras) +
-                                  split_arrival_bytes(max_num_tokens, max_loras));
-}
-unsigned int* split_arrivals(const void* workspace, int64_t max_num_tokens, int64_t max_loras) {
-  return reinterpret_cast<unsigned int*>(static_cast<char*>(const_cast<void*>(workspace)) +
-                                         grg::workspace_bytes_needed(max_num_tokens, max_loras));
+                                  grg::workspace_bytes_needed(max_num_tokens, max_loras));
 }
 }  // namespace
 
@@ -341,15 +329,9 @@ int lora_prepare_metadata(const int32_t* token_lora_mapping, const int32_t* num_
                                sorted_token_ids, num_tokens_per_lora, lora_token_start_loc,
                                workspace, workspace_bytes);
   if (rc != LORA_OK) return rc;
-  // a workspace with room for the split path's arrival counters gets them zeroed
-  const size_t base = grg::workspace_bytes_needed(max_num_tokens, max_loras);
-  const bool counters = workspace_bytes >= base + split_arrival_bytes(max_num_tokens, max_loras);
   return grg::launch_metadata(token_lora_mapping, num_tokens, static_cast<int>(max_num_tokens),
                               static_cast<int>(max_loras), sorted_token_ids, num_tokens_per_lora,
-                              lora_token_start_loc, workspace,
-                              counters ? split_arrivals(workspace, max_num_tokens, max_loras)
-                                       : nullptr,
-                              static_cast<cudaStream_t>(stream));
+                              lora_token_start_loc, workspace, static_cast<cudaStream_t>(stream));
 }
 
 int lora_shrink(const uint16_t* x, int64_t x_row_stride, int64_t hidden,
@@ -411,7 +393,7 @@ int lora_expand_paged(const float* u, const uint64_t* const* lora_b_tables,
 
 namespace {
 // The split-K one-call path applies: a decode-sized shape, a workspace with
-// room for the arrival counters and partial tiles, and a split of at least 2.
+// room for the partial tiles, and a split of at least 2.
 bool split_path_ok(const grg::ShrinkArgs& sa, size_t workspace_bytes) {
   const int64_t T = sa.max_num_tokens, L = sa.num_loras;
   return split_shape(T, sa.rank) &&
@@ -434,13 +416,7 @@ int shrink_expand(grg::ShrinkArgs& sa, grg::ExpandArgs& ea, int64_t hidden,
   // and the expand sums them in rank order (no cluster-wide steps)
   const int64_t T = sa.max_num_tokens, L = sa.num_loras;
   if (split_path_ok(sa, workspace_bytes)) {
-    float* partials = split_partials(workspace, T, L);
-    // one kernel when its grid fits the device at once, else two
-    rc = grg::launch_split_fused(sa, ea, grg::shrink_split(sa, true), partials,
-                                 split_arrivals(workspace, T, L), s);
-    if (rc < 0) return rc;
-    if (rc == 1) return LORA_OK;
-    sa.partials = partials;
+    sa.partials = split_partials(workspace, T, L);
     rc = grg::launch_shrink(sa, s);
     if (rc != LORA_OK) return rc;
     ea.partials = sa.partials;
@@ -594,12 +570,7 @@ int lora_shrink_expand_path(int64_t max_num_tokens, int64_t max_loras, int64_t h
   sa.rank = rank;
   sa.max_num_tokens = T;
   sa.num_loras = L;
-  if (split_path_ok(sa, workspace_bytes)) {
-    if (!paged && grg::split_fused_fits(T, L, H, w, num_slices, rank,
-                                        grg::shrink_split(sa, true), fp16 != 0))
-      return LORA_PATH_SPLIT_FUSED;
-    return LORA_PATH_SPLIT_PAIR;
-  }
+  if (split_path_ok(sa, workspace_bytes)) return LORA_PATH_SPLIT_PAIR;
   return LORA_PATH_PAIR;
 }
 

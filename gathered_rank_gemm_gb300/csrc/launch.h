@@ -38,11 +38,9 @@ int make_weight_tmap(CUtensorMap* map, const void* base, long long cols, long lo
 int make_tmap_2d(CUtensorMap* map, const void* base, long long cols, long long rows,
                  long long row_stride_bytes, int box_rows);
 
-// arrivals: null, or the split path's tile_list_capacity(.., 0) arrival
-// counters, which the kernel zeroes
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
                     int num_loras, int32_t* sorted_ids, int32_t* counts, int32_t* starts,
-                    void* workspace, unsigned int* arrivals, cudaStream_t stream);
+                    void* workspace, cudaStream_t stream);
 
 struct ShrinkArgs {
   const void* x;
@@ -104,16 +102,6 @@ struct ExpandArgs {
   bool y_early = false;
 };
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
-
-// One-kernel split path (split-K shrink, hand-off through the arrival
-// counters, expand): 1 when launched, 0 when the shape or its grid does not
-// fit (run the split-K shrink + expand pair instead), < 0 on error.
-int launch_split_fused(const ShrinkArgs& sa, const ExpandArgs& ea, int split, float* partials,
-                       unsigned int* arrivals, cudaStream_t stream);
-// 1 when launch_split_fused would launch for this shape and split on the
-// current device (its whole grid resident at once), else 0.
-int split_fused_fits(int max_num_tokens, int num_loras, int hidden, const int* widths,
-                     int num_slices, int rank, int split, bool f16);
 
 // Fused shrink -> expand: 1 when launched, 0 when the shape does not fit the
 // fused kernel (run launch_shrink + launch_expand instead), < 0 on error.

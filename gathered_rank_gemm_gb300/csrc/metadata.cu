@@ -100,8 +100,6 @@ struct MetaParams {
   int32_t* counts;
   int32_t* starts;
   WsView ws;
-  unsigned int* arrivals;  // split path's arrival counters to zero, or null
-  int num_arrivals;
 };
 
 __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaParams p) {
@@ -273,8 +271,6 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
     }
   }
   for (int t = n + ctid; t < p.max_num_tokens; t += cthreads) p.sorted_ids[t] = -1;
-  if (p.arrivals != nullptr)
-    for (int i = ctid; i < p.num_arrivals; i += cthreads) p.arrivals[i] = 0u;
   if (crank == 0) {
     for (int b = tid; b < nbins; b += kMetaThreads) p.counts[b] = total[b];
     for (int b = tid; b <= nbins; b += kMetaThreads) p.starts[b] = start[b];
@@ -321,7 +317,7 @@ static size_t meta_smem_bytes(int num_loras) {
 
 int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_num_tokens,
                     int num_loras, int32_t* sorted_ids, int32_t* counts, int32_t* starts,
-                    void* workspace, unsigned int* arrivals, cudaStream_t stream) {
+                    void* workspace, cudaStream_t stream) {
   MetaParams p;
   p.mapping = mapping;
   p.num_tokens = num_tokens;
@@ -331,8 +327,6 @@ int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_n
   p.counts = counts;
   p.starts = starts;
   p.ws = ws_view(workspace, max_num_tokens, num_loras);
-  p.arrivals = arrivals;
-  p.num_arrivals = static_cast<int>(tile_list_capacity(max_num_tokens, num_loras, 0));
   const size_t smem = meta_smem_bytes(num_loras);
   if (ensure_smem_attr(reinterpret_cast<const void*>(lora_metadata_kernel), smem) != 0)
     return -6;

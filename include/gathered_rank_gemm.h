@@ -192,17 +192,11 @@ int lora_expand(const float *u, const uint16_t *const *lora_b, const int64_t *sl
  * with rank <= 32, the split-K path runs: the shrink's CTAs (up to 16 per
  * tile, no cluster) write partial tiles of u into the workspace and the
  * expand adds them up in CTA order (u and y then match the two separate calls
- * up to the order of the fp32 partial sums).  With stacked weights, when
- * every CTA of its grid fits on the device at once, both halves run in ONE
- * kernel whose CTAs hand each tile's partials over through arrival counters
- * in the workspace (release / acquire, bounded waits), bit for bit the
- * results of the two halves; else the two halves run as two kernels.  Else
- * the kernels of lora_shrink and lora_expand run unchanged.  Either way the
- * work stays on the GPU; lora_shrink_expand_path tells which path a shape
- * takes.  The split paths keep state in the workspace (partial tiles, arrival
- * counters that lora_prepare_metadata zeroes when its workspace_bytes covers
- * them): pass the same workspace size to lora_prepare_metadata, and order
- * calls that share a workspace on one stream.
+ * up to the order of the fp32 partial sums).  Else the kernels of
+ * lora_shrink and lora_expand run unchanged.  Either way the work stays on
+ * the GPU; lora_shrink_expand_path tells which path a shape takes.  The
+ * split-K path keeps its partial tiles in the workspace: order calls that
+ * share a workspace on one stream.
  */
 int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
                        const uint16_t *const *lora_a, const uint16_t *const *lora_b,
@@ -214,11 +208,10 @@ int lora_shrink_expand(const uint16_t *x, int64_t x_row_stride, int64_t hidden,
 
 /*
  * Workspace bytes that let lora_shrink_expand take its split-K path for this
- * shape: lora_workspace_size, then one 4-byte arrival counter per 16-token
- * tile of the batch (rounded up to 256 bytes), then P * 16 * num_slices *
- * rank * 4 bytes of partial tiles per 16-token tile (P = 16 for rank <= 16,
- * 8 for rank 32: the largest split) when max_num_tokens <= 1024 and
- * rank <= 32 (else just lora_workspace_size); 0 for sizes the calls reject.
+ * shape: lora_workspace_size plus P * 16 * num_slices * rank * 4 bytes of
+ * partial tiles per 16-token tile of the batch (P = 16 for rank <= 16, 8 for
+ * rank 32: the largest split) when max_num_tokens <= 1024 and rank <= 32
+ * (else just lora_workspace_size); 0 for sizes the calls reject.
  * A smaller workspace (at least lora_workspace_size) is still valid for
  * every call.
  */
@@ -316,9 +309,8 @@ int lora_shrink_expand_paged(const uint16_t *x, int64_t x_row_stride, int64_t hi
  *   - lora_shrink_partials splits each 16-token tile's hidden dimension over
  *     up to P CTAs (as for the workspace size above; no cluster) and writes
  *     each CTA's fp32 partial tile (its warps summed) into the workspace
- *     behind the metadata and the arrival counters:
- *     [tile][split][16][num_slices * rank].  It does not scale and does not
- *     write u.
+ *     behind the metadata: [tile][split][16][num_slices * rank].  It does not
+ *     scale and does not write u.
  *   - lora_expand_partials takes `hidden` (it fixes the split), `scale` and
  *     `lora_scales`, sums each tile's partials in CTA order, multiplies by
  *     c(lora) as lora_shrink does, writes the result to u (rows of tokens
@@ -357,17 +349,12 @@ int lora_shrink_expand_kernels(int64_t max_num_tokens, int64_t max_loras, int64_
  * and the current device; host-only, no GPU work:
  *   LORA_PATH_FUSED        one kernel holding a tile's whole problem on chip
  *                          (tiny batches; never with paged weights)
- *   LORA_PATH_SPLIT_FUSED  one kernel: the split-K shrink, a hand-off through
- *                          per-tile arrival counters in the workspace, then
- *                          the expand (decode-sized batches whose grid fits
- *                          the device at once; stacked weights)
  *   LORA_PATH_SPLIT_PAIR   the split-K shrink, then the partial-sum expand
+ *                          (needs lora_shrink_expand_workspace_size bytes)
  *   LORA_PATH_PAIR         the kernels of lora_shrink, then of lora_expand
- * The split paths need a workspace of lora_shrink_expand_workspace_size bytes.
  * A negative LORA_ERR_* code for sizes the calls reject.
  */
 #define LORA_PATH_FUSED 1
-#define LORA_PATH_SPLIT_FUSED 2
 #define LORA_PATH_SPLIT_PAIR 3
 #define LORA_PATH_PAIR 4
 int lora_shrink_expand_path(int64_t max_num_tokens, int64_t max_loras, int64_t hidden,

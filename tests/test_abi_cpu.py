@@ -63,15 +63,13 @@ def test_workspace_size(lib):
 
 def test_shrink_expand_workspace_size(lib):
     base = binding.lora_workspace_size(256, 4)
-    # split-K path: one arrival counter per 16-token tile (rounded up to 256
-    # bytes), then up to 16 (rank <= 16) or 8 (rank 32) partial tiles of
-    # 16 rows x S*R floats per tile
+    # split-K path: up to 16 (rank <= 16) or 8 (rank 32) partial tiles of
+    # 16 rows x S*R floats per 16-token tile
     tiles = 256 // 16 + 4
-    counters = (tiles * 4 + 255) // 256 * 256
     assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4096,) * 3, 8) == \
-        base + counters + tiles * 16 * 16 * 24 * 4
+        base + tiles * 16 * 16 * 24 * 4
     assert binding.lora_shrink_expand_workspace_size(256, 4, 4096, (4096,), 32) == \
-        base + counters + tiles * 8 * 16 * 32 * 4
+        base + tiles * 8 * 16 * 32 * 4
     # beyond 1024 tokens or rank 32 only the metadata part
     assert binding.lora_shrink_expand_workspace_size(2048, 4, 4096, (4096,), 16) == \
         binding.lora_workspace_size(2048, 4)

@@ -451,10 +451,8 @@ def _path_of(case):
 def test_split_k_one_call_matches_the_oracle(name, spec, dev):
     case = _split_case(name, spec, dev)
     assert case.ws.view.numel() > case.ws_base  # the larger workspace was offered
-    path = _path_of(case)
-    assert path in (binding.LORA_PATH_SPLIT_FUSED, binding.LORA_PATH_SPLIT_PAIR)
+    assert _path_of(case) == binding.LORA_PATH_SPLIT_PAIR
     check_case(case, fused=True)   # every adapter row
-    print(name, binding.PATH_NAMES[path])
     # the split-K path ran: its partial tiles landed behind the metadata
     assert torch.any(case.ws.view[case.ws_base:] != 0)
 
@@ -829,26 +827,23 @@ def test_batch_without_adapter_tokens_after_a_kernel_that_writes_y(one_call, dev
     assert torch.all(case.u.view.view(torch.int32) == U_SENTINEL_BITS)
 
 
-# ------------------------------------------------------------ the split-K one-kernel path
+# ------------------------------------------------------------ one-call paths
 
 def test_path_query_names_each_path(dev):
-    """lora_shrink_expand_path: decode takes the split-K one-kernel path with
-    the larger workspace and the cluster pair without it; tiny batches the
-    fused kernel; a rank-32 three-slice batch with a long hidden dimension
-    (its CTAs' k-ranges do not fit on chip) the split-K pair; paged weights
-    never the one-kernel paths."""
+    """lora_shrink_expand_path: decode takes the split-K pair with the larger
+    workspace and the cluster pair without it; tiny batches the fused kernel
+    (never with paged weights); prefill the cluster pair."""
     q = binding.lora_shrink_expand_path
     dq = W.CONFIGS["decode_qkv"]
     big = binding.lora_shrink_expand_workspace_size(256, 4, 4096, dq.slice_widths, 8)
     base = binding.lora_workspace_size(256, 4)
-    assert q(256, 4, 4096, dq.slice_widths, 8, big) == binding.LORA_PATH_SPLIT_FUSED
-    assert q(256, 4, 4096, dq.slice_widths, 8, big, fp16=True) == binding.LORA_PATH_SPLIT_FUSED
+    assert q(256, 4, 4096, dq.slice_widths, 8, big) == binding.LORA_PATH_SPLIT_PAIR
+    assert q(256, 4, 4096, dq.slice_widths, 8, big, fp16=True) == binding.LORA_PATH_SPLIT_PAIR
     assert q(256, 4, 4096, dq.slice_widths, 8, base) == binding.LORA_PATH_PAIR
     assert q(256, 4, 4096, dq.slice_widths, 8, big, paged=True) == binding.LORA_PATH_SPLIT_PAIR
-    assert q(64, 4, 512, (512,), 8, binding.lora_workspace_size(64, 4)) == binding.LORA_PATH_FUSED
-    w32 = (1032, 520, 264)
-    big32 = binding.lora_shrink_expand_workspace_size(1000, 5, 8264, w32, 32)
-    assert q(1000, 5, 8264, w32, 32, big32) == binding.LORA_PATH_SPLIT_PAIR
+    tiny_ws = binding.lora_workspace_size(64, 4)
+    assert q(64, 4, 512, (512,), 8, tiny_ws) == binding.LORA_PATH_FUSED
+    assert q(64, 4, 512, (512,), 8, tiny_ws, paged=True) == binding.LORA_PATH_PAIR
     pf = W.CONFIGS["chunked_prefill"]
     assert q(8192, 8, 4096, pf.slice_widths, 16,
              binding.lora_workspace_size(8192, 8)) == binding.LORA_PATH_PAIR
@@ -863,19 +858,21 @@ def _layer_case(T, n, H, widths, L, R, seed, dev, ws_bytes):
     return case
 
 
-def test_split_one_kernel_layers_of_different_splits_share_a_workspace(dev):
-    """Layers of different hidden sizes (splits of 8 and 4) run one after the
-    other on one workspace, as a model's LoRA layers share one grouping: the
-    arrival counters carry over from launch to launch (every finished tile
-    adds 16), and every call gives the results of the two split-K halves bit
-    for bit."""
-    T, n, L, R, widths = 1024, 1000, 4, 8, (4096, 4096, 4096)
-    ws_bytes = max(binding.lora_shrink_expand_workspace_size(T, L, H, widths, R)
-                   for H in (4096, 1024))
+def test_split_k_layers_of_different_splits_share_a_workspace(dev):
+    """Layers of different hidden sizes (splits of 16 and 8) run one after
+    the other on one workspace, as a model's LoRA layers share one grouping:
+    each call's partial tiles overwrite the previous call's, and every call
+    gives the results of the two split-K halves run on a workspace of its
+    own bit for bit."""
+    # 16 adapters and wide slices keep the batch off the fused kernel; hidden
+    # 3072 gives 48 k-blocks (a split of 8), hidden 4096 64 (a split of 16)
+    T, n, L, R, widths = 256, 250, 16, 8, (8192, 4096, 4096)
+    hs = (4096, 3072, 4096)
+    ws_bytes = max(binding.lora_shrink_expand_workspace_size(T, L, H, widths, R) for H in hs)
     layers = [_layer_case(T, n, H, widths, L, R, 70 + i, dev, ws_bytes)
-              for i, H in enumerate((4096, 1024, 4096))]
+              for i, H in enumerate(hs)]
     for c in layers:
-        assert _path_of(c) == binding.LORA_PATH_SPLIT_FUSED
+        assert _path_of(c) == binding.LORA_PATH_SPLIT_PAIR, c.shape.hidden
     m = layers[0]
     for c in layers[1:]:   # one batch: the same mapping for every layer
         c.mapping.copy_(m.mapping)
@@ -898,4 +895,4 @@ def test_split_one_kernel_layers_of_different_splits_share_a_workspace(dev):
         torch.cuda.synchronize()
         assert torch.equal(c.y.view.view(torch.int16), ref.y.view.view(torch.int16)), i
         assert torch.equal(c.u.view.view(torch.int32), ref.u.view.view(torch.int32)), i
-    assert m.ws.view[:4].view(torch.int32).item() == 0   # no wait timed out
+    assert m.ws.view[:4].view(torch.int32).item() == 0   # status clean
