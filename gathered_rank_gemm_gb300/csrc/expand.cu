@@ -548,6 +548,10 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
 }
 
 int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
+  // ranks 64 and 128 on large batches: the tcgen05 kernel (128-token tiles)
+  const int tc = launch_expand_tc(a, stream);
+  if (tc < 0) return tc;
+  if (tc == 1) return 0;
   // small batches: 16-token tiles give more, shorter items (latency); large
   // batches: 32-token tiles amortise each item's B block over more rows
   if (a.max_num_tokens <= 1024) return launch_expand_bm<16>(a, stream);

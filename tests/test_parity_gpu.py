@@ -115,9 +115,9 @@ def test_many_loras_uses_every_bin(dev):
 
 # ------------------------------------------------------------ exact integer cases
 
-def _int_case(dev, T, H, sparse_k=None, seed=0, **kw):
+def _int_case(dev, T, H, sparse_k=None, seed=0, R=8, widths=(16, 8), **kw):
     rng = np.random.default_rng(seed)
-    L, R, widths = 3, 8, (16, 8)
+    L = 3
     if sparse_k is None:
         xi = rng.choice([-2, 0, 2], size=(T, H))
     else:
@@ -162,7 +162,7 @@ def test_small_integer_inputs_are_bit_exact(T, H, sparse, one_call, split_ws, ke
     u = case.u.view.cpu().numpy()
     y = oracle.bf16_bits_to_f64(bits_of(case.y.view))
     u_ref = oracle.shrink(case.layer.x, case.layer.lora_a, 0.5, m, T, 3,
-                          u_init=np.zeros((2, T, 8)))
+                          u_init=np.zeros((2, T, case.shape.rank)))
     y_ref = oracle.expand(u_ref, case.layer.lora_b, case.layer.y, m, T, 3)
     rows = lora_rows(m, T, 3)
     assert np.array_equal(u[:, rows].astype(np.float64), u_ref[:, rows])
@@ -896,3 +896,76 @@ def test_split_k_layers_of_different_splits_share_a_workspace(dev):
         assert torch.equal(c.y.view.view(torch.int16), ref.y.view.view(torch.int16)), i
         assert torch.equal(c.u.view.view(torch.int32), ref.u.view.view(torch.int32)), i
     assert m.ws.view[:4].view(torch.int32).item() == 0   # status clean
+
+
+# ------------------------------------------------------------ the tcgen05 expand (ranks 64 / 128)
+
+# more than 1024 tokens and rank 64 or 128: lora_expand runs the tcgen05 kernel
+# (128-token tiles, 128-column blocks, accumulators in tensor memory)
+TC_SHAPES = [
+    # (T, n, H, widths, L, R)
+    (2048, 1900, 512, (1032, 520, 264), 5, 64),   # three slices, partial column blocks
+    (1100, 1100, 256, (128,), 3, 128),            # one column block, ragged tiles
+    (4096, 3000, 384, (2048,), 40, 128),          # many adapters, mostly partial tiles
+    (1536, 1536, 1024, (264, 136), 2, 64),        # few adapters, several full tiles each
+]
+
+
+@pytest.mark.parametrize("one_call", [False, True])
+@pytest.mark.parametrize("T,n,H,widths,L,R", TC_SHAPES)
+def test_tcgen05_expand_matches_the_oracle(T, n, H, widths, L, R, one_call, dev):
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, neg_prob=0.15)
+    check_case(make_case(shape, dev, seed=T + R + len(widths)), fused=one_call)
+
+
+@pytest.mark.parametrize("T,n,H,widths,L,R", TC_SHAPES[:2])
+def test_tcgen05_expand_fp16_inputs(T, n, H, widths, L, R, dev):
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, scale=0.5, neg_prob=0.15)
+    rng = np.random.default_rng(T + 5)
+    case = DeviceCase(shape, W.make_mapping(shape, rng), W.make_layer(shape, rng), dev, f16=True)
+    check_case(case, fused=True)
+
+
+@pytest.mark.parametrize("R", [64, 128])
+def test_tcgen05_expand_small_integers_are_bit_exact(R, dev):
+    """Integer x, A, B and y keep u and every partial sum of the expand exact
+    in fp32 whatever the summation order, so the tensor-memory accumulation
+    must give the oracle's exact y rounded once to bf16 (round to nearest
+    even; sums of up to 128 terms can exceed bf16's exact integers), bit for
+    bit, and the oracle's u exactly."""
+    T, H = 1100, 64
+    case, (xi, ai, bi, yi, m) = _int_case(dev, T, H, 16, seed=R, R=R, widths=(136, 264))
+    case.run()
+    u_ref = oracle.shrink(case.layer.x, case.layer.lora_a, 0.5, m, T, 3,
+                          u_init=np.zeros((2, T, R)))
+    y_ref = oracle.expand(u_ref, case.layer.lora_b, case.layer.y, m, T, 3)
+    assert np.all(np.abs(y_ref) < 2 ** 24) and np.array_equal(y_ref, np.round(y_ref))
+    rows = lora_rows(m, T, 3)
+    assert np.array_equal(case.u.view.cpu().numpy()[:, rows].astype(np.float64), u_ref[:, rows])
+    assert np.array_equal(bits_of(case.y.view), W.f32_to_bf16_bits(y_ref.astype(np.float32)))
+
+
+def test_tcgen05_expand_alone_equals_the_oracle_on_the_gpu_u(dev):
+    """The expand by itself on a u the test writes (every row of every slice
+    set, not only adapter rows): only adapter rows of y change, by exactly the
+    oracle's expand of that u within the bar."""
+    shape = W.custom_shape(max_num_tokens=2048, num_tokens=2000, hidden=64,
+                           slice_widths=(1024, 512), max_loras=6, rank=128, neg_prob=0.2)
+    case = make_case(shape, dev, seed=91)
+    case.prepare()
+    rng = np.random.default_rng(92)
+    u = rng.standard_normal((2, 2048, 128)).astype(np.float32)
+    case.u.view.copy_(torch.from_numpy(u))
+    case.expand()
+    torch.cuda.synchronize()
+    y_ref = oracle.expand(u.astype(np.float64), case.layer.lora_b, case.y_in_bits[:, :1536],
+                          case.mapping_np, 2000, 6)
+    y = oracle.bf16_bits_to_f64(bits_of(case.y_view))
+    rows = lora_rows(case.mapping_np, 2000, 6)
+    ok, worst = within_tol(y[rows], y_ref[rows])
+    assert ok, worst
+    keep = np.setdiff1d(np.arange(2048), rows)
+    assert np.array_equal(bits_of(case.y.view)[keep], case.y_in_bits[keep])
+    assert case.guards_intact()
