@@ -657,6 +657,19 @@ def run_ours(args, world, rank, local):
     clocks = ClockSampler(local)
     clocks.start()
     records, head = {}, None
+    if args.mode == "profile":
+        # eager steps only (grouping + every layer's call), for profiler launch lists
+        clocks.stop()
+        run = WorkloadRun(args, W.CONFIGS[headline], dev, stream, rank, l2)
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                run.launch("metadata")
+                run.launch("layers")
+        stream.synchronize()
+        if rank == 0:
+            print(json.dumps({"mode": "profile", "workload": headline, "layers": run.layers,
+                              "steps": args.steps, "path": binding.PATH_NAMES[run.path]}))
+        return 0
     try:
         for name in names:
             run = WorkloadRun(args, W.CONFIGS[name], dev, stream, rank, l2)
@@ -758,6 +771,8 @@ def parse_args(argv=None):
     ap.add_argument("--lora-scales", action="store_true", help="per-adapter scale factors")
     ap.add_argument("--dtype", choices=["bf16", "f16"], default="bf16",
                     help="type of x, A, B and y (fp32 accumulation either way)")
+    ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
+                    help="profile: only run --steps eager steps of one workload (for ncu)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 0)
     return args

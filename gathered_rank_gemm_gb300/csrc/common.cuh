@@ -269,6 +269,37 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (global_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }
+// mbar_wait for kernels with many waiting warps: one lane of the warp waits,
+// suspended in the barrier (a suspend-time hint instead of a polling loop),
+// and the other lanes wait at the warp barrier, so waiting warps take no issue
+// slots from working ones.  The warp barrier orders the waiting lane's
+// observation before the other lanes' reads.  Every lane gets the result.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    if (!mbar_try_wait_sleep(bar, parity)) {
+      const unsigned long long t0 = global_ns();
+      while (!mbar_try_wait_sleep(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) {
+          ok = false;
+          break;
+        }
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return ok;
+}
 // global -> shared bulk copy (16-byte aligned, size a multiple of 16) that
 // completes `bytes` transactions on the mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

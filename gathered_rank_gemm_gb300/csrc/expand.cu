@@ -548,7 +548,7 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
 }
 
 int launch_expand(const ExpandArgs& a, cudaStream_t stream) {
-  // ranks 64 and 128 on large batches: the tcgen05 kernel (128-token tiles)
+  // rank 128 on large batches: the tcgen05 kernel (128-token tiles)
   const int tc = launch_expand_tc(a, stream);
   if (tc < 0) return tc;
   if (tc == 1) return 0;

@@ -102,8 +102,8 @@ struct ExpandArgs {
   bool y_early = false;
 };
 int launch_expand(const ExpandArgs& a, cudaStream_t stream);
-// The tcgen05 expand (ranks 64 and 128, stacked weights, more than 1024
-// tokens): 1 when launched, 0 when the arguments are not its case, < 0 on error.
+// The tcgen05 expand (rank 128, stacked weights, more than 1024 tokens): 1
+// when launched, 0 when the arguments are not its case, < 0 on error.
 int launch_expand_tc(const ExpandArgs& a, cudaStream_t stream);
 int expand_tc_applies(const ExpandArgs& a);
 

@@ -900,14 +900,16 @@ def test_split_k_layers_of_different_splits_share_a_workspace(dev):
 
 # ------------------------------------------------------------ the tcgen05 expand (ranks 64 / 128)
 
-# more than 1024 tokens and rank 64 or 128: lora_expand runs the tcgen05 kernel
-# (128-token tiles, 128-column blocks, accumulators in tensor memory)
+# more than 1024 tokens and rank 128: lora_expand runs the tcgen05 kernel
+# (128-token tiles, 128-column blocks, accumulators in tensor memory); the
+# rank-64 shapes run the mma.sync kernel beside them
 TC_SHAPES = [
     # (T, n, H, widths, L, R)
-    (2048, 1900, 512, (1032, 520, 264), 5, 64),   # three slices, partial column blocks
+    (2048, 1900, 512, (1032, 520, 264), 5, 128),  # three slices, partial column blocks
     (1100, 1100, 256, (128,), 3, 128),            # one column block, ragged tiles
     (4096, 3000, 384, (2048,), 40, 128),          # many adapters, mostly partial tiles
-    (1536, 1536, 1024, (264, 136), 2, 64),        # few adapters, several full tiles each
+    (1536, 1536, 1024, (264, 136), 2, 128),       # few adapters, several full tiles each
+    (2048, 1900, 512, (1032, 520, 264), 5, 64),   # rank 64: the mma.sync kernel
 ]
 
 
@@ -928,7 +930,7 @@ def test_tcgen05_expand_fp16_inputs(T, n, H, widths, L, R, dev):
     check_case(case, fused=True)
 
 
-@pytest.mark.parametrize("R", [64, 128])
+@pytest.mark.parametrize("R", [128])
 def test_tcgen05_expand_small_integers_are_bit_exact(R, dev):
     """Integer x, A, B and y keep u and every partial sum of the expand exact
     in fp32 whatever the summation order, so the tensor-memory accumulation
