@@ -35,7 +35,8 @@ EXPORTED = ("lora_workspace_size", "lora_prepare_metadata", "lora_shrink", "lora
             "lora_shrink_expand_workspace_size", "lora_shrink_partials", "lora_expand_partials",
             "lora_shrink_paged", "lora_expand_paged", "lora_shrink_expand_paged",
             "lora_shrink_f16", "lora_expand_f16", "lora_shrink_expand_f16",
-            "lora_shrink_partials_f16", "lora_expand_partials_f16", "lora_shrink_expand_path")
+            "lora_shrink_partials_f16", "lora_expand_partials_f16", "lora_shrink_expand_path",
+            "lora_testing_inject_timeout")
 
 LORA_PATH_FUSED = 1
 LORA_PATH_SPLIT_PAIR = 3
@@ -104,6 +105,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         f16.argtypes = getattr(lib, name).argtypes
     lib.lora_shrink_expand_path.restype = i32
     lib.lora_shrink_expand_path.argtypes = [i64, i64, i64, p, i32, i32, sz, i32, i32]
+    lib.lora_testing_inject_timeout.restype = i32
+    lib.lora_testing_inject_timeout.argtypes = [i32]
     lib.lora_apply_noalloc.restype = i32
     lib.lora_apply_noalloc.argtypes = [p, p, i64, i64, p, i64, i64, p, p, p, i32, i32,
                                        ctypes.c_float, p, p, p, i64, p, p, p, p, p]
@@ -398,6 +401,13 @@ def lora_read_status(workspace, stream=None) -> int:
                                  _stream_ptr(stream, workspace.device))
     _check("lora_read_status", rc)
     return int(out.value)
+
+
+def lora_testing_inject_timeout(on: bool) -> bool:
+    """Test hook (include/gathered_rank_gemm_testing.h): while on, the shrink
+    kernel's bounded waits run out after 1 ms and it reports
+    LORA_STATUS_TIMEOUT.  Returns the previous setting."""
+    return bool(load().lora_testing_inject_timeout(1 if on else 0))
 
 
 @_on_tensor_device

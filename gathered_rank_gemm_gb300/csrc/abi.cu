@@ -3,6 +3,7 @@
 #include <cstdint>
 
 #include "gathered_rank_gemm.h"
+#include "gathered_rank_gemm_testing.h"
 #include "common.cuh"
 #include "launch.h"
 
@@ -586,6 +587,8 @@ int lora_read_status(void* workspace, uint32_t* status, void* stream) {
   *status = host;
   return LORA_OK;
 }
+
+int lora_testing_inject_timeout(int on) { return grg::set_wait_fault(on); }
 
 const char* lora_error_string(int code) {
   switch (code) {

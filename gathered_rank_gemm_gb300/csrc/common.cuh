@@ -119,14 +119,6 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
   return pol;
 }
-// cp_async_16 with an L2 cache policy.
-__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, bool pred,
-                                                 uint64_t pol) {
-  const int bytes = pred ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;\n" ::"r"(dst),
-               "l"(src), "r"(bytes), "l"(pol)
-               : "memory");
-}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
@@ -261,45 +253,43 @@ __device__ __forceinline__ void mbar_arrive_count(uint32_t bar, uint32_t count) 
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
-// Waits for the phase with the given parity; false if the time limit passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Bounded waiting by a CTA that gives up as a whole.  The first of its waits
+// that runs out sets a flag in the CTA's shared memory; every later wait then
+// returns false at once, the kernel issues no further copy and stores no
+// output, and before it exits it waits (bounded again, mbar_drain) for the
+// bulk copies it had already issued, so that none is still writing its shared
+// memory when it leaves.  Every block-wide or named barrier is still reached
+// by every thread: giving up changes no control flow around them.
+struct CtaAbort {
+  volatile int* flag;           // in shared memory, 0 until a wait runs out
+  unsigned long long limit_ns;  // kWaitLimitNs, or 1 ms under the test hook
+  __device__ __forceinline__ bool raised() const { return *flag != 0; }
+  // Waits for the phase with the given parity; false if the time limit
+  // passed (which raises the flag) or the flag was already up.
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (*flag != 0) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+      if (*flag != 0) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *flag = 1;
+        return false;
+      }
+    }
+    return true;
+  }
+};
+// After giving up: waits, with the limit, for a copy issued on the barrier's
+// phase of the given parity to land.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long limit_ns) {
   const unsigned long long t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+    if (global_ns() - t0 > limit_ns) return;
 }
-// mbar_wait for kernels with many waiting warps: one lane of the warp waits,
-// suspended in the barrier (a suspend-time hint instead of a polling loop),
-// and the other lanes wait at the warp barrier, so waiting warps take no issue
-// slots from working ones.  The warp barrier orders the waiting lane's
-// observation before the other lanes' reads.  Every lane gets the result.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(20000u)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool warp_mbar_wait(uint32_t bar, uint32_t parity) {
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) {
-    if (!mbar_try_wait_sleep(bar, parity)) {
-      const unsigned long long t0 = global_ns();
-      while (!mbar_try_wait_sleep(bar, parity))
-        if (global_ns() - t0 > kWaitLimitNs) {
-          ok = false;
-          break;
-        }
-    }
-  }
-  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-  __syncwarp();
-  return ok;
-}
+// The test hook's wait limit.
+constexpr unsigned long long kTestWaitLimitNs = 1000ull * 1000ull;
 // global -> shared bulk copy (16-byte aligned, size a multiple of 16) that
 // completes `bytes` transactions on the mbarrier.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,

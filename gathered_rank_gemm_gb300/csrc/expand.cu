@@ -62,6 +62,10 @@ struct ExpandParams {
   uint32_t* status;
   int tile_capacity;
   int num_loras;
+  // the bounded waits' limit; under the test hook (wait_fault) no copy is
+  // issued and the first record barrier is armed with one arrival too many
+  unsigned long long wait_limit_ns;
+  int wait_fault;
 };
 
 
@@ -78,7 +82,9 @@ struct ExpandLayout {
   static constexpr int kRecBytes = record_ints(BM) * 4;
   static constexpr int kRec = NS * kStage;
   static constexpr int kBar = kRec + kRecSlots * kRecBytes;  // NS stage + kRecSlots record barriers
-  static constexpr int kSmem = 1024 + kBar + 8 * (NS + kRecSlots);
+  // then the CtaAbort flag and thread 0's last record / B block issued
+  static constexpr int kFlag = kBar + 8 * (NS + kRecSlots);
+  static constexpr int kSmem = 1024 + kFlag + 16;
 };
 
 // Stage count per rank (more stages cost occupancy: two stages at three
@@ -122,8 +128,17 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     return;
   }
 
+  // giving up (CtaAbort): no copy and no store once a wait has run out, nor
+  // under the test hook
+  volatile int* const flags = reinterpret_cast<int*>(smem + Lay::kFlag);
+  const CtaAbort cta_abort{flags, p.wait_limit_ns};
+  auto stopped = [&]() { return cta_abort.raised() || p.wait_fault != 0; };
   if (tid == 0) {
-    for (int s = 0; s < NS + RS; ++s) mbar_init(stage_bar + 8 * s, 1);
+    flags[0] = 0;
+    flags[1] = -1;  // the last item whose record went out
+    flags[2] = -1;  // the last item whose B block went out
+    for (int s = 0; s < NS + RS; ++s)
+      mbar_init(stage_bar + 8 * s, 1 + (p.wait_fault && s == NS ? 1 : 0));
     fence_mbar_init();
     if constexpr (!PAGED)
       for (int s = 0; s < 3; ++s) prefetch_tmap(&p.tmap[s]);
@@ -158,18 +173,19 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
   };
   // tile record of item k -> its slot (thread 0, bulk copy on the slot's barrier)
   auto issue_rec = [&](int k) {
+    if (stopped()) return;
+    flags[1] = k;
     const uint32_t bar = rec_bar + 8 * (k % RS);
     mbar_arrive_expect_tx(bar, Lay::kRecBytes);
     bulk_g2s(smem_u32(rec_of(k)),
              p.records + static_cast<long long>(item_of(k).tile) * record_ints(BM), Lay::kRecBytes,
              bar);
   };
-  bool timed_out = false;
-  auto wait_rec = [&](int k) {
-    if (!mbar_wait(rec_bar + 8 * (k % RS), (k / RS) & 1)) timed_out = true;
-  };
+  auto wait_rec = [&](int k) { cta_abort.wait(rec_bar + 8 * (k % RS), (k / RS) & 1); };
   // B block of item k -> stage (thread 0): boxes starting past the slice are skipped
   auto issue_b = [&](int k) {
+    if (stopped()) return;
+    flags[2] = k;
     const Item it = item_of(k);
     const TileView tv = TileView::of(rec_of(k), BM, p.num_loras);
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
@@ -192,6 +208,7 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
     const int ych = tid & 31;
     const int col = it.c0 + ych * 8;
+    if (stopped()) return;  // (the group is closed by issue_u all the same)
 #pragma unroll
     for (int i = 0; i < BM / 4; ++i) {
       const int row = (tid >> 5) + 4 * i;
@@ -225,6 +242,10 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     const TileView tv = TileView::of(rec, BM, p.num_loras);
     const uint32_t st = sbase + (k % NS) * Lay::kStage;
     constexpr int UCH = RANK / 4;  // 16-byte chunks per u row
+    if (stopped()) {
+      cp_async_commit();  // an empty group: the count of groups stays the same
+      return;
+    }
     if constexpr (PARTIAL) {
       // the split's partial rows of this slice (the valid rows only)
       const float* base = p.partials + static_cast<long long>(it.tile) * p.split * BM * p.sr +
@@ -279,7 +300,7 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     // the wait only L2 prefetches (L2 is the coherence point, so the copies
     // after the wait read the final values) of item 0's B block and y rows
     wait_rec(0);
-    {
+    if (!stopped()) {  // (no prefetch from a record that did not arrive)
       const Item it = item_of(0);
       const int32_t* rec = rec_of(0);
       const TileView tv = TileView::of(rec, BM, p.num_loras);
@@ -312,7 +333,7 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     // item k's copies: its cp.async group (later groups may stay pending) and its B block
     cp_async_wait_dyn(min(NS, nloc - k) - 1);
     __syncthreads();
-    if (!mbar_wait(stage_bar + 8 * (k % NS), (k / NS) & 1)) timed_out = true;
+    cta_abort.wait(stage_bar + 8 * (k % NS), (k / NS) & 1);  // (after giving up: garbage in)
 
     const Item it = item_of(k);
     const int32_t* rec = rec_of(k);
@@ -343,7 +364,7 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
         }
         *reinterpret_cast<float4*>(stp + Lay::kU + row * Lay::kUPitch + ch * 16) = sum;
         const int t = record_token(rec, row, tv.count, p.max_num_tokens);
-        if (it.c0 == 0 && t >= 0)
+        if (it.c0 == 0 && t >= 0 && !stopped())
           *reinterpret_cast<float4*>(const_cast<float*>(p.u) +
                                      (static_cast<long long>(it.s) * p.max_num_tokens + t) * RANK +
                                      ch * 4) = sum;
@@ -423,8 +444,9 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     }
     __syncthreads();  // the updated stage is complete
 
-    // coalesced 16-byte stores of the valid rows and columns
-    {
+    // coalesced 16-byte stores of the valid rows and columns (none once the
+    // CTA has given up; every wait of this item is over, so one value for all)
+    if (!stopped()) {
       const int ych = tid & 31;
       const int col = it.c0 + ych * 8;
 #pragma unroll
@@ -446,7 +468,19 @@ __global__ void __launch_bounds__(kExpandThreads, RANK >= 64 ? 2 : 4)
     }
     if (tid == 0 && k + RS < nloc) issue_rec(k + RS);
   }
-  if (timed_out) atomicOr(p.status, kStatusTimeout);
+  // Leave with no copy in flight: the cp.async groups, and after giving up
+  // thread 0's last bulk copies (a slot is refilled only once its previous
+  // contents were consumed, so only the last NS B blocks and RS records can be
+  // pending; waiting on one that landed returns at once).  The flag is final
+  // here: the last item's waits came before its block-wide barriers.
+  cp_async_wait<0>();
+  if (tid == 0 && cta_abort.raised()) {
+    for (int k = max(0, flags[2] - NS + 1); k <= flags[2]; ++k)
+      mbar_drain(stage_bar + 8 * (k % NS), (k / NS) & 1, p.wait_limit_ns);
+    for (int k = max(0, flags[1] - RS + 1); k <= flags[1]; ++k)
+      mbar_drain(rec_bar + 8 * (k % RS), (k / RS) & 1, p.wait_limit_ns);
+    atomicOr(p.status, kStatusTimeout);
+  }
 }
 
 template <int BM, int RANK, bool PARTIAL>
@@ -523,6 +557,8 @@ static int launch_expand_bm(const ExpandArgs& a, cudaStream_t stream) {
   p.tile_capacity =
       static_cast<int>(tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM)));
   p.num_loras = a.num_loras;
+  p.wait_fault = wait_fault() ? 1 : 0;
+  p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   const long long max_items = static_cast<long long>(p.tile_capacity) * cb_total;
   if (a.partials != nullptr) {
     // partial mode: 16-token tiles and ranks up to 32 only

@@ -70,7 +70,12 @@ struct ExpandTcParams {
   int off_b;
   int off_y;        // [group][nsy] y stages
   int off_tok;      // [group][nsy][kTcCPW][128] token of each row
-  int off_bar;
+  int off_bar;      // the barriers, then three ints: the abort flag, the last
+                    // item whose B block went out, the last item committed
+  // the bounded waits' limit; under the test hook (wait_fault) no copy is
+  // issued and the first B barrier is armed with one arrival too many
+  unsigned long long wait_limit_ns;
+  int wait_fault;
 };
 
 // tcgen05 shared-memory matrix descriptor, 128-byte swizzle.
@@ -161,9 +166,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   const int nloc = static_cast<int>(it1 - it0);
 
+  // giving up (CtaAbort): no copy, no MMA and no store once a wait has run
+  // out, nor under the test hook
+  volatile int* const flags = reinterpret_cast<int*>(smem + p.off_bar + 8 * (2 * NSB + 5));
+  const CtaAbort cta_abort{flags, p.wait_limit_ns};
+  auto stopped = [&]() { return cta_abort.raised() || p.wait_fault != 0; };
   if (tid == 0) {
+    flags[0] = 0;
+    flags[1] = -1;
+    flags[2] = -1;
     for (int i = 0; i < NSB; ++i) {
-      mbar_init(full_b + 8 * i, 1);                 // the producer's expect_tx
+      // the producer's expect_tx (+ one that never comes: the test hook)
+      mbar_init(full_b + 8 * i, 1 + (p.wait_fault && i == 0 ? 1 : 0));
       mbar_init(empty_b + 8 * i, kTcGroupWarps);    // the warps of the item's group
     }
     for (int i = 0; i < 2; ++i) {
@@ -222,7 +236,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tv.count = ok ? h.y : 0;
     return tv;
   };
-  bool timed_out = false;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
@@ -246,14 +259,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           pf_tile = pf.tile;
           pf_lora = tile_head(pf_tile).lora;
         }
-        if (lane == 0) {
+        if (lane == 0 && !stopped()) {
           const int boxes = min(2, (pf.width - pf.c0 + 63) / 64);
           for (int bx = 0; bx < boxes; ++bx)
             tma_prefetch_2d(&p.tmap[pf.s], pf.c0 + 64 * bx, pf_lora * RANK);
         }
       }
-      if (k >= NSB && !mbar_wait(empty_b + 8 * si, ((k / NSB) - 1) & 1)) timed_out = true;
-      if (lane == 0) {
+      if (k >= NSB) cta_abort.wait(empty_b + 8 * si, ((k / NSB) - 1) & 1);
+      if (lane == 0 && !stopped()) {
+        flags[1] = k;
         const uint32_t st = sbase + p.off_b + si * kBBytes;
         const int boxes = min(2, (it.width - it.c0 + 63) / 64);
         const uint32_t bar = full_b + 8 * si;
@@ -271,14 +285,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int k = 0; k < nloc; ++k, it.next(p, cbt)) {
       const int si = k % NSB, b = k & 1;
       if (it.group != group) {  // wait for the new u tile
-        if (!mbar_wait(u_ready, ngroups & 1)) timed_out = true;
+        cta_abort.wait(u_ready, ngroups & 1);
         group = it.group;
         ++ngroups;
       }
-      if (!mbar_wait(full_b + 8 * si, (k / NSB) & 1)) timed_out = true;
-      if (k >= 2 && !mbar_wait(acc_empty + 8 * b, ((k >> 1) - 1) & 1)) timed_out = true;
+      cta_abort.wait(full_b + 8 * si, (k / NSB) & 1);
+      if (k >= 2) cta_abort.wait(acc_empty + 8 * b, ((k >> 1) - 1) & 1);
       tc_fence_after();
-      if (lane == 0) {
+      if (lane == 0 && !stopped()) {
         const uint32_t d = taddr + b * kAccCols;
         const uint32_t sbm = sbase + p.off_b + si * kBBytes;
         const uint32_t su = sbase + p.off_u;
@@ -293,6 +307,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         umma_commit(acc_full + 8 * b);
+        flags[2] = k;
       }
       __syncwarp();
     }
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int v = __ldcg(rec + kRecordHeaderInts + row);
         cur_tok = (row < tv.count && v >= 0 && v < p.max_num_tokens) ? v : -1;
       }
-      const int t = cur_tok;
+      const int t = stopped() ? -1 : cur_tok;  // no copy once the CTA has given up
       tok_at(j, row) = t;
       if (t >= 0) {
         const uint32_t dst = sbase + ystage(j) + row * kTcYPitch + part * CW * 2;
@@ -353,8 +368,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     };
     const int mine = (nloc - grp + 1) / 2;  // items of this group
     for (int i = 0; i < min(NSY, mine); ++i) issue_y();
-    int ugroup = first.group;               // the u tile the MMA warp works on
-    Item prev = first;                      // item k - 1 (for the u hand-over)
+      Item prev = first;                      // item k - 1 (for the u hand-over)
     Item it = first;
     if (grp == 1) {
       prev = first;
@@ -370,8 +384,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // has completed (item k - 1's accumulator is full: the other group's
         // item), split the new u rows into the swizzled K-major high / residual
         // operands (each part its chunks)
-        if (k > 0 && !mbar_wait(acc_full + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1))
-          timed_out = true;
+        if (k > 0) cta_abort.wait(acc_full + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1);
         const float* urow =
             p.u + (static_cast<long long>(it.s) * p.max_num_tokens + (t >= 0 ? t : 0)) * RANK;
         unsigned char* uh = smem + p.off_u;
@@ -400,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // a warp whose 32 rows hold no token only frees the accumulator and B block
       const bool active = __any_sync(0xffffffffu, t >= 0);
       cp_async_wait_dyn(min(NSY, mine - i) - 1);  // my y segment of item k has landed
-      if (!mbar_wait(acc_full + 8 * b, (k >> 1) & 1)) timed_out = true;
+      cta_abort.wait(acc_full + 8 * b, (k >> 1) & 1);
       tc_fence_after();
       if (!active) {
         tc_fence_before();
@@ -454,7 +467,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int r0 = 0; r0 < 32; r0 += RPI) {
           const int r = 32 * quarter + r0 + lane / CCH;
           const int tr = tok_at(j, r);
-          if (tr >= 0 && col < it.width)
+          if (tr >= 0 && col < it.width && !stopped())
             *reinterpret_cast<int4*>(p.y + static_cast<long long>(tr) * p.y_stride + it.off +
                                      col) =
                 *reinterpret_cast<const int4*>(ys + r * kTcYPitch + part * CW * 2 + ch * 16);
@@ -467,18 +480,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       it.next(p, cbt);
       it.next(p, cbt);
     }
-    (void)ugroup;
     cp_async_wait<0>();
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1)
+  // After giving up (the flag is final here: every wait came before the
+  // barrier above), the producer's last TMA loads land and the last MMAs
+  // complete (their commit) before the CTA frees its TMEM and leaves; waiting
+  // on a copy that landed returns at once.
+  const bool gave_up = cta_abort.raised();
+  if (gave_up && warp == 0 && lane == 0)
+    for (int k = max(0, flags[1] - NSB + 1); k <= flags[1]; ++k)
+      mbar_drain(full_b + 8 * (k % NSB), (k / NSB) & 1, p.wait_limit_ns);
+  if (warp == 1) {
+    if (gave_up) {
+      if (lane == 0 && flags[2] >= 0)
+        mbar_drain(acc_full + 8 * (flags[2] & 1), (flags[2] >> 1) & 1, p.wait_limit_ns);
+      __syncwarp();
+    }
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr),
                  "r"(2 * kAccCols)
                  : "memory");
-  if (timed_out) atomicOr(p.status, kStatusTimeout);
+  }
+  if (tid == 0 && gave_up) atomicOr(p.status, kStatusTimeout);
 }
 
 namespace {
@@ -493,7 +519,7 @@ int run_expand_tc(ExpandTcParams& p, cudaStream_t stream) {
   p.off_y = p.off_b + p.nsb * 2 * RANK * 128;
   p.off_tok = p.off_y + kTcGroups * p.nsy * kTcBM * kTcYPitch;
   p.off_bar = p.off_tok + kTcGroups * p.nsy * kTcCPW * kTcBM * 4;
-  const size_t smem = 1024 + static_cast<size_t>(p.off_bar) + 8 * (2 * p.nsb + 5);
+  const size_t smem = 1024 + static_cast<size_t>(p.off_bar) + 8 * (2 * p.nsb + 5) + 16;
   const void* fn = reinterpret_cast<const void*>(lora_expand_tc_kernel<RANK, F16>);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
@@ -549,6 +575,8 @@ int launch_expand_tc(const ExpandArgs& a, cudaStream_t stream) {
   p.tile_capacity =
       static_cast<int>(tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(kTcBM)));
   p.num_loras = a.num_loras;
+  p.wait_fault = wait_fault() ? 1 : 0;
+  p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   return a.f16 ? run_expand_tc<128, true>(p, stream) : run_expand_tc<128, false>(p, stream);
 }
 

@@ -65,6 +65,10 @@ struct FusedParams {
   int warps_n;
   int ntw;
   int off_a, off_x, off_b, off_y, off_u, off_red, off_rec, off_bar;
+  // the bounded waits' limit; under the test hook (wait_fault) no copy is
+  // issued and the first A barrier is armed with one arrival too many
+  unsigned long long wait_limit_ns;
+  int wait_fault;
 };
 
 template <int NTW, bool F16>
@@ -101,8 +105,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   const int un0 = crank * p.units_per_rank;
   const int nun = max(min(un0 + p.units_per_rank, units_total) - un0, 0);
 
+  // giving up (CtaAbort): the flag after the barriers; the CTA keeps walking
+  // its items in step with its cluster (the cluster barriers) but issues no
+  // copy and stores nothing more, nor under the test hook
+  const CtaAbort cta_abort{reinterpret_cast<int*>(smem + p.off_bar + 8 * (kFusedMaxKb + 1)),
+                           p.wait_limit_ns};
+  auto stopped = [&]() { return cta_abort.raised() || p.wait_fault != 0; };
   if (tid == 0) {
-    for (int i = 0; i < kFusedMaxKb + 1; ++i) mbar_init(bar_a + 8 * i, 1);
+    *cta_abort.flag = 0;
+    for (int i = 0; i < kFusedMaxKb + 1; ++i)
+      mbar_init(bar_a + 8 * i, 1 + (p.wait_fault && i == 0 ? 1 : 0));
     fence_mbar_init();
     for (int s = 0; s < p.num_slices; ++s) {
       prefetch_tmap(&p.amap[s]);
@@ -117,8 +129,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   };
 
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
-  bool waited = false, timed_out = false;
+  bool waited = false;
   uint32_t phase = 0;
+  int issued_phase = -1;  // thread 0: the barrier phase of its last TMA loads
 
   for (int item = cluster_id; item < ntiles; item += nclusters) {
     load_record<kFBM>(p.records, item, rec);
@@ -131,7 +144,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       // before the wait only L2 prefetches (L2 is the coherence point, so the
       // copies after the wait read the final values) of this CTA's weight
       // blocks and x / y rows
-      if (tid == 0) {
+      if (tid == 0 && !p.wait_fault) {  // (the test hook issues nothing)
         for (int i = 0; i < nkb; ++i)
           for (int s = 0; s < p.num_slices; ++s)
             tma_prefetch_2d(&p.amap[s], (kb0 + i) * 64, lora * R);
@@ -141,7 +154,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           tma_prefetch_2d(&p.bmap[s], (unit - p.unit_start[s]) * 64, lora * R);
         }
       }
-      for (int r = tid; r < cnt; r += kFusedThreads) {
+      for (int r = tid; r < cnt && !p.wait_fault; r += kFusedThreads) {
         const int t = record_token(rec, r, cnt, p.max_num_tokens);
         if (t < 0) continue;
         if (nkb > 0)
@@ -161,7 +174,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       waited = true;
     }
     // weights (A blocks of this CTA's k-range, B blocks of its units) by TMA
-    if (tid == 0) {
+    // (none once the CTA has given up: every wait of earlier items is over,
+    // so one value for all)
+    const bool copy = !stopped();
+    if (tid == 0 && copy) {
+      issued_phase = static_cast<int>(phase);
       for (int i = 0; i < nkb; ++i) {
         mbar_arrive_expect_tx(bar_a + 8 * i, static_cast<uint32_t>(SR * 128));
         for (int s = 0; s < p.num_slices; ++s)
@@ -179,7 +196,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     // activations: x rows of the k-range (group 1), y segments of the units (group 2)
-    for (int c = tid; c < nkb * kFBM * 8; c += kFusedThreads) {
+    for (int c = tid; copy && c < nkb * kFBM * 8; c += kFusedThreads) {
       const int i = c >> 7, row = (c >> 3) & 15, ch = c & 7;
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
       const int kcol = (kb0 + i) * 64 + ch * 8;
@@ -188,7 +205,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
                   ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
     }
     cp_async_commit();
-    for (int c = tid; c < nun * kFBM * 8; c += kFusedThreads) {
+    for (int c = tid; copy && c < nun * kFBM * 8; c += kFusedThreads) {
       const int j = c >> 7, row = (c >> 3) & 15, ch = c & 7;
       const int unit = un0 + j;
       const int s = unit_slice(unit);
@@ -210,7 +227,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     cp_async_wait<1>();
     __syncthreads();  // x rows are in
     for (int i = 0; i < nkb; ++i) {
-      if (!mbar_wait(bar_a + 8 * i, phase)) timed_out = true;
+      cta_abort.wait(bar_a + 8 * i, phase);  // (after giving up: garbage in, nothing out)
       const uint32_t sx = sbase + p.off_x + i * 2048;
       const uint32_t sw = sbase + p.off_a + i * SR * 128;
 #pragma unroll
@@ -266,6 +283,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     cluster_sync_all();
+    const bool store_u = !stopped();  // (the A waits are over: one value for all)
 
     // ---- every CTA sums the C partial tiles in rank order -> full u tile
     for (int idx = tid; idx < e4; idx += kFusedThreads) {
@@ -291,7 +309,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       const int row = e / SR;
       const int col = e - row * SR;
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
-      if (t >= 0 && (idx % C) == crank) {
+      if (t >= 0 && (idx % C) == crank && store_u) {
         const int s = col >> p.rank_shift;
         const int r = col - (s << p.rank_shift);
         *reinterpret_cast<float4*>(p.u + (static_cast<long long>(s) * p.max_num_tokens + t) * R + r) =
@@ -300,7 +318,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     }
     cp_async_wait<0>();
     __syncthreads();  // u tile complete, y segments are in
-    if (nun > 0 && !mbar_wait(bar_b, phase)) timed_out = true;
+    if (nun > 0) cta_abort.wait(bar_b, phase);
 
     // ---- expand over this CTA's units (warps take units round-robin)
     for (int j = warp; j < nun; j += 4) {
@@ -363,8 +381,10 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       }
     }
     __syncthreads();
-    // 16-byte stores of the valid rows and columns
-    for (int c = tid; c < nun * kFBM * 8; c += kFusedThreads) {
+    // 16-byte stores of the valid rows and columns (none once the CTA has
+    // given up; every wait of this item is over, so one value for all)
+    const bool store_y = !stopped();
+    for (int c = tid; store_y && c < nun * kFBM * 8; c += kFusedThreads) {
       const int j = c >> 7, row = (c >> 3) & 15, ch = c & 7;
       const int unit = un0 + j;
       const int s = unit_slice(unit);
@@ -384,7 +404,16 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     pdl_wait();
     pdl_launch_dependents();
   }
-  if (timed_out) atomicOr(p.status, kStatusTimeout);
+  // after giving up, thread 0's last TMA loads land before the CTA leaves
+  // (waiting on one that landed returns at once; each item's cp.async groups
+  // were waited for inside the item)
+  if (tid == 0 && cta_abort.raised()) {
+    if (issued_phase >= 0) {
+      for (int i = 0; i < nkb; ++i) mbar_drain(bar_a + 8 * i, issued_phase, p.wait_limit_ns);
+      if (nun > 0) mbar_drain(bar_b, issued_phase, p.wait_limit_ns);
+    }
+    atomicOr(p.status, kStatusTimeout);
+  }
 }
 
 struct FusedPlan {
@@ -429,7 +458,7 @@ static FusedPlan fused_plan(int max_num_tokens, int num_loras, int hidden, const
   f.off_red = off; off += f.wk * kFBM * SR * 4;
   f.off_rec = off; off += record_ints(kFBM) * 4;
   off = (off + 15) / 16 * 16;
-  f.off_bar = off; off += 8 * (kFusedMaxKb + 1);
+  f.off_bar = off; off += 8 * (kFusedMaxKb + 1) + 16;  // the barriers, then the abort flag
   f.smem = 1024 + static_cast<size_t>(off);
   f.ok = f.smem <= 200 * 1024;
   return f;
@@ -564,6 +593,8 @@ int launch_fused(const ShrinkArgs& sa, const ExpandArgs& ea, cudaStream_t stream
   p.off_red = f.off_red;
   p.off_rec = f.off_rec;
   p.off_bar = f.off_bar;
+  p.wait_fault = wait_fault() ? 1 : 0;
+  p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
 
   const void* fn = fused_fn(f.ntw, sa.f16);
   if (ensure_smem_attr(fn, smem) != 0) return -6;

@@ -3,6 +3,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 #include <utility>
@@ -10,6 +11,7 @@
 namespace grg {
 
 namespace {
+std::atomic<int> g_wait_fault{0};
 std::mutex g_mu;
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices] = {0};
@@ -37,6 +39,9 @@ int current_device() {
   return dev;
 }
 }  // namespace
+
+int set_wait_fault(int on) { return g_wait_fault.exchange(on ? 1 : 0); }
+int wait_fault() { return g_wait_fault.load(); }
 
 int device_sm_count() {
   const int dev = current_device();

@@ -12,6 +12,12 @@ namespace grg {
 // Raises a kernel's dynamic shared-memory limit once per (device, kernel).
 int ensure_smem_attr(const void* func, size_t smem_bytes);
 
+// Test hook: while on, every shrink / expand / fused kernel launched arms the
+// first barrier it waits on with one arrival too many, issues no copy and
+// gives up its waits after 1 ms.  set_wait_fault returns the previous setting.
+int set_wait_fault(int on);
+int wait_fault();
+
 // Streaming multiprocessors of the current device (cached).
 int device_sm_count();
 

@@ -14,7 +14,7 @@
 //  - a producer warp fills a stage with the adapter's R x 64 block of every
 //    slice (one TMA tile load each: tensor map, 128-byte swizzle) and the BM
 //    gathered x rows (16-byte cp.async, zero-filled past the tile's tokens and
-//    past H, under an L2 evict-first policy: x is read once); TMA bytes and
+//    past H; a run tile's rows as one TMA box); TMA bytes and
 //    the lanes' cp.async arrivals complete the stage's "full" mbarrier;
 //  - four consumer warps wait on "full", run the tensor-core MMAs (mma.sync
 //    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
@@ -67,6 +67,10 @@ struct ShrinkParams {
   const uint64_t* a_tab[3];
   int paged;
   int f16;  // fp16 x and A (else bf16)
+  // the bounded waits' limit; under the test hook (wait_fault) no copy is
+  // issued and the first stage's barrier is armed with one arrival too many
+  unsigned long long wait_limit_ns;
+  int wait_fault;
 };
 
 template <int BM, int NTW, int NST, bool PAGED, bool F16>
@@ -90,10 +94,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
 
-  // the gathered x rows are read once (by this kernel's CTAs only): their L2
-  // lines go first, which leaves the L2 to the adapter blocks every tile of
-  // a LoRA re-reads and to the lines the expand works on (prefill layer
-  // 52 -> 48 us)
+  // x is read once: a run tile's TMA box of x loads under an L2 evict-first
+  // policy, leaving the L2 to the adapter blocks every tile of a LoRA re-reads
   const uint64_t x_pol = l2_evict_first_policy();
 
   uint32_t cl_size;
@@ -115,9 +117,13 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
                           : (crank < p.kblocks ? (p.kblocks - crank + C - 1) / C : 0);
   auto kb_of = [&](int i) { return kb0 + i * kstep; };
 
+  // giving up (CtaAbort): the flag after the barriers
+  const CtaAbort cta_abort{reinterpret_cast<int*>(smem + p.bar_offset + 2 * 8 * 8), p.wait_limit_ns};
   if (tid == 0) {
+    *cta_abort.flag = 0;
     for (int s = 0; s < NST; ++s) {
-      mbar_init(full_bar + 8 * s, 1 + kShrinkThreads);  // expect_tx + one per thread
+      // expect_tx + one per thread (+ one that never comes: the test hook)
+      mbar_init(full_bar + 8 * s, 1 + kShrinkThreads + (p.wait_fault && s == 0 ? 1 : 0));
       mbar_init(empty_bar + 8 * s, kConsumerWarps);  // one arrival per consumer warp
     }
     fence_mbar_init();
@@ -128,8 +134,11 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
 
   // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
-  bool waited = false, timed_out = false;
+  bool waited = false;
   int kb_global = 0;  // k-blocks processed by this CTA so far (stage phases)
+  int issued_g = -1;  // producer lane 0: the last k-block whose TMA part went out
+  // no copy and no store once the CTA has given up, nor under the test hook
+  auto stopped = [&]() { return cta_abort.raised() || p.wait_fault != 0; };
 
   for (int item = cluster_id; item < ntiles; item += nclusters) {
     load_record<BM>(p.records, item, rec);
@@ -153,13 +162,15 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
       const int kcol = kb * kBK + ch * 8;
       const bool ok = t >= 0 && kcol < p.hidden;
-      cp_async_16_hint(sbase + st * p.stage_bytes + swz128(row, ch),
-                       ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok, x_pol);
+      cp_async_16(sbase + st * p.stage_bytes + swz128(row, ch),
+                  ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
     };
     // the TMA part of k-block kb -> stage st (one thread): the adapter blocks
     // (stacked weights) and the x box (a run tile); with neither, a plain
     // arrival stands in for the transaction count
     auto issue_a = [&](int st, int kb) {
+      if (stopped()) return;
+      issued_g = kb_global + (kb - kb0) / kstep;
       const uint32_t bar = full_bar + 8 * st;
       const uint32_t bytes = (PAGED ? 0u : static_cast<uint32_t>(SR * 128)) +
                              (xbox ? static_cast<uint32_t>(BM * 128) : 0u);
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     };
     auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
       const int st = g % NST, use = g / NST;
-      if (use > 0 && !mbar_wait(empty_bar + 8 * st, (use - 1) & 1)) timed_out = true;
+      if (use > 0) cta_abort.wait(empty_bar + 8 * st, (use - 1) & 1);
     };
 
     if (!waited) {
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       // the first stages' adapter blocks and of this CTA's first x columns
       // (cluster mode: the span of the first npro rounds, its rows shared out
       // between the cluster's CTAs); the copies after the wait then hit L2.
-      if (producer && npro > 0) {
+      if (producer && npro > 0 && !p.wait_fault) {  // (the test hook issues nothing)
         if constexpr (!PAGED) {
           if (lane == 0)
             for (int i = 0; i < npro; ++i)
@@ -248,13 +259,15 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         issue_a((kb_global + i) % NST, kb_of(i));
       }
     }
+    const bool copy = !stopped();  // no copy once the CTA has given up
     if constexpr (PAGED) {
       // every stage is free here (the previous tile ended with a block-wide
       // barrier); each thread's adapter chunks complete with its x chunks
-      for (int i = 0; i < npro; ++i)
-        a_chunks((kb_global + i) % NST, kb_of(i), tid, kShrinkThreads);
+      if (copy)
+        for (int i = 0; i < npro; ++i)
+          a_chunks((kb_global + i) % NST, kb_of(i), tid, kShrinkThreads);
     }
-    for (int i = 0; i < npro; ++i) {
+    for (int i = 0; i < npro && copy; ++i) {
       const int st = (kb_global + i) % NST;
       if (!xbox)
         for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb_of(i), c);
@@ -278,23 +291,24 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         const int st = g % NST;
         wait_empty(g);  // every lane: the consumers released the stage
         __syncwarp();
-        if (lane == 0) {
+        const bool go = !stopped();  // no further copy once the CTA has given up
+        if (lane == 0 && go) {
           issue_a(st, kb_of(i));
           mbar_arrive_count(full_bar + 8 * st, kShrinkThreads - 32);
         }
-        if constexpr (PAGED) a_chunks(st, kb_of(i), lane, 32);
-        if (!xbox) {
+        if constexpr (PAGED)
+          if (go) a_chunks(st, kb_of(i), lane, 32);
+        if (!xbox && go) {
           const uint32_t sx = sbase + st * p.stage_bytes;
           const int kb = kb_of(i);
           const bool kin = kb * kBK + xch * 8 < p.hidden;
 #pragma unroll
           for (int j = 0; j < XJ; ++j) {
             const bool ok = xrow[j] != nullptr && kin;
-            cp_async_16_hint(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x,
-                             ok, x_pol);
+            cp_async_16(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
           }
         }
-        cp_async_mbar_arrive(full_bar + 8 * st);
+        if (go) cp_async_mbar_arrive(full_bar + 8 * st);
       }
     } else {
       float acc[BM / 16][NTW][4];
@@ -308,7 +322,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       for (int i = 0; i < nkb; ++i) {
         const int g = kb_global + i;
         const int st = g % NST;
-        if (!mbar_wait(full_bar + 8 * st, (g / NST) & 1)) timed_out = true;
+        cta_abort.wait(full_bar + 8 * st, (g / NST) & 1);  // (after giving up: garbage in, nothing out)
         const uint32_t sx = sbase + st * p.stage_bytes;
         const uint32_t sw = sx + BM * 128;
 #pragma unroll
@@ -365,6 +379,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     }
     kb_global += nkb;
     __syncthreads();  // all partials are in red[] (the producer has issued everything)
+    const bool store = !stopped();  // (every wait of this item is over: one value for all)
 
     // sum the k-split warps into red[0]
     float* red = reinterpret_cast<float*>(smem);
@@ -374,7 +389,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       // order) goes to the workspace; the expand sums the split in rank order
       float4* dst = reinterpret_cast<float4*>(p.partials) +
                     (static_cast<long long>(item) * C + crank) * e4;
-      for (int idx = tid; idx < e4; idx += kShrinkThreads) {
+      for (int idx = tid; idx < e4 && store; idx += kShrinkThreads) {
         float4 v = reinterpret_cast<float4*>(red)[idx];
         for (int w = 1; w < WK; ++w) {
           const float4 o = reinterpret_cast<float4*>(red + w * BM * SR)[idx];
@@ -405,7 +420,7 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     cluster_sync_all();
 
     // cluster reduction in rank order, scale, store the valid rows
-    for (int idx = crank * kShrinkThreads + tid; idx < e4; idx += C * kShrinkThreads) {
+    for (int idx = crank * kShrinkThreads + tid; idx < e4 && store; idx += C * kShrinkThreads) {
       const int e = idx << 2;
       const int row = e / SR;
       const int col = e - row * SR;
@@ -441,7 +456,18 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     pdl_wait();
     pdl_launch_dependents();
   }
-  if (timed_out) atomicOr(p.status, kStatusTimeout);
+  // Leave with no copy in flight: each thread's cp.async, and after giving
+  // up the producer's last TMA loads (a stage is refilled only once its
+  // previous load was consumed, so only the last NST can be pending; waiting
+  // on one that landed returns at once).  The flag is final here: the last
+  // wait of the last item came before that item's block-wide barrier.
+  cp_async_wait<0>();
+  if (cta_abort.raised()) {
+    if (producer && lane == 0)
+      for (int g = max(0, issued_g - NST + 1); g <= issued_g; ++g)
+        mbar_drain(full_bar + 8 * (g % NST), (g / NST) & 1, p.wait_limit_ns);
+    if (tid == 0) atomicOr(p.status, kStatusTimeout);
+  }
 }
 
 template <int BM, int NTW, int NST>
@@ -522,6 +548,8 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   memset(&p, 0, sizeof(p));
   p.paged = a.a_tables[0] != nullptr;
   p.f16 = a.f16 ? 1 : 0;
+  p.wait_fault = wait_fault() ? 1 : 0;
+  p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   for (int s = 0; s < 3; ++s) {
     p.a_tab[s] = s < a.num_slices ? a.a_tables[s] : a.a_tables[0];
     if (p.paged) continue;
@@ -565,7 +593,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int body = ((ring > red ? ring : red) + 127) / 128 * 128;
   p.rec_offset = body;
   p.bar_offset = body + record_ints(BM) * 4;
-  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8;
+  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8 + 16;  // + the flag
 
   // Every (tile height, column tiles per warp, ring depth) the rules above can
   // produce has its own instantiation; the shared-memory plan was sized for

@@ -83,7 +83,8 @@ extern "C" {
 
 #define LORA_STATUS_BAD_LORA_ID 0x1u     /* some m[t], t < n, was outside [-1, L) */
 #define LORA_STATUS_BAD_NUM_TOKENS 0x2u  /* n was outside [0, max_num_tokens]; clamped */
-#define LORA_STATUS_TIMEOUT 0x4u         /* a kernel's bounded wait for its own copies gave up */
+#define LORA_STATUS_TIMEOUT 0x4u         /* a kernel's bounded wait for its own copies gave up;
+                                            the outputs of that call are unspecified */
 #define LORA_STATUS_BAD_WEIGHT 0x8u      /* a paged weight address was not 16-byte aligned */
 
 #define LORA_MAX_SLICES 3

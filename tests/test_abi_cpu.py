@@ -2,6 +2,7 @@
 function the header declares; host-side validation rejects bad arguments
 before any CUDA call (so these run without a GPU)."""
 import ctypes
+import glob
 import os
 import re
 
@@ -11,7 +12,7 @@ from gathered_rank_gemm_gb300 import binding
 from gathered_rank_gemm_gb300 import build as B
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "gathered_rank_gemm.h")
+HEADERS = sorted(glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 @pytest.fixture(scope="module")
@@ -21,7 +22,7 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(lora_[a-z0-9_]+)\s*\(", text)))
 
@@ -214,3 +215,10 @@ def test_binding_selects_the_input_type_and_rejects_mixtures():
         binding._is_f16([torch.zeros(2)])
     with pytest.raises(ValueError):   # entry points without an fp16 variant
         binding._is_f16([hf], fp16_ok=False)
+
+
+def test_timeout_hook_is_off_by_default_and_reports_its_setting(lib):
+    """The test hook of gathered_rank_gemm_testing.h only flips a host flag."""
+    assert binding.lora_testing_inject_timeout(False) is False
+    assert binding.lora_testing_inject_timeout(True) is False
+    assert binding.lora_testing_inject_timeout(False) is True
