@@ -15,7 +15,10 @@ in ``per_workload``.  For each workload:
 value   = n * layers / t_layers  (tokens/s per LoRA layer, whole job): t_layers
           is the device time of the shrink + expand calls of a step, read with
           CUDA events around them; the grouping's time is reported on its own
-          (``us.metadata_in_step``) and ``value_with_metadata`` counts it in
+          (``us.metadata_in_step``: inside the step, with the replay of its own
+          graph; ``us.metadata_alone``: per kernel, from a graph of 16 grouping
+          launches, the way the shrink and expand are timed alone) and
+          ``value_with_metadata`` counts it in
 ms_per_step = grouping + layers, device time of one step
 e2e     = the same metric through the C ABI with each step's inputs (mapping,
           n, every layer's x and y) copied from pinned host memory and every
@@ -58,12 +61,15 @@ UNIT = "tokens/s"
 HEADLINE = "down_proj_graph"
 ORDER = ("tiny", "decode_qkv", "chunked_prefill", "mlp_gate_up", "down_proj_graph")
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = {"expand": "gathered_rank_gemm_gb300/csrc/expand.cu",
-                  "shrink": "gathered_rank_gemm_gb300/csrc/shrink.cu",
-                  "expand-split": "gathered_rank_gemm_gb300/csrc/expand.cu",
-                  "shrink-split": "gathered_rank_gemm_gb300/csrc/shrink.cu",
-                  "shrink_expand": "gathered_rank_gemm_gb300/csrc/fused.cu",
-                  "metadata": "gathered_rank_gemm_gb300/csrc/metadata.cu"}
+# the sources of each timed kernel (the expand of rank 128 on large batches is
+# the tcgen05 kernel)
+KERNEL_SOURCES = {"expand": ("gathered_rank_gemm_gb300/csrc/expand.cu",
+                             "gathered_rank_gemm_gb300/csrc/expand_tc.cu"),
+                  "shrink": ("gathered_rank_gemm_gb300/csrc/shrink.cu",),
+                  "expand-split": ("gathered_rank_gemm_gb300/csrc/expand.cu",),
+                  "shrink-split": ("gathered_rank_gemm_gb300/csrc/shrink.cu",),
+                  "shrink_expand": ("gathered_rank_gemm_gb300/csrc/fused.cu",),
+                  "metadata": ("gathered_rank_gemm_gb300/csrc/metadata.cu",)}
 
 
 # ---------------------------------------------------------------- accounting
@@ -137,7 +143,7 @@ def load_peaks():
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in (KERNEL_SOURCES[kernel], "gathered_rank_gemm_gb300/csrc/common.cuh"):
+    for rel in KERNEL_SOURCES[kernel] + ("gathered_rank_gemm_gb300/csrc/common.cuh",):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -426,6 +432,10 @@ class WorkloadRun:
         if which == "metadata":
             m.prepare(self.mapping, self.n_dev, s)
             return
+        if which == "metadata_x16":
+            for _ in range(16):
+                m.prepare(self.mapping, self.n_dev, s)
+            return
         for k in range(self.layers):
             if which == "layers":
                 if self.args.paged:
@@ -463,7 +473,7 @@ class WorkloadRun:
             # the split paths leave partial tiles behind the metadata part of
             # the (zero-initialised) workspace: check that this one ran
             assert bool(self.meta.workspace[base:].any().item()), "split-K path did not run"
-        for which in ("metadata", "layers", "shrink", "expand"):
+        for which in ("metadata", "metadata_x16", "layers", "shrink", "expand"):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=self.stream):
                 self.launch(which)
@@ -536,7 +546,7 @@ class WorkloadRun:
         self.ms_one = self.time_graph("layers") / self.layers
         self.ms_shrink = self.time_graph("shrink") / self.layers
         self.ms_expand = self.time_graph("expand") / self.layers
-        self.ms_meta_alone = self.time_graph("metadata")
+        self.ms_meta_alone = self.time_graph("metadata_x16") / 16
 
     def e2e(self, steps, world):
         """Steps through the public API with host buffers: the step's inputs

@@ -309,6 +309,153 @@ __global__ void __launch_bounds__(kMetaThreads, 1) lora_metadata_kernel(MetaPara
   pdl_launch_dependents();
 }
 
+// Short batches (max_num_tokens <= 1024, at most 128 adapters): one CTA,
+// one token per thread, and fewer dependent steps than the cluster kernel.
+// n and every thread's mapping entry load in one round trip (the entries
+// past n are loaded but never used); per-warp bin counts
+// (__match_any_sync); per bin, one warp scans the warps' counts into the
+// warps' offsets and the bin total; one warp scans the bins for the bin starts
+// and, per tile height, each adapter's first tile; then every thread writes
+// its token's slots.  Same outputs, bit for bit, as the cluster kernel.
+constexpr int kSmallMaxTokens = 1024;
+constexpr int kSmallMaxLoras = 128;
+constexpr int kSmallBins = kSmallMaxLoras + 1;
+
+__global__ void __launch_bounds__(kSmallMaxTokens, 1) lora_metadata_small_kernel(MetaParams p) {
+  __shared__ int32_t cnt[32][kSmallBins];  // per warp and bin: count, then offset in the bin
+  __shared__ int32_t total[kSmallBins];
+  __shared__ int32_t start[kSmallBins + 1];
+  __shared__ int32_t toff[kNumTileSizes][kSmallBins + 1];  // first tile of each adapter
+
+  const int L = p.num_loras, nbins = L + 1;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwarps = static_cast<int>(blockDim.x) >> 5;
+  pdl_wait();
+
+  const int t = tid;
+  int n = *p.num_tokens;
+  const int id = t < p.max_num_tokens ? p.mapping[t] : -1;
+  for (int i = tid; i < 32 * kSmallBins; i += blockDim.x) (&cnt[0][0])[i] = 0;
+  uint32_t st = 0;
+  if (n < 0) {
+    n = 0;
+    st = 2u;
+  }
+  if (n > p.max_num_tokens) {
+    n = p.max_num_tokens;
+    st = 2u;
+  }
+  // bin of this thread's token (nbins: no token)
+  int bin = nbins;
+  bool bad = false;
+  if (t < n) {
+    if (id >= 0 && id < L) {
+      bin = id;
+    } else {
+      bin = L;
+      bad = id != -1;
+    }
+  }
+  if (__syncthreads_or(bad)) st |= 1u;  // (and the counts are zeroed)
+  const unsigned peers = __match_any_sync(0xffffffffu, bin);
+  if (bin < nbins && lane == __ffs(peers) - 1) cnt[warp][bin] = __popc(peers);
+  __syncthreads();
+
+  // per bin: the warps' offsets inside the bin (warp scan over the warps) and the total
+  for (int b = warp; b < nbins; b += nwarps) {
+    const int c = lane < nwarps ? cnt[lane][b] : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane < nwarps) cnt[lane][b] = incl - c;
+    if (lane == 31) total[b] = incl;
+  }
+  __syncthreads();
+
+  // one warp: bin starts and, per tile height, each adapter's first tile
+  if (warp == 0) {
+    int run[1 + kNumTileSizes] = {0, 0, 0, 0, 0};
+    for (int b0 = 0; b0 < nbins; b0 += 32) {
+      const int b = b0 + lane;
+      int v[1 + kNumTileSizes];
+      const int tot = b < nbins ? total[b] : 0;
+      v[0] = tot;
+#pragma unroll
+      for (int k = 0; k < kNumTileSizes; ++k)
+        v[1 + k] = b < L ? (tot + tile_rows_of(k) - 1) / tile_rows_of(k) : 0;
+#pragma unroll
+      for (int a = 0; a < 1 + kNumTileSizes; ++a) {
+        int incl = v[a];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int excl = run[a] + incl - v[a];
+        if (b <= nbins) {
+          if (a == 0) start[b] = excl;
+          else toff[a - 1][b] = excl;
+        }
+        run[a] += __shfl_sync(0xffffffffu, incl, 31);
+      }
+    }
+    // the entries past the last bin (b == nbins when nbins is a multiple of 32)
+    if (lane == 0 && nbins % 32 == 0) {
+      start[nbins] = run[0];
+#pragma unroll
+      for (int k = 0; k < kNumTileSizes; ++k) toff[k][nbins] = run[1 + k];
+    }
+  }
+  __syncthreads();
+
+  // this thread's token: sorted_token_ids and its entry in every tile list
+  if (bin < nbins) {
+    const int rel = cnt[warp][bin] + __popc(peers & ((1u << lane) - 1u));
+    p.sorted_ids[start[bin] + rel] = t;
+    if (bin < L) {
+#pragma unroll
+      for (int k = 0; k < kNumTileSizes; ++k) {
+        const int tile = toff[k][bin] + (rel >> (4 + k));
+        p.ws.lists[k][static_cast<long long>(tile) * record_ints(tile_rows_of(k)) +
+                      kRecordHeaderInts + (rel & (tile_rows_of(k) - 1))] = t;
+      }
+    }
+  } else if (t >= n && t < p.max_num_tokens) {
+    p.sorted_ids[t] = -1;
+  }
+  for (int b = tid; b < nbins; b += blockDim.x) p.counts[b] = total[b];
+  for (int b = tid; b <= nbins; b += blockDim.x) p.starts[b] = start[b];
+  // record headers (largest adapter l with toff[l] <= i: adapters without a
+  // tile share the next offset)
+#pragma unroll
+  for (int k = 0; k < kNumTileSizes; ++k) {
+    const int rows = tile_rows_of(k);
+    const int count = toff[k][L];
+    int32_t* list = p.ws.lists[k];
+    for (int i = tid; i < count; i += blockDim.x) {
+      int a = 0, b = L - 1;
+      while (a < b) {
+        const int mid = (a + b + 1) >> 1;
+        if (toff[k][mid] <= i) a = mid; else b = mid - 1;
+      }
+      const int j = i - toff[k][a];
+      *reinterpret_cast<int4*>(list + static_cast<long long>(i) * record_ints(rows)) =
+          make_int4(a, min(rows, total[a] - j * rows), start[a] + j * rows, 0);
+    }
+    if (tid == 0) p.ws.num_tiles[k] = count;
+  }
+  if (tid == 0) {
+    *p.ws.n = n;
+    if (st) atomicOr(p.ws.status, st);
+  }
+  __threadfence();
+  __syncthreads();
+  pdl_launch_dependents();
+}
+
 static size_t meta_smem_bytes(int num_loras) {
   const size_t nb = static_cast<size_t>(num_loras) + 1;
   return sizeof(int32_t) * (kMetaWarps * nb + nb + (nb + 1) + kScanArrays * nb +
@@ -327,6 +474,11 @@ int launch_metadata(const int32_t* mapping, const int32_t* num_tokens, int max_n
   p.counts = counts;
   p.starts = starts;
   p.ws = ws_view(workspace, max_num_tokens, num_loras);
+  if (max_num_tokens <= kSmallMaxTokens && num_loras <= kSmallMaxLoras) {
+    const int threads = (max_num_tokens + 31) / 32 * 32;
+    return launch_pdl(reinterpret_cast<const void*>(lora_metadata_small_kernel), dim3(1),
+                      dim3(static_cast<unsigned>(threads)), 0, stream, 0, &p);
+  }
   const size_t smem = meta_smem_bytes(num_loras);
   if (ensure_smem_attr(reinterpret_cast<const void*>(lora_metadata_kernel), smem) != 0)
     return -6;
