@@ -107,11 +107,15 @@ size_t lora_workspace_size(int64_t max_num_tokens, int64_t max_loras);
  * kernels for V1", "Why do we need a new set of kernels": V1 keeps the batch
  * unsorted, so the grouping is computed on the device from the token -> LoRA
  * map; "[Kernel] LoRA - Enable CUDAGraphs for V1": the map is a static
- * max_num_tokens buffer).  One thread-block cluster (one CTA per 1024 tokens
- * of max_num_tokens, up to 8) runs a histogram / prefix-sum / stable scatter;
- * the grid depends only on max_num_tokens, not on the data.
+ * max_num_tokens buffer).  A histogram / prefix-sum / stable scatter, run by
+ * one CTA when max_num_tokens <= 1024 and max_loras <= 128 (one token per
+ * thread), else by one thread-block cluster (one CTA per 1024 tokens of
+ * max_num_tokens, up to 8); the grid depends only on max_num_tokens and
+ * max_loras, not on the data.
  *
- *   token_lora_mapping   int32[max_num_tokens]; entries t >= n are never read
+ *   token_lora_mapping   int32[max_num_tokens]; entries t >= n may be loaded
+ *                        (the one-CTA kernel loads every entry at once with
+ *                        n) but never affect any output
  *   num_tokens           device int32: n
  *   sorted_token_ids     int32[max_num_tokens] out: tokens of LoRA 0 in
  *                        ascending order, then LoRA 1, ..., then the tokens
