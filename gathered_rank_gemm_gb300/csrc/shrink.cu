@@ -541,8 +541,15 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
     nst = 4;
   else if (kb_per <= 8)
     nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
+  else if (SR == 128)
+    // three stages keep three CTAs per SM: on down_proj_graph (11008 wide)
+    // every tile's cluster is resident at once (shrink 96.4 -> 88.5 us, two
+    // stages had too few bytes in flight, four left too few clusters for the
+    // tiles); on mlp_gate_up the smaller CTAs let the expand's start beside
+    // them (one call 103.6 -> 91.8 us)
+    nst = 3;
   else
-    nst = ((SR >= 128 && kb_per > 32) || 4 * stage > 96 * 1024) ? 2 : 4;
+    nst = 4 * stage > 96 * 1024 ? 2 : 4;
 
   ShrinkParams p;
   memset(&p, 0, sizeof(p));
@@ -606,6 +613,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   if (BM == 16 && ntw_t == 8 && nst == 8) run = run_shrink<16, 8, 8>;
   if (BM == 16 && ntw_t == 8 && nst == 4) run = run_shrink<16, 8, 4>;
   if (BM == 16 && ntw_t == 8 && nst == 2) run = run_shrink<16, 8, 2>;
+  if (BM == 16 && ntw_t == 8 && nst == 3) run = run_shrink<16, 8, 3>;
   if (BM == 16 && ntw_t == 12 && nst == 4) run = run_shrink<16, 12, 4>;
   if (BM == 16 && ntw_t == 12 && nst == 2) run = run_shrink<16, 12, 2>;
   if (BM == 32 && ntw_t == 4 && nst == 8) run = run_shrink<32, 4, 8>;
@@ -613,6 +621,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   if (BM == 32 && ntw_t == 8 && nst == 8) run = run_shrink<32, 8, 8>;
   if (BM == 32 && ntw_t == 8 && nst == 4) run = run_shrink<32, 8, 4>;
   if (BM == 32 && ntw_t == 8 && nst == 2) run = run_shrink<32, 8, 2>;
+  if (BM == 32 && ntw_t == 8 && nst == 3) run = run_shrink<32, 8, 3>;
   if (run == nullptr) return -6;
   return run(p, cluster, smem, stream, max_tiles);
 }
