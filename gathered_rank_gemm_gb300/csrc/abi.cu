@@ -413,6 +413,7 @@ int shrink_expand(grg::ShrinkArgs& sa, grg::ExpandArgs& ea, int64_t hidden,
   if (rc == 1) return LORA_OK;
   // the expand directly follows the shrink, which never writes y
   ea.y_early = true;
+  sa.expand_follows = true;
   // split-K: with the larger workspace, the shrink's CTAs write partial tiles
   // and the expand sums them in rank order (no cluster-wide steps)
   const int64_t T = sa.max_num_tokens, L = sa.num_loras;

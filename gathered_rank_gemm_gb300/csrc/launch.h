@@ -70,6 +70,9 @@ struct ShrinkArgs {
   // ([rank][hidden] bf16); all null for stacked weights (lora_a)
   const uint64_t* a_tables[3] = {nullptr, nullptr, nullptr};
   bool f16 = false;  // fp16 x and A (else bf16)
+  // the expand of the same call follows at once (the one-call paths): keep
+  // the shrink's CTAs small, so that the expand's start beside them
+  bool expand_follows = false;
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);
 // CTAs sharing one tile's hidden dimension for this shape on the current

@@ -73,7 +73,7 @@ struct ShrinkParams {
   int wait_fault;
 };
 
-template <int BM, int NTW, int NST, bool PAGED, bool F16>
+template <int BM, int NTW, int NST, int KS, bool PAGED, bool F16>
 __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW > 8) ? 3 : 4)
     lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -106,16 +106,26 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
                             : static_cast<int>(cluster_ctarank());
   const int cluster_id = blockIdx.x / C;
   const int nclusters = gridDim.x / C;
-  // Cluster mode: the CTAs of a tile take its k-blocks round-robin (k-block
-  // i of this CTA is crank + i * C), so at any moment they read neighbouring
-  // 128-byte pieces of the same rows (prefill shrink 4 % faster).  Split-K
-  // mode: contiguous k-ranges (decode 1 % faster).
-  const int kbp = (p.kblocks + C - 1) / C;
+  // A stage holds a k-group: KS consecutive k-blocks (the last group may be
+  // shorter), filled under one expect_tx and released once, so the per-stage
+  // costs (barrier round trip, issue) are paid once per KS k-blocks.
+  // Cluster mode: the CTAs of a tile take its k-groups round-robin (group i
+  // of this CTA is crank + i * C), so at any moment they read neighbouring
+  // pieces of the same rows (prefill shrink 4 % faster than contiguous
+  // halves).  Split-K mode: contiguous ranges of k-groups (decode 1 % faster).
+  const int ngroups = (p.kblocks + KS - 1) / KS;
+  const int kbp = (ngroups + C - 1) / C;
   const int kb0 = split_k ? crank * kbp : crank;
   const int kstep = split_k ? 1 : C;
-  const int nkb = split_k ? max(min(kb0 + kbp, p.kblocks) - kb0, 0)
-                          : (crank < p.kblocks ? (p.kblocks - crank + C - 1) / C : 0);
-  auto kb_of = [&](int i) { return kb0 + i * kstep; };
+  const int nkb = split_k ? max(min(kb0 + kbp, ngroups) - kb0, 0)
+                          : (crank < ngroups ? (ngroups - crank + C - 1) / C : 0);
+  auto kb_of = [&](int i) { return kb0 + i * kstep; };            // the CTA's i-th k-group
+  auto nsub_of = [&](int grp) {  // its k-blocks (a stage of one k-block is always full)
+    return KS == 1 ? 1 : min(KS, p.kblocks - grp * KS);
+  };
+  // stage layout: KS x boxes of [BM][128 B], then KS adapter blocks of [S*R][128 B]
+  constexpr int kXSub = BM * 128;
+  const int a_off = KS * kXSub, a_sub = SR * 128;
 
   // giving up (CtaAbort): the flag after the barriers
   const CtaAbort cta_abort{reinterpret_cast<int*>(smem + p.bar_offset + 2 * 8 * 8), p.wait_limit_ns};
@@ -135,8 +145,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
   bool waited = false;
-  int kb_global = 0;  // k-blocks processed by this CTA so far (stage phases)
-  int issued_g = -1;  // producer lane 0: the last k-block whose TMA part went out
+  int kb_global = 0;  // k-groups (stages) processed by this CTA so far (stage phases)
+  int issued_g = -1;  // producer lane 0: the last stage whose TMA part went out
   // no copy and no store once the CTA has given up, nor under the test hook
   auto stopped = [&]() { return cta_abort.raised() || p.wait_fault != 0; };
 
@@ -156,34 +166,41 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
                       rec[kRecordHeaderInts + BM - 1] - t_first == BM - 1 &&
                       t_first <= p.max_num_tokens - BM;
 
-    // x chunk (row, 16-byte chunk) c of k-block kb -> stage st
-    auto x_chunk = [&](int st, int kb, int c) {
-      const int row = c >> 3, ch = c & 7;
+    // x chunk (sub-block, row, 16-byte chunk) c of k-group grp -> stage st
+    auto x_chunk = [&](int st, int grp, int c) {
+      const int j = c / (BM * 8), rc = c - j * (BM * 8);
+      const int row = rc >> 3, ch = rc & 7;
       const int t = record_token(rec, row, cnt, p.max_num_tokens);
-      const int kcol = kb * kBK + ch * 8;
+      const int kcol = (grp * KS + j) * kBK + ch * 8;
       const bool ok = t >= 0 && kcol < p.hidden;
-      cp_async_16(sbase + st * p.stage_bytes + swz128(row, ch),
+      cp_async_16(sbase + st * p.stage_bytes + j * kXSub + swz128(row, ch),
                   ok ? p.x + static_cast<long long>(t) * p.x_stride + kcol : p.x, ok);
     };
-    // the TMA part of k-block kb -> stage st (one thread): the adapter blocks
-    // (stacked weights) and the x box (a run tile); with neither, a plain
+    // the TMA part of k-group grp -> stage st (one thread): the adapter blocks
+    // (stacked weights) and the x boxes (a run tile); with neither, a plain
     // arrival stands in for the transaction count
-    auto issue_a = [&](int st, int kb) {
+    auto issue_a = [&](int st, int grp) {
       if (stopped()) return;
-      issued_g = kb_global + (kb - kb0) / kstep;
+      issued_g = kb_global + (grp - kb0) / kstep;
+      const int nsub = nsub_of(grp);
       const uint32_t bar = full_bar + 8 * st;
-      const uint32_t bytes = (PAGED ? 0u : static_cast<uint32_t>(SR * 128)) +
-                             (xbox ? static_cast<uint32_t>(BM * 128) : 0u);
+      const uint32_t bytes = static_cast<uint32_t>(nsub) *
+                             ((PAGED ? 0u : static_cast<uint32_t>(SR * 128)) +
+                              (xbox ? static_cast<uint32_t>(kXSub) : 0u));
       if (bytes == 0) {
         mbar_arrive(bar);
         return;
       }
       mbar_arrive_expect_tx(bar, bytes);
       const uint32_t sx = sbase + st * p.stage_bytes;
-      if constexpr (!PAGED)
-        for (int s = 0; s < p.num_slices; ++s)
-          tma_load_2d(sx + BM * 128 + s * p.rank * 128, &p.tmap[s], kb * kBK, lora * p.rank, bar);
-      if (xbox) tma_load_2d_hint(sx, &p.xmap, kb * kBK, t_first, bar, x_pol);
+      for (int j = 0; j < nsub; ++j) {
+        const int kcol = (grp * KS + j) * kBK;
+        if constexpr (!PAGED)
+          for (int s = 0; s < p.num_slices; ++s)
+            tma_load_2d(sx + a_off + j * a_sub + s * p.rank * 128, &p.tmap[s], kcol, lora * p.rank,
+                        bar);
+        if (xbox) tma_load_2d_hint(sx + j * kXSub, &p.xmap, kcol, t_first, bar, x_pol);
+      }
     };
     auto wait_empty = [&](int g) {  // stage of global k-block g may be refilled
       const int st = g % NST, use = g / NST;
@@ -202,16 +219,19 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         if constexpr (!PAGED) {
           if (lane == 0)
             for (int i = 0; i < npro; ++i)
-              for (int s = 0; s < p.num_slices; ++s)
-                tma_prefetch_2d(&p.tmap[s], kb_of(i) * kBK, lora * p.rank);
+              for (int j = 0; j < nsub_of(kb_of(i)); ++j)
+                for (int s = 0; s < p.num_slices; ++s)
+                  tma_prefetch_2d(&p.tmap[s], (kb_of(i) * KS + j) * kBK, lora * p.rank);
         }
         if (xbox) {
           if (lane == 0)
-            for (int i = 0; i < npro; ++i) tma_prefetch_2d(&p.xmap, kb_of(i) * kBK, t_first);
+            for (int i = 0; i < npro; ++i)
+              for (int j = 0; j < nsub_of(kb_of(i)); ++j)
+                tma_prefetch_2d(&p.xmap, (kb_of(i) * KS + j) * kBK, t_first);
         } else {
-          const int kcol = kb_of(0) * kBK;
+          const int kcol = kb_of(0) * KS * kBK;
           const int r0 = split_k ? lane : crank + C * lane, rstep = split_k ? 32 : 32 * C;
-          const int bytes = min(npro * kstep * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
+          const int bytes = min(npro * kstep * KS * kBK, p.hidden - (split_k ? kcol : 0)) * 2;
           for (int r = r0; r < cnt; r += rstep) {
             const int t = record_token(rec, r, cnt, p.max_num_tokens);
             if (t >= 0)
@@ -221,7 +241,11 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         }
       }
       pdl_wait();
-      pdl_launch_dependents();
+      // k-group stages release the next kernel only once this CTA's last
+      // stage is issued (below): its CTAs, started early, would load their
+      // own inputs while this kernel streams (prefill one call 56.3 -> 48 us
+      // with four-k-block stages); single k-block stages release it here
+      if constexpr (KS == 1) pdl_launch_dependents();
       waited = true;
     }
 
@@ -235,18 +259,20 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         else if (tid == 0) atomicOr(p.status, kStatusBadWeight);
       }
     }
-    // paged weights: the adapter rows of k-block kb -> stage st by cp.async,
+    // paged weights: the adapter rows of k-group grp -> stage st by cp.async,
     // into the layout the TMA boxes would give (chunks first, first + step, ...)
-    auto a_chunks = [&](int st, int kb, int first, int step) {
-      const uint32_t sa = sbase + st * p.stage_bytes + BM * 128;
-      for (int c = first; c < SR * 8; c += step) {
-        const int row = c >> 3, ch = c & 7;
-        const int s = row >> p.rank_shift, r = row - (s << p.rank_shift);
-        const int kcol = kb * kBK + ch * 8;
-        const __nv_bfloat16* base = abase[s];
-        const bool ok = base != nullptr && kcol < p.hidden;
-        cp_async_16(sa + swz128(row, ch), ok ? base + static_cast<long long>(r) * p.hidden + kcol : p.x,
-                    ok);
+    auto a_chunks = [&](int st, int grp, int first, int step) {
+      for (int j = 0; j < nsub_of(grp); ++j) {
+        const uint32_t sa = sbase + st * p.stage_bytes + a_off + j * a_sub;
+        for (int c = first; c < SR * 8; c += step) {
+          const int row = c >> 3, ch = c & 7;
+          const int s = row >> p.rank_shift, r = row - (s << p.rank_shift);
+          const int kcol = (grp * KS + j) * kBK + ch * 8;
+          const __nv_bfloat16* base = abase[s];
+          const bool ok = base != nullptr && kcol < p.hidden;
+          cp_async_16(sa + swz128(row, ch),
+                      ok ? base + static_cast<long long>(r) * p.hidden + kcol : p.x, ok);
+        }
       }
     };
 
@@ -270,7 +296,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
     for (int i = 0; i < npro && copy; ++i) {
       const int st = (kb_global + i) % NST;
       if (!xbox)
-        for (int c = tid; c < BM * 8; c += kShrinkThreads) x_chunk(st, kb_of(i), c);
+        for (int c = tid; c < nsub_of(kb_of(i)) * BM * 8; c += kShrinkThreads)
+          x_chunk(st, kb_of(i), c);
       cp_async_mbar_arrive(full_bar + 8 * st);
     }
 
@@ -300,16 +327,25 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
           if (go) a_chunks(st, kb_of(i), lane, 32);
         if (!xbox && go) {
           const uint32_t sx = sbase + st * p.stage_bytes;
-          const int kb = kb_of(i);
-          const bool kin = kb * kBK + xch * 8 < p.hidden;
+          const int grp = kb_of(i), nsub = nsub_of(grp);
 #pragma unroll
-          for (int j = 0; j < XJ; ++j) {
-            const bool ok = xrow[j] != nullptr && kin;
-            cp_async_16(sx + swz128((lane >> 3) + 4 * j, xch), ok ? xrow[j] + kb * kBK : p.x, ok);
+          for (int jj = 0; jj < KS; ++jj) {
+            if (jj < nsub) {
+              const int kb = grp * KS + jj;
+              const bool kin = kb * kBK + xch * 8 < p.hidden;
+#pragma unroll
+              for (int j = 0; j < XJ; ++j) {
+                const bool ok = xrow[j] != nullptr && kin;
+                cp_async_16(sx + jj * kXSub + swz128((lane >> 3) + 4 * j, xch),
+                            ok ? xrow[j] + kb * kBK : p.x, ok);
+              }
+            }
           }
         }
         if (go) cp_async_mbar_arrive(full_bar + 8 * st);
       }
+      if constexpr (KS > 1)
+        if (lane == 0 && item + nclusters >= ntiles) pdl_launch_dependents();  // last issue done
     } else {
       float acc[BM / 16][NTW][4];
 #pragma unroll
@@ -323,35 +359,42 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         const int g = kb_global + i;
         const int st = g % NST;
         cta_abort.wait(full_bar + 8 * st, (g / NST) & 1);  // (after giving up: garbage in, nothing out)
-        const uint32_t sx = sbase + st * p.stage_bytes;
-        const uint32_t sw = sx + BM * 128;
+        const uint32_t stg = sbase + st * p.stage_bytes;
+        const int nsub = nsub_of(kb_of(i));
 #pragma unroll
-        for (int ks = 0; ks < kBK / 16; ++ks) {
-          if ((ks & (WK - 1)) != wk) continue;
-          uint32_t af[BM / 16][4];
+        for (int jj = 0; jj < KS; ++jj) {
+          if (jj >= nsub) break;
+          const uint32_t sx = stg + jj * kXSub;       // x rows of k-block jj of the group
+          const uint32_t sw = stg + a_off + jj * a_sub;  // its adapter rows
 #pragma unroll
-          for (int mi = 0; mi < BM / 16; ++mi)
-            ldsm_x4(af[mi], sx + swz128(mi * 16 + (lane & 15), ks * 2 + (lane >> 4)));
+          for (int ks = 0; ks < kBK / 16; ++ks) {
+            if ((ks & (WK - 1)) != wk) continue;
+            uint32_t af[BM / 16][4];
 #pragma unroll
-          for (int j = 0; j < NTW; j += 2) {
-            if (j < nt_cnt) {
-              const int n0 = (nt0 + j) * 8;
-              uint32_t bf[4];
-              if (j + 1 < nt_cnt) {
-                ldsm_x4(bf, sw + swz128(n0 + (lane & 7) + ((lane >> 4) << 3),
-                                        ks * 2 + ((lane >> 3) & 1)));
-              } else {
-                uint32_t b2[2];
-                ldsm_x2(b2, sw + swz128(n0 + (lane & 7), ks * 2 + ((lane >> 3) & 1)));
-                bf[0] = b2[0];
-                bf[1] = b2[1];
-                bf[2] = 0u;
-                bf[3] = 0u;
-              }
+            for (int mi = 0; mi < BM / 16; ++mi)
+              ldsm_x4(af[mi], sx + swz128(mi * 16 + (lane & 15), ks * 2 + (lane >> 4)));
 #pragma unroll
-              for (int mi = 0; mi < BM / 16; ++mi) {
-                mma_t<F16>(acc[mi][j], af[mi], bf[0], bf[1]);
-                if (j + 1 < NTW && j + 1 < nt_cnt) mma_t<F16>(acc[mi][j + 1], af[mi], bf[2], bf[3]);
+            for (int j = 0; j < NTW; j += 2) {
+              if (j < nt_cnt) {
+                const int n0 = (nt0 + j) * 8;
+                uint32_t bf[4];
+                if (j + 1 < nt_cnt) {
+                  ldsm_x4(bf, sw + swz128(n0 + (lane & 7) + ((lane >> 4) << 3),
+                                          ks * 2 + ((lane >> 3) & 1)));
+                } else {
+                  uint32_t b2[2];
+                  ldsm_x2(b2, sw + swz128(n0 + (lane & 7), ks * 2 + ((lane >> 3) & 1)));
+                  bf[0] = b2[0];
+                  bf[1] = b2[1];
+                  bf[2] = 0u;
+                  bf[3] = 0u;
+                }
+#pragma unroll
+                for (int mi = 0; mi < BM / 16; ++mi) {
+                  mma_t<F16>(acc[mi][j], af[mi], bf[0], bf[1]);
+                  if (j + 1 < NTW && j + 1 < nt_cnt)
+                    mma_t<F16>(acc[mi][j + 1], af[mi], bf[2], bf[3]);
+                }
               }
             }
           }
@@ -470,15 +513,15 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   }
 }
 
-template <int BM, int NTW, int NST>
+template <int BM, int NTW, int NST, int KS>
 static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStream_t stream,
                       long long max_tiles) {
   // fp16 inputs come with stacked weights only
   if (prm.paged && prm.f16) return -3;
   const void* fn =
-      prm.paged  ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, true, false>)
-      : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false, true>)
-                : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, false, false>);
+      prm.paged  ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, false>)
+      : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, true>)
+                : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, false>);
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
@@ -529,15 +572,29 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const long long max_tiles = tile_list_capacity(a.max_num_tokens, a.num_loras, tile_index_of(BM));
   const int cluster = shrink_split(a, a.partials != nullptr);
   if (a.partials != nullptr && BM != 16) return -3;
-  const int kb_per = (kblocks + cluster - 1) / cluster;
+  // k-blocks per stage: narrow adapters on 32-token tiles (prefill: S*R <=
+  // 32, 6 KB per k-block) spend more on the per-stage round trip and issue
+  // than on the bytes (a per-CTA trace: ~1100 cycles per stage, at any ring
+  // depth), so a stage takes four k-blocks there (prefill shrink 21.3 ->
+  // 18.3 us).  Not when the expand of the same call follows: its CTAs, which
+  // start beside the shrink's under programmatic launch, find no room next to
+  // the 50 KB CTAs this needs, and the one call loses more than the shrink
+  // gains (prefill 48.9 -> 54.1 us)
+  const int ks = (a.partials == nullptr && !a.expand_follows && BM == 32 && SR <= 32 &&
+                  kblocks >= 32)
+                     ? 4
+                     : 1;
+  const int kb_per = ((kblocks + ks - 1) / ks + cluster - 1) / cluster;  // stages per CTA
   // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
   // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
   // for the next kernel's CTAs to start under programmatic launch).  Up to 4
   // blocks, 4 stages hold the whole range and leave the room to the expand
   // CTAs that start under this kernel (decode layer 8.72 -> 8.49 us)
-  const int stage = (BM + SR) * 128;  // a multiple of 1024: BM and S*R are multiples of 8
+  const int stage = ks * (BM + SR) * 128;  // a multiple of 1024: BM and S*R are multiples of 8
   int nst;
-  if (kb_per <= 4 && ntw <= 8)
+  if (ks == 4)
+    nst = 2;  // two stages of up to 32 KB keep four CTAs per SM
+  else if (kb_per <= 4 && ntw <= 8)
     nst = 4;
   else if (kb_per <= 8)
     nst = (8 * stage <= 64 * 1024 && ntw <= 8) ? 8 : (4 * stage <= 96 * 1024 ? 4 : 2);
@@ -602,26 +659,28 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.bar_offset = body + record_ints(BM) * 4;
   const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8 + 16;  // + the flag
 
-  // Every (tile height, column tiles per warp, ring depth) the rules above can
-  // produce has its own instantiation; the shared-memory plan was sized for
-  // exactly that ring, so any other combination is refused, never rounded.
+  // Every (tile height, column tiles per warp, ring depth, k-blocks per stage)
+  // the rules above can produce has its own instantiation; the shared-memory
+  // plan was sized for exactly that ring, so any other combination is refused,
+  // never rounded.
   using Run = int (*)(const ShrinkParams&, int, size_t, cudaStream_t, long long);
   Run run = nullptr;
   const int ntw_t = ntw <= 4 ? 4 : (ntw <= 8 ? 8 : 12);
-  if (BM == 16 && ntw_t == 4 && nst == 8) run = run_shrink<16, 4, 8>;
-  if (BM == 16 && ntw_t == 4 && nst == 4) run = run_shrink<16, 4, 4>;
-  if (BM == 16 && ntw_t == 8 && nst == 8) run = run_shrink<16, 8, 8>;
-  if (BM == 16 && ntw_t == 8 && nst == 4) run = run_shrink<16, 8, 4>;
-  if (BM == 16 && ntw_t == 8 && nst == 2) run = run_shrink<16, 8, 2>;
-  if (BM == 16 && ntw_t == 8 && nst == 3) run = run_shrink<16, 8, 3>;
-  if (BM == 16 && ntw_t == 12 && nst == 4) run = run_shrink<16, 12, 4>;
-  if (BM == 16 && ntw_t == 12 && nst == 2) run = run_shrink<16, 12, 2>;
-  if (BM == 32 && ntw_t == 4 && nst == 8) run = run_shrink<32, 4, 8>;
-  if (BM == 32 && ntw_t == 4 && nst == 4) run = run_shrink<32, 4, 4>;
-  if (BM == 32 && ntw_t == 8 && nst == 8) run = run_shrink<32, 8, 8>;
-  if (BM == 32 && ntw_t == 8 && nst == 4) run = run_shrink<32, 8, 4>;
-  if (BM == 32 && ntw_t == 8 && nst == 2) run = run_shrink<32, 8, 2>;
-  if (BM == 32 && ntw_t == 8 && nst == 3) run = run_shrink<32, 8, 3>;
+  if (BM == 16 && ntw_t == 4 && ks == 1 && nst == 8) run = run_shrink<16, 4, 8, 1>;
+  if (BM == 16 && ntw_t == 4 && ks == 1 && nst == 4) run = run_shrink<16, 4, 4, 1>;
+  if (BM == 16 && ntw_t == 8 && ks == 1 && nst == 8) run = run_shrink<16, 8, 8, 1>;
+  if (BM == 16 && ntw_t == 8 && ks == 1 && nst == 4) run = run_shrink<16, 8, 4, 1>;
+  if (BM == 16 && ntw_t == 8 && ks == 1 && nst == 2) run = run_shrink<16, 8, 2, 1>;
+  if (BM == 16 && ntw_t == 8 && ks == 1 && nst == 3) run = run_shrink<16, 8, 3, 1>;
+  if (BM == 16 && ntw_t == 12 && ks == 1 && nst == 4) run = run_shrink<16, 12, 4, 1>;
+  if (BM == 16 && ntw_t == 12 && ks == 1 && nst == 2) run = run_shrink<16, 12, 2, 1>;
+  if (BM == 32 && ntw_t == 4 && ks == 1 && nst == 8) run = run_shrink<32, 4, 8, 1>;
+  if (BM == 32 && ntw_t == 4 && ks == 1 && nst == 4) run = run_shrink<32, 4, 4, 1>;
+  if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 8) run = run_shrink<32, 8, 8, 1>;
+  if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 4) run = run_shrink<32, 8, 4, 1>;
+  if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 2) run = run_shrink<32, 8, 2, 1>;
+  if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 3) run = run_shrink<32, 8, 3, 1>;
+  if (BM == 32 && ntw_t == 4 && ks == 4 && nst == 2) run = run_shrink<32, 4, 2, 4>;
   if (run == nullptr) return -6;
   return run(p, cluster, smem, stream, max_tiles);
 }

@@ -71,6 +71,27 @@ def test_ragged_and_edge_shapes(T, n, H, widths, L, R, kind, dev):
     check_case(case)
 
 
+# 32-token tiles of narrow adapters (S*R <= 32) over at least 32 k-blocks:
+# lora_shrink's stages hold four k-blocks each (the one call keeps stages of
+# one k-block).  A short last group and a last k-block past the hidden size
+# (2120, 3000), run tiles (one TMA box per k-block) and gathered tiles, one to
+# three slices.
+KGROUP_SHAPES = [
+    (2048, 2000, 2120, (264,), 6, 16, "runs"),
+    (4096, 3900, 4096, (512, 520), 8, 16, "runs"),
+    (1100, 1100, 2048, (256, 128, 136), 5, 8, "uniform"),
+    (1500, 1400, 3000, (1024,), 3, 32, "runs"),
+]
+
+
+@pytest.mark.parametrize("one_call", [False, True])
+@pytest.mark.parametrize("T,n,H,widths,L,R,kind", KGROUP_SHAPES)
+def test_k_group_stages_match_the_oracle(T, n, H, widths, L, R, kind, one_call, dev):
+    shape = W.custom_shape(max_num_tokens=T, num_tokens=n, hidden=H, slice_widths=widths,
+                           max_loras=L, rank=R, mapping=kind, neg_prob=0.1)
+    check_case(make_case(shape, dev, seed=T + H + R), fused=one_call)
+
+
 @pytest.mark.parametrize("R", [8, 16, 32, 64, 128])
 @pytest.mark.parametrize("S", [1, 2, 3])
 def test_every_rank_and_slice_count(R, S, dev):
@@ -143,6 +164,8 @@ INT_PATHS = [
     (64, 4096, 16, True, False, 1),       # the fused kernel, a long hidden dimension
     (64, 8200, 16, True, True, 2),        # the split-K pair
     (1100, 1032, 16, True, False, 2),     # the cluster pair (past the split-K sizes)
+    (1100, 2120, 16, False, False, None),  # shrink stages of four k-blocks, the last short
+    (1100, 2120, 16, True, False, 2),     # the cluster pair on the same shape
 ]
 
 
@@ -579,6 +602,7 @@ PAGED_SHAPES = [
     ("prefill_like_cluster", (2048, 2000, 1024, (1024,), 8, 16), False, True),
     ("rank128", (512, 500, 512, (256,), 6, 128), False, False),
     ("tiny_one_call", (64, 64, 512, (512,), 4, 8), False, True),
+    ("prefill_k_groups", (2048, 2000, 2120, (264,), 6, 16), False, False),
 ]
 
 
@@ -635,6 +659,7 @@ F16_SHAPES = [
     ("rank64_two_slices", (1024, 1000, 1024, (1032, 520), 8, 64), False, True),
     ("rank128", (512, 500, 2048, (256,), 6, 128), False, False),
     ("split_k_rank32", (1000, 977, 8264, (1032, 520, 264), 5, 32), True, True),
+    ("prefill_k_groups", (2048, 1990, 2120, (264, 136), 6, 8), False, False),
 ]
 
 
