@@ -427,7 +427,8 @@ class WorkloadRun:
 
     def launch(self, which):
         """Enqueue one step's part: metadata, layers (one call each), or the
-        one-call path's shrink / expand kernels alone (one launch per layer)."""
+        shrink / expand alone (lora_shrink / lora_expand, or the split-K pair's
+        halves where the one call takes that path; one launch per layer)."""
         m, sh, s = self.meta, self.shape, self.stream
         if which == "metadata":
             m.prepare(self.mapping, self.n_dev, s)
@@ -674,7 +675,7 @@ def run_ours(args, world, rank, local):
         with torch.cuda.stream(stream):
             for _ in range(args.steps):
                 run.launch("metadata")
-                run.launch("layers")
+                run.launch(args.profile_part)
         stream.synchronize()
         if rank == 0:
             print(json.dumps({"mode": "profile", "workload": headline, "layers": run.layers,
@@ -783,6 +784,9 @@ def parse_args(argv=None):
                     help="type of x, A, B and y (fp32 accumulation either way)")
     ap.add_argument("--mode", choices=["bench", "profile"], default="bench",
                     help="profile: only run --steps eager steps of one workload (for ncu)")
+    ap.add_argument("--profile-part", choices=["layers", "shrink", "expand"], default="layers",
+                    help="profile mode: per layer the one call (layers), or lora_shrink / "
+                         "lora_expand alone")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 0)
     return args
