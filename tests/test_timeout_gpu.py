@@ -1,7 +1,8 @@
 """The kernels' bounded waits, made to run out on purpose through the test
 hook of include/gathered_rank_gemm_testing.h (one barrier arrival too many,
 no copy issued, a 1 ms limit).  On every path (the two calls, the fused
-kernel, the split-K pair, the tcgen05 expand) the call must finish, report
+kernel, the split-K pair, the tcgen05 expand, the shrink's stages of four
+k-blocks) the call must finish, report
 LORA_STATUS_TIMEOUT, write no output, leave every guard band alone, and leave
 the GPU and the buffers fit for the next call, which must match the oracle."""
 import numpy as np
@@ -67,6 +68,10 @@ CASES = [
      binding.LORA_PATH_PAIR),
     ("tcgen05 expand", lambda d: _custom(d, 2048, 1900, 512, (1032, 520, 264), 5, 128), False,
      None),
+    # 32-token tiles of rank 16 over 34 k-blocks: lora_shrink's stages of four
+    # k-blocks, the last short
+    ("two calls, four-k-block stages", lambda d: _custom(d, 1100, 1100, 2120, (264,), 4, 16),
+     False, None),
 ]
 
 
