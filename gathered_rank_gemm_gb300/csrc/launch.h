@@ -71,7 +71,8 @@ struct ShrinkArgs {
   const uint64_t* a_tables[3] = {nullptr, nullptr, nullptr};
   bool f16 = false;  // fp16 x and A (else bf16)
   // the expand of the same call follows at once (the one-call paths): keep
-  // the shrink's CTAs small, so that the expand's start beside them
+  // the shrink's CTAs small, so that the expand's start beside them, and (in
+  // the cluster pair) prefetch the first stages into L2 before the wait
   bool expand_follows = false;
 };
 int launch_shrink(const ShrinkArgs& a, cudaStream_t stream);

@@ -20,10 +20,11 @@
 //    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
 //    mbarrier; no block-wide barrier inside the k-loop.
 // Before griddepcontrol.wait a CTA reads only its first tile record
-// (lora_prepare_metadata's output) and prefetches that tile's first adapter
-// blocks and x rows into L2; every copy into shared memory comes after it.  The C partial tiles are
-// summed in rank order through distributed shared memory (no atomics, no
-// global scratch), scaled once and stored to u.
+// (lora_prepare_metadata's output) and, in the cluster pair of the one call,
+// prefetches that tile's first adapter blocks and x rows into L2; every copy
+// into shared memory comes after it.  The C partial tiles are summed in rank
+// order through distributed shared memory (no atomics, no global scratch),
+// scaled once and stored to u.
 #include <cstring>
 
 #include "common.cuh"
@@ -71,6 +72,7 @@ struct ShrinkParams {
   // issued and the first stage's barrier is armed with one arrival too many
   unsigned long long wait_limit_ns;
   int wait_fault;
+  int prefetch;  // L2 prefetches before the dependency wait (the cluster one call)
 };
 
 template <int BM, int NTW, int NST, int KS, bool PAGED, bool F16>
@@ -215,7 +217,11 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       // the first stages' adapter blocks and of this CTA's first x columns
       // (cluster mode: the span of the first npro rounds, its rows shared out
       // between the cluster's CTAs); the copies after the wait then hit L2.
-      if (producer && npro > 0 && !p.wait_fault) {  // (the test hook issues nothing)
+      // Only in the cluster pair of the one call: elsewhere the wait returns
+      // before the prefetches land (0.5-0.9 us after them on decode) and the
+      // copies queue behind them (decode's first stage landed 2.0 instead of
+      // 1.6 us after the wait; one call 9.95 -> 9.06 us without them)
+      if (producer && npro > 0 && p.prefetch && !p.wait_fault) {  // (the test hook issues nothing)
         if constexpr (!PAGED) {
           if (lane == 0)
             for (int i = 0; i < npro; ++i)
@@ -612,6 +618,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   memset(&p, 0, sizeof(p));
   p.paged = a.a_tables[0] != nullptr;
   p.f16 = a.f16 ? 1 : 0;
+  p.prefetch = (a.expand_follows && a.partials == nullptr) ? 1 : 0;
   p.wait_fault = wait_fault() ? 1 : 0;
   p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   for (int s = 0; s < 3; ++s) {
