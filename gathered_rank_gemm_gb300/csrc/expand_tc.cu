@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* smem = smem_raw + (sbase - raw);
   const int NSB = p.nsb, NSY = p.nsy;
   const uint32_t full_b = sbase + p.off_bar;         // [NSB]: B block landed (TMA)
-  const uint32_t empty_b = full_b + 8 * NSB;         // [NSB]: B block consumed (a group's warps)
+  const uint32_t empty_b = full_b + 8 * NSB;         // [NSB]: B block consumed (the MMAs' commit)
   const uint32_t acc_full = empty_b + 8 * NSB;       // [2]: accumulator computed
   const uint32_t acc_empty = acc_full + 16;          // [2]: accumulator read (a group's warps)
   const uint32_t u_ready = acc_empty + 16;           // u tile written (1 arrival)
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < NSB; ++i) {
       // the producer's expect_tx (+ one that never comes: the test hook)
       mbar_init(full_b + 8 * i, 1 + (p.wait_fault && i == 0 ? 1 : 0));
-      mbar_init(empty_b + 8 * i, kTcGroupWarps);    // the warps of the item's group
+      mbar_init(empty_b + 8 * i, 1);                // the commit of the item's MMAs
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + 8 * i, 1);               // the MMA warp's commit
@@ -307,6 +307,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         umma_commit(acc_full + 8 * b);
+        // the B stage is free once the MMAs that read it complete, before
+        // the epilogue has read the accumulator
+        umma_commit(empty_b + 8 * si);
         flags[2] = k;
       }
       __syncwarp();
@@ -420,7 +423,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(acc_empty + 8 * b);
-          mbar_arrive(empty_b + 8 * (k % NSB));
         }
         if (i + NSY < mine) issue_y();
         prev = it;
@@ -456,7 +458,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();  // the warp's 32 row segments are updated
       if (lane == 0) {
         mbar_arrive(acc_empty + 8 * b);
-        mbar_arrive(empty_b + 8 * (k % NSB));  // the MMA on this B block is complete
       }
       // this warp's 32 row segments: 32 / CCH rows per instruction, 16 B per lane
       {
