@@ -107,6 +107,19 @@ def test_strided_rows_are_respected(dev):
     check_case(case)
 
 
+@pytest.mark.parametrize("one_call", [False, True])
+def test_strided_rows_on_run_tiles_and_k_group_stages(one_call, dev):
+    """Padded x and y rows where the shrink loads run tiles as TMA boxes of a
+    tensor map over x (its row stride is the caller's), in stages of four
+    k-blocks for lora_shrink and of one in the one call (hidden 2112: a
+    short last group)."""
+    shape = W.custom_shape(max_num_tokens=2048, num_tokens=2000, hidden=2112,
+                           slice_widths=(264,), max_loras=6, rank=16, mapping="runs",
+                           neg_prob=0.05)
+    case = make_case(shape, dev, seed=7, x_pad=40, y_pad=24)
+    check_case(case, fused=one_call)
+
+
 def test_no_tokens_changes_nothing(dev):
     shape = W.custom_shape(max_num_tokens=64, num_tokens=0, hidden=128, slice_widths=(64,),
                            max_loras=2, rank=8)
