@@ -342,6 +342,47 @@ def test_graph_captured_once_replays_new_mappings_and_n(dev):
             assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
 
 
+def test_graph_with_run_tiles_and_k_group_stages(dev):
+    """lora_shrink's four-k-block stages and run tiles (TMA boxes of x) in a
+    graph captured once: replays with new request-run mappings and new n
+    equal eager runs on separate buffers bit for bit."""
+    T, H, widths, L, R = 2048, 2112, (264,), 6, 16
+    sh = W.custom_shape(max_num_tokens=T, num_tokens=T, hidden=H, slice_widths=widths,
+                        max_loras=L, rank=R, mapping="runs", neg_prob=0.05)
+    rng = np.random.default_rng(21)
+    layer = W.make_layer(sh, rng)
+    g_case = DeviceCase(sh, W.make_mapping(sh, rng), layer, dev)
+    stream = torch.cuda.Stream()
+    y_clean = g_case.y.view.clone()
+    with torch.cuda.stream(stream):
+        g_case.prepare(stream); g_case.shrink(stream); g_case.expand(stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        g_case.prepare(stream)
+        g_case.shrink(stream)
+        g_case.expand(stream)
+    for trial, n_new in enumerate((T, 1500, 1111)):
+        m_new = W.make_mapping(W.custom_shape(max_num_tokens=T, num_tokens=n_new, hidden=8,
+                                              slice_widths=(8,), max_loras=L, rank=8,
+                                              mapping="runs", neg_prob=0.05),
+                               np.random.default_rng(200 + trial))
+        g_case.mapping.copy_(torch.from_numpy(m_new))
+        g_case.n.fill_(n_new)
+        g_case.y.view.copy_(y_clean)
+        g_case.u.view.view(torch.int32).fill_(U_SENTINEL_BITS)
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        sh2 = W.custom_shape(max_num_tokens=T, num_tokens=n_new, hidden=H, slice_widths=widths,
+                             max_loras=L, rank=R)
+        eager = DeviceCase(sh2, m_new, layer, dev)
+        eager.run()
+        assert torch.equal(g_case.sorted.view, eager.sorted.view)
+        assert torch.equal(g_case.y.view.view(torch.int16), eager.y.view.view(torch.int16))
+        assert torch.equal(g_case.u.view.view(torch.int32), eager.u.view.view(torch.int32))
+
+
 def test_down_proj_workload_inside_a_graph(dev):
     wl = W.make_workload("down_proj_graph")
     sh = wl.shape
