@@ -87,6 +87,35 @@ int occupancy_blocks(const void* func, int threads, size_t smem_bytes) {
   return n;
 }
 
+int resident_blocks(const void* func, int threads, size_t smem_bytes) {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess || fa.numRegs <= 0) return 1;
+  int regs_sm = 0, smem_sm = 0, reserved = 0, threads_sm = 0, blocks_sm = 0;
+  if (cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev) != cudaSuccess)
+    return 1;
+  // registers are allocated per warp in units of 256
+  const long long warp_regs = (static_cast<long long>(fa.numRegs) * 32 + 255) / 256 * 256;
+  const long long warps = (threads + 31) / 32;
+  const long long by_regs = regs_sm / (warp_regs * warps);
+  const long long by_smem =
+      smem_sm / (static_cast<long long>(smem_bytes) + fa.sharedSizeBytes + reserved);
+  const long long by_threads = threads_sm / threads;
+  long long n = by_regs;
+  if (by_smem < n) n = by_smem;
+  if (by_threads < n) n = by_threads;
+  if (blocks_sm < n) n = blocks_sm;
+  return n < 1 ? 1 : static_cast<int>(n);
+}
+
 int launch_raw(const void* func, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
                int cluster, void* params) {
   cudaLaunchConfig_t cfg = {};

@@ -23,6 +23,9 @@ int device_sm_count();
 
 // Resident CTAs per SM for a kernel (cached per device, kernel, block, smem).
 int occupancy_blocks(const void* func, int threads, size_t smem_bytes);
+// Resident CTAs per SM from the kernel's registers, shared memory and threads
+// alone (for kernels the occupancy calculator under-reports).
+int resident_blocks(const void* func, int threads, size_t smem_bytes);
 
 // Launches func(params) with programmatic dependent launch allowed and, when
 // cluster > 0, a 1-D thread-block cluster of that size.  Returns 0 or a

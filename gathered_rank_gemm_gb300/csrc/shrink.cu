@@ -73,9 +73,10 @@ struct ShrinkParams {
   unsigned long long wait_limit_ns;
   int wait_fault;
   int prefetch;  // L2 prefetches before the dependency wait (the cluster one call)
+  int tc;        // S*R = 128: tcgen05 MMAs into TMEM instead of mma.sync
 };
 
-template <int BM, int NTW, int NST, int KS, bool PAGED, bool F16>
+template <int BM, int NTW, int NST, int KS, bool TC, bool PAGED, bool F16>
 __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW > 8) ? 3 : 4)
     lora_shrink_kernel(const __grid_constant__ ShrinkParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -91,7 +92,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   const bool producer = warp == kConsumerWarps;
   const int SR = p.sr;
   const int NT = SR >> 3;
-  const int WK = kConsumerWarps / p.warps_n;
+  // k-split consumer warps (mma.sync); the tensor-core path accumulates in TMEM
+  const int WK = TC ? 1 : kConsumerWarps / p.warps_n;
   const int wn = warp % p.warps_n, wk = warp / p.warps_n;
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
@@ -129,20 +131,46 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   constexpr int kXSub = BM * 128;
   const int a_off = KS * kXSub, a_sub = SR * 128;
 
-  // giving up (CtaAbort): the flag after the barriers
+  // giving up (CtaAbort): the flag after the barriers; then (tensor-core
+  // path) two more barriers and the TMEM address
   const CtaAbort cta_abort{reinterpret_cast<int*>(smem + p.bar_offset + 2 * 8 * 8), p.wait_limit_ns};
+  const uint32_t acc_bar = full_bar + 2 * 8 * 8 + 16, fin_bar = acc_bar + 8;
+  uint32_t* const taddr_slot = reinterpret_cast<uint32_t*>(smem + p.bar_offset + 2 * 8 * 8 + 32);
   if (tid == 0) {
     *cta_abort.flag = 0;
     for (int s = 0; s < NST; ++s) {
       // expect_tx + one per thread (+ one that never comes: the test hook)
       mbar_init(full_bar + 8 * s, 1 + kShrinkThreads + (p.wait_fault && s == 0 ? 1 : 0));
-      mbar_init(empty_bar + 8 * s, kConsumerWarps);  // one arrival per consumer warp
+      // one arrival per consumer warp, or the commit of the stage's MMAs
+      mbar_init(empty_bar + 8 * s, TC ? 1 : kConsumerWarps);
+    }
+    if constexpr (TC) {
+      mbar_init(acc_bar, 1);  // an item's MMAs have completed
+      mbar_init(fin_bar, 1);  // every MMA of the CTA has completed (before TMEM is freed)
     }
     fence_mbar_init();
     if constexpr (!PAGED)
       for (int s = 0; s < p.num_slices; ++s) prefetch_tmap(&p.tmap[s]);
   }
   __syncthreads();
+  // tensor-core path: 32 TMEM columns hold the tile's partial product,
+  // transposed (lane r: row r of the S*R = 128 stacked adapter rows, column
+  // t: token t)
+  uint32_t taddr = 0;
+  if constexpr (TC) {
+    if (warp == 0) {
+      asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                       smem_u32(taddr_slot)),
+                   "r"(32)
+                   : "memory");
+      asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    taddr = *taddr_slot;
+  }
+  int n_acc = 0;  // tensor-core path: items whose MMAs were committed to acc_bar
 
   // the work list is metadata output: safe to read before the dependency wait
   const int ntiles = min(max(*p.num_tiles, 0), p.tile_capacity);
@@ -352,6 +380,55 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       }
       if constexpr (KS > 1)
         if (lane == 0 && item + nclusters >= ntiles) pdl_launch_dependents();  // last issue done
+    } else if constexpr (TC) {
+      // Tensor cores (S*R = 128): per stage one thread issues the k-block's
+      // four tcgen05.mma (M = 128 adapter rows, N = BM tokens, K = 16; both
+      // operands K-major in the ring's 128-byte-swizzled layout) into the
+      // TMEM accumulator and commits them to the stage's "empty" barrier
+      constexpr uint32_t kFmt = F16 ? 0u : 1u;
+      constexpr uint32_t kIdesc = (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+                                  (static_cast<uint32_t>(BM >> 3) << 17) | (8u << 24);
+      if (warp == 0) {
+        for (int i = 0; i < nkb; ++i) {
+          const int g = kb_global + i;
+          const int st = g % NST;
+          cta_abort.wait(full_bar + 8 * st, (g / NST) & 1);
+          tc_fence_after();
+          if (lane == 0 && !stopped()) {
+            // gathered rows arrive by cp.async (generic proxy); the tensor
+            // cores read through the async proxy
+            fence_proxy_async();
+            const uint32_t stg = sbase + st * p.stage_bytes;
+            const int nsub = nsub_of(kb_of(i));
+            for (int jj = 0; jj < KS; ++jj) {
+              if (jj >= nsub) break;
+              const uint32_t sx = stg + jj * kXSub, sw = stg + a_off + jj * a_sub;
+#pragma unroll
+              for (int ks = 0; ks < kBK / 16; ++ks)
+                umma_f16(taddr, umma_desc_sw128(sw + ks * 32, 16, 1024),
+                         umma_desc_sw128(sx + ks * 32, 16, 1024), kIdesc,
+                         (i | jj | ks) != 0 ? 1u : 0u);
+            }
+            umma_commit(empty_bar + 8 * st);  // the stage is free once these complete
+          }
+          __syncwarp();
+        }
+        if (lane == 0 && nkb > 0 && !stopped()) umma_commit(acc_bar);
+        __syncwarp();
+      }
+      // every consumer warp: lane r = 32 warp + lane of the accumulator holds
+      // row r of S*R for the tile's tokens (columns) -> red[token][r]
+      const bool have = nkb > 0 && cta_abort.wait(acc_bar, n_acc & 1);
+      if (nkb > 0) ++n_acc;
+      tc_fence_after();
+      named_barrier_sync(1, 32 * kConsumerWarps);  // every MMA on the ring has completed
+      float d[32];
+      tmem_ld32(taddr + (static_cast<uint32_t>(32 * warp) << 16), d);
+      tc_fence_before();
+      float* red = reinterpret_cast<float*>(smem);
+      const int r = 32 * warp + lane;
+#pragma unroll
+      for (int t = 0; t < BM; ++t) red[t * SR + r] = have ? d[t] : 0.f;
     } else {
       float acc[BM / 16][NTW][4];
 #pragma unroll
@@ -517,6 +594,20 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         mbar_drain(full_bar + 8 * (g % NST), (g / NST) & 1, p.wait_limit_ns);
     if (tid == 0) atomicOr(p.status, kStatusTimeout);
   }
+  if constexpr (TC) {
+    // the MMA thread's last commit covers every MMA it issued (also after
+    // giving up): TMEM is freed only once they have all completed
+    if (tid == 0) {
+      umma_commit(fin_bar);
+      mbar_drain(fin_bar, 0, p.wait_limit_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(32)
+                   : "memory");
+  }
 }
 
 template <int BM, int NTW, int NST, int KS>
@@ -524,14 +615,31 @@ static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStr
                       long long max_tiles) {
   // fp16 inputs come with stacked weights only
   if (prm.paged && prm.f16) return -3;
-  const void* fn =
-      prm.paged  ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, false>)
-      : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, true>)
-                : reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, false>);
+  const void* fn = nullptr;
+  if (prm.tc) {
+    // S*R = 128 (8 column tiles per warp): the tensor-core path
+    if constexpr (NTW == 8) {
+      fn = prm.paged ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, true, false>)
+           : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, false, true>)
+                     : reinterpret_cast<const void*>(
+                           lora_shrink_kernel<BM, NTW, NST, KS, true, false, false>);
+    } else {
+      return -6;
+    }
+  } else {
+    fn = prm.paged ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, true, false>)
+         : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, false, false, true>)
+                   : reinterpret_cast<const void*>(
+                         lora_shrink_kernel<BM, NTW, NST, KS, false, false, false>);
+  }
   if (ensure_smem_attr(fn, smem) != 0) return -6;
   const int sms = device_sm_count();
   if (sms <= 0) return -6;
-  int per_sm = occupancy_blocks(fn, kShrinkThreads, smem);
+  // the occupancy calculator reports one CTA per SM for the tcgen05
+  // instantiations (three fit by registers and shared memory, and run: the
+  // down_proj_graph shrink takes 73.7 us with three, 139.7 us with one)
+  int per_sm = prm.tc ? resident_blocks(fn, kShrinkThreads, smem)
+                      : occupancy_blocks(fn, kShrinkThreads, smem);
   if (per_sm < 1) per_sm = 1;
   long long grid = static_cast<long long>(sms) * per_sm / cluster * cluster;
   const long long useful = max_tiles * cluster;
@@ -619,6 +727,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.paged = a.a_tables[0] != nullptr;
   p.f16 = a.f16 ? 1 : 0;
   p.prefetch = (a.expand_follows && a.partials == nullptr) ? 1 : 0;
+  p.tc = (SR == 128 && a.partials == nullptr) ? 1 : 0;
   p.wait_fault = wait_fault() ? 1 : 0;
   p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   for (int s = 0; s < 3; ++s) {
@@ -664,7 +773,8 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   const int body = ((ring > red ? ring : red) + 127) / 128 * 128;
   p.rec_offset = body;
   p.bar_offset = body + record_ints(BM) * 4;
-  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8 + 16;  // + the flag
+  // + the flag (16 bytes), the tensor-core path's two barriers and TMEM address (32)
+  const size_t smem = 1024 + static_cast<size_t>(p.bar_offset) + 2 * 8 * 8 + 48;
 
   // Every (tile height, column tiles per warp, ring depth, k-blocks per stage)
   // the rules above can produce has its own instantiation; the shared-memory
