@@ -18,7 +18,12 @@
 //    the lanes' cp.async arrivals complete the stage's "full" mbarrier;
 //  - four consumer warps wait on "full", run the tensor-core MMAs (mma.sync
 //    m16n8k16, bf16 in, fp32 accumulate) and release the stage on its "empty"
-//    mbarrier; no block-wide barrier inside the k-loop.
+//    mbarrier; no block-wide barrier inside the k-loop.  With S*R = 128 the
+//    MMAs run on tcgen05 instead: one thread issues a k-block's four
+//    tcgen05.mma (M = the 128 stacked adapter rows, N = the tile's tokens,
+//    K = 16; both operands K-major, straight from the ring) into a TMEM
+//    accumulator and commits them to the stage's "empty" barrier, and the
+//    four warps read the accumulator (transposed) once per tile.
 // Before griddepcontrol.wait a CTA reads only its first tile record
 // (lora_prepare_metadata's output) and, in the cluster pair of the one call,
 // prefetches that tile's first adapter blocks and x rows into L2; every copy
