@@ -623,11 +623,12 @@ static int run_shrink(const ShrinkParams& prm, int cluster, size_t smem, cudaStr
   const void* fn = nullptr;
   if (prm.tc) {
     // S*R = 128 (8 column tiles per warp): the tensor-core path
+    // (stacked weights only)
     if constexpr (NTW == 8) {
-      fn = prm.paged ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, true, false>)
-           : prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, false, true>)
-                     : reinterpret_cast<const void*>(
-                           lora_shrink_kernel<BM, NTW, NST, KS, true, false, false>);
+      if (prm.paged) return -6;
+      fn = prm.f16 ? reinterpret_cast<const void*>(lora_shrink_kernel<BM, NTW, NST, KS, true, false, true>)
+                   : reinterpret_cast<const void*>(
+                         lora_shrink_kernel<BM, NTW, NST, KS, true, false, false>);
     } else {
       return -6;
     }
@@ -732,7 +733,10 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   p.paged = a.a_tables[0] != nullptr;
   p.f16 = a.f16 ? 1 : 0;
   p.prefetch = (a.expand_follows && a.partials == nullptr) ? 1 : 0;
-  p.tc = (SR == 128 && a.partials == nullptr) ? 1 : 0;
+  // the tensor-core path for S*R = 128 with stacked weights; paged weights
+  // (adapter rows gathered by cp.async) keep the mma.sync consumers, which
+  // were faster there (down_proj_graph paged shrink 160.6 vs 281.9 us)
+  p.tc = (SR == 128 && a.partials == nullptr && !p.paged) ? 1 : 0;
   p.wait_fault = wait_fault() ? 1 : 0;
   p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   for (int s = 0; s < 3; ++s) {
