@@ -102,9 +102,10 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
   const int wn = warp % p.warps_n, wk = warp / p.warps_n;
   const int nt0 = wn * p.ntw;
   const int nt_cnt = min(p.ntw, NT - nt0);
-  // k-groups serve narrow adapters only (S*R <= 32: one column warp group,
-  // WK = 4), so warp wk takes k-step wk of every k-block
-  constexpr bool kOneStep = !TC && KS > 1;
+  // at most four n8 column tiles per warp means one column warp group (more
+  // than four tiles are split over two or four column groups only from nine
+  // tiles up), so WK = 4 and warp wk takes k-step wk of every k-block
+  constexpr bool kOneStep = !TC && NTW <= 4;
 
   // x is read once: a run tile's TMA box of x loads under an L2 evict-first
   // policy, leaving the L2 to the adapter blocks every tile of a LoRA re-reads
@@ -708,7 +709,6 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
                   kblocks >= 32)
                      ? 4
                      : 1;
-  if (ks > 1 && WK != kConsumerWarps) return -6;  // the k-group consumers take one k-step each
   const int kb_per = ((kblocks + ks - 1) / ks + cluster - 1) / cluster;  // stages per CTA
   // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
   // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
@@ -797,6 +797,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   using Run = int (*)(const ShrinkParams&, int, size_t, cudaStream_t, long long);
   Run run = nullptr;
   const int ntw_t = ntw <= 4 ? 4 : (ntw <= 8 ? 8 : 12);
+  if (ntw_t <= 4 && WK != kConsumerWarps) return -6;  // those kernels take one k-step per warp
   if (BM == 16 && ntw_t == 4 && ks == 1 && nst == 8) run = run_shrink<16, 4, 8, 1>;
   if (BM == 16 && ntw_t == 4 && ks == 1 && nst == 4) run = run_shrink<16, 4, 4, 1>;
   if (BM == 16 && ntw_t == 8 && ks == 1 && nst == 8) run = run_shrink<16, 8, 8, 1>;
@@ -812,9 +813,10 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 2) run = run_shrink<32, 8, 2, 1>;
   if (BM == 32 && ntw_t == 8 && ks == 1 && nst == 3) run = run_shrink<32, 8, 3, 1>;
   if (BM == 32 && ntw_t == 4 && ks == 4 && nst == 2) run = run_shrink<32, 4, 2, 4>;
-  // one or two column tiles (S*R <= 16) in k-groups: the accumulators of two
-  // tiles only (prefill shrink 16.7 -> 16.5 us)
+  // one or two column tiles (S*R <= 16) on 32-token tiles: the accumulators
+  // of two tiles only (prefill lora_shrink 16.7 -> 16.5 us)
   if (BM == 32 && ntw <= 2 && ks == 4 && nst == 2) run = run_shrink<32, 2, 2, 4>;
+  if (BM == 32 && ntw <= 2 && ks == 1 && nst == 4) run = run_shrink<32, 2, 4, 1>;
   if (run == nullptr) return -6;
   return run(p, cluster, smem, stream, max_tiles);
 }
