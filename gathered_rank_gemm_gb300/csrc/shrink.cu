@@ -79,6 +79,9 @@ struct ShrinkParams {
   int wait_fault;
   int prefetch;  // L2 prefetches before the dependency wait (the cluster one call)
   int tc;        // S*R = 128: tcgen05 MMAs into TMEM instead of mma.sync
+  // k-groups in the one call: the expand is released only when this grid ends
+  // (no explicit trigger), not once the last stage is issued
+  int release_at_exit;
 };
 
 template <int BM, int NTW, int NST, int KS, bool TC, bool PAGED, bool F16>
@@ -285,9 +288,10 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
       }
       pdl_wait();
       // k-group stages release the next kernel only once this CTA's last
-      // stage is issued (below): its CTAs, started early, would load their
-      // own inputs while this kernel streams (prefill one call 56.3 -> 48 us
-      // with four-k-block stages); single k-block stages release it here
+      // stage is issued (below), or in the one call only at the grid's end:
+      // its CTAs, started early, would load their own inputs while this
+      // kernel streams (prefill one call 56.3 -> 48 us with four-k-block
+      // stages); single k-block stages release it here
       if constexpr (KS == 1) pdl_launch_dependents();
       waited = true;
     }
@@ -388,7 +392,8 @@ __global__ void __launch_bounds__(kShrinkThreads, ((BM == 32 && NTW > 4) || NTW 
         if (go) cp_async_mbar_arrive(full_bar + 8 * st);
       }
       if constexpr (KS > 1)
-        if (lane == 0 && item + nclusters >= ntiles) pdl_launch_dependents();  // last issue done
+        if (lane == 0 && item + nclusters >= ntiles && !p.release_at_exit)
+          pdl_launch_dependents();  // last issue done
     } else if constexpr (TC) {
       // Tensor cores (S*R = 128): per stage one thread issues the k-block's
       // four tcgen05.mma (M = 128 adapter rows, N = BM tokens, K = 16; both
@@ -701,14 +706,12 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   // 32, 6 KB per k-block) spend more on the per-stage round trip and issue
   // than on the bytes (a per-CTA trace: ~1100 cycles per stage, at any ring
   // depth), so a stage takes four k-blocks there (prefill shrink 21.3 ->
-  // 18.3 us).  Not when the expand of the same call follows: its CTAs, which
-  // start beside the shrink's under programmatic launch, find no room next to
-  // the 50 KB CTAs this needs, and the one call loses more than the shrink
-  // gains (prefill 48.9 -> 54.1 us)
-  const int ks = (a.partials == nullptr && !a.expand_follows && BM == 32 && SR <= 32 &&
-                  kblocks >= 32)
-                     ? 4
-                     : 1;
+  // 18.3 us).  In the one call the expand's CTAs, which would start beside the
+  // shrink's under programmatic launch, find no room next to the 50 KB CTAs
+  // this needs (some started only as others finished: prefill one call 48.9
+  // -> 54.1 us), so there the expand is released only when the shrink's grid
+  // ends (one call 47.9 -> 46.9 us against one-k-block stages)
+  const int ks = (a.partials == nullptr && BM == 32 && SR <= 32 && kblocks >= 32) ? 4 : 1;
   const int kb_per = ((kblocks + ks - 1) / ks + cluster - 1) / cluster;  // stages per CTA
   // Ring depth: a short k-range (up to 8 blocks) keeps all of it in flight;
   // long ranges prefer occupancy (smaller rings, more CTAs per SM, and room
@@ -743,6 +746,7 @@ int launch_shrink(const ShrinkArgs& a, cudaStream_t stream) {
   // were faster there (down_proj_graph paged shrink 160.6 vs 281.9 us)
   p.tc = (SR == 128 && a.partials == nullptr && !p.paged) ? 1 : 0;
   p.wait_fault = wait_fault() ? 1 : 0;
+  p.release_at_exit = (ks > 1 && a.expand_follows) ? 1 : 0;
   p.wait_limit_ns = p.wait_fault ? kTestWaitLimitNs : kWaitLimitNs;
   for (int s = 0; s < 3; ++s) {
     p.a_tab[s] = s < a.num_slices ? a.a_tables[s] : a.a_tables[0];

@@ -72,10 +72,10 @@ def test_ragged_and_edge_shapes(T, n, H, widths, L, R, kind, dev):
 
 
 # 32-token tiles of narrow adapters (S*R <= 32) over at least 32 k-blocks:
-# lora_shrink's stages hold four k-blocks each (the one call keeps stages of
-# one k-block).  A short last group and a last k-block past the hidden size
-# (2120, 3000), run tiles (one TMA box per k-block) and gathered tiles, one to
-# three slices.
+# the shrink's stages hold four k-blocks each, in lora_shrink and in the one
+# call (whose expand then starts at the shrink's end).  A short last group
+# and a last k-block past the hidden size (2120, 3000), run tiles (one TMA box
+# per k-block) and gathered tiles, one to three slices.
 KGROUP_SHAPES = [
     (2048, 2000, 2120, (264,), 6, 16, "runs"),
     (4096, 3900, 4096, (512, 520), 8, 16, "runs"),

@@ -68,10 +68,12 @@ CASES = [
      binding.LORA_PATH_PAIR),
     ("tcgen05 expand", lambda d: _custom(d, 2048, 1900, 512, (1032, 520, 264), 5, 128), False,
      None),
-    # 32-token tiles of rank 16 over 34 k-blocks: lora_shrink's stages of four
-    # k-blocks, the last short
+    # 32-token tiles of rank 16 over 34 k-blocks: stages of four k-blocks, the
+    # last short (lora_shrink, and the shrink of the cluster pair)
     ("two calls, four-k-block stages", lambda d: _custom(d, 1100, 1100, 2120, (264,), 4, 16),
      False, None),
+    ("cluster pair, four-k-block stages",
+     lambda d: _custom(d, 1100, 1100, 2120, (264,), 4, 16), True, binding.LORA_PATH_PAIR),
 ]
 
 
