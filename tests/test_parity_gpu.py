@@ -81,6 +81,12 @@ KGROUP_SHAPES = [
     (4096, 3900, 4096, (512, 520), 8, 16, "runs"),
     (1100, 1100, 2048, (256, 128, 136), 5, 8, "uniform"),
     (1500, 1400, 3000, (1024,), 3, 32, "runs"),
+    # one column tile (S*R = 8) in the two-tile kernel
+    (1536, 1500, 2048, (512,), 4, 8, "runs"),
+    # 24 k-blocks over clusters of two (enough tiles for three CTAs per SM):
+    # twelve one-k-block stages per CTA in the two-tile kernel, S*R = 16 and 8
+    (8192, 8000, 1536, (512,), 8, 16, "runs"),
+    (8192, 7900, 1536, (256,), 6, 8, "uniform"),
 ]
 
 
