@@ -663,6 +663,7 @@ PAGED_SHAPES = [
     ("rank128", (512, 500, 512, (256,), 6, 128), False, False),
     ("tiny_one_call", (64, 64, 512, (512,), 4, 8), False, True),
     ("prefill_k_groups", (2048, 2000, 2120, (264,), 6, 16), False, False),
+    ("prefill_k_groups_one_call", (2048, 2000, 2120, (264,), 6, 16), False, True),
 ]
 
 
@@ -720,6 +721,7 @@ F16_SHAPES = [
     ("rank128", (512, 500, 2048, (256,), 6, 128), False, False),
     ("split_k_rank32", (1000, 977, 8264, (1032, 520, 264), 5, 32), True, True),
     ("prefill_k_groups", (2048, 1990, 2120, (264, 136), 6, 8), False, False),
+    ("prefill_k_groups_one_call", (2048, 1990, 2120, (264, 136), 6, 8), False, True),
 ]
 
 
